@@ -1,0 +1,146 @@
+"""Gated linear attention (GLA) on one NVIDIA GB300 (sm_103a).
+
+Python face of ``libgla.so`` (C ABI in ``include/gla.h``).  PyTorch supplies
+device memory and streams only; every step of the computation runs in the
+library's CUDA kernels, and a missing library is an error, never a fallback.
+
+    out, final = chunk_fwd(q, k, v, g, init_state=S0)          # prefill
+    out = decode_step(q, k, v, g, state)                         # one token, in place
+
+The recurrence (the "i14 Laplace 3B on AWS Trainium2" page, paragraph "GLA
+mixer"): ``S_t = diag(exp g_t) S_{t-1} + k_t^T v_t``, ``o_t = scale q_t S_t``.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _binding
+from ._binding import (GLA_FLAG_FP32_IO, GLA_FLAG_FP32_OUT, GLA_FLAG_VECTOR_GATE,  # noqa: F401
+                       GlaError, lib, status_string, version)
+
+__all__ = ["chunk_fwd", "decode_step", "status_sync", "GlaError", "lib", "version",
+           "GLA_FLAG_FP32_IO", "GLA_FLAG_FP32_OUT", "GLA_FLAG_VECTOR_GATE"]
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _out_dtype(q: torch.Tensor, out, out_dtype):
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype is None:
+        out_dtype = q.dtype
+    _check(out_dtype == q.dtype or (q.dtype == torch.bfloat16 and out_dtype == torch.float32),
+           "out is q's dtype, or fp32 for bf16 inputs")
+    return out_dtype
+
+
+def _io_flags(q: torch.Tensor, g: torch.Tensor, gate_shape_scalar, gate_shape_vector,
+              out_dtype) -> int:
+    _check(q.dtype in (torch.bfloat16, torch.float32), "q/k/v must be bf16 or fp32")
+    flags = GLA_FLAG_FP32_IO if q.dtype == torch.float32 else 0
+    if q.dtype == torch.bfloat16 and out_dtype == torch.float32:
+        flags |= GLA_FLAG_FP32_OUT
+    _check(g.dtype == torch.float32, "g must be fp32")
+    if tuple(g.shape) == tuple(gate_shape_vector):
+        flags |= GLA_FLAG_VECTOR_GATE
+    else:
+        _check(tuple(g.shape) == tuple(gate_shape_scalar),
+               f"g must be {tuple(gate_shape_scalar)} or {tuple(gate_shape_vector)}")
+    return flags
+
+
+def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seqlens=None,
+              chunk: int = 128, out=None, final_state=None, output_final_state: bool = True,
+              stream=None, out_dtype=None):
+    """Chunked GLA prefill; returns ``(out, final_state)``.
+
+    Dense: ``q, k [B, T, H, dk]``, ``v [B, T, H, dv]``, ``g [B, T, H]`` or
+    ``[B, T, H, dk]`` (fp32).  Packed: ``q, k [1, R, H, dk]`` (or ``[R, H, dk]``)
+    with ``cu_seqlens`` int32 ``[B+1]`` on the device.  ``init_state`` and the
+    returned ``final_state`` are fp32 ``[B, H, dk, dv]``.  ``out`` has q's dtype,
+    or fp32 (``out_dtype=torch.float32``) for bf16 inputs.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _check(k.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype,
+           "k must match q; v must have q's dtype")
+    H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    _check(v.shape[:-1] == q.shape[:-1], "v must be [..., H, dv] with q's leading dims")
+    if cu_seqlens is not None:
+        _check(cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32,
+               "cu_seqlens must be int32 on the GPU")
+        B = cu_seqlens.numel() - 1
+        T = q.numel() // (H * dk)
+        _check(q.dim() == 3 or (q.dim() == 4 and q.shape[0] == 1),
+               "packed inputs are [1, R, H, d] or [R, H, d]")
+    else:
+        _check(q.dim() == 4, "dense inputs are [B, T, H, d]")
+        B, T = q.shape[0], q.shape[1]
+    out_dtype = _out_dtype(q, out, out_dtype)
+    flags = _io_flags(q, g, q.shape[:-1], q.shape, out_dtype)
+    if scale is None:
+        scale = dk ** -0.5
+    if init_state is not None:
+        _check(init_state.is_cuda and init_state.dtype == torch.float32 and
+               init_state.is_contiguous() and tuple(init_state.shape) == (B, H, dk, dv),
+               f"init_state must be contiguous fp32 [{B}, {H}, {dk}, {dv}]")
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    rc = _binding.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state),
+                                _ptr(out), _ptr(final_state), _ptr(cu_seqlens), B, H, T, dk,
+                                dv, chunk, _stream(stream), flags)
+    if rc != 0:
+        raise GlaError(rc, "gla_chunk_fwd")
+    return out, final_state
+
+
+def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stream=None,
+                out_dtype=None):
+    """One recurrent step for N sequences; ``state [N, H, dk, dv]`` (fp32) is
+    updated in place.  ``q, k [N, H, dk]``, ``v [N, H, dv]``, ``g [N, H]`` or
+    ``[N, H, dk]``.  Returns ``out [N, H, dv]`` in q's dtype (or fp32)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("state", state)):
+        _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _check(q.dim() == 3 and k.shape == q.shape and v.shape[:-1] == q.shape[:-1],
+           "q, k are [N, H, dk] and v is [N, H, dv]")
+    _check(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v share one dtype")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(state.dtype == torch.float32 and tuple(state.shape) == (N, H, dk, dv),
+           f"state must be fp32 [{N}, {H}, {dk}, {dv}]")
+    out_dtype = _out_dtype(q, out, out_dtype)
+    flags = _io_flags(q, g, (N, H), (N, H, dk), out_dtype)
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=out_dtype, device=q.device)
+    rc = _binding.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(state),
+                                  _ptr(out), N, H, dk, dv, _stream(stream), flags)
+    if rc != 0:
+        raise GlaError(rc, "gla_decode_step")
+    return out
+
+
+def status_sync(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status; raises on error."""
+    rc = _binding.gla_status_sync(_stream(stream))
+    if rc != 0:
+        raise GlaError(rc, "gla_status_sync")
+    return rc

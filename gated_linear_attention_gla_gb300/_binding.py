@@ -1,0 +1,94 @@
+"""ctypes binding of libgla.so -- argument marshalling only.
+
+Every call goes straight to the C ABI declared in ``include/gla.h``; all
+arithmetic runs in the library's CUDA kernels.  If the library is missing the
+first call raises: there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgla.so")
+
+GLA_OK = 0
+GLA_ERR_INVALID_ARG = 1
+GLA_ERR_UNSUPPORTED = 2
+GLA_ERR_MISALIGNED = 3
+GLA_ERR_CUDA = 4
+GLA_ERR_TIMEOUT = 5
+
+GLA_FLAG_FP32_IO = 1 << 0
+GLA_FLAG_VECTOR_GATE = 1 << 1
+GLA_FLAG_FP32_OUT = 1 << 2
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+class GlaError(RuntimeError):
+    """A libgla call returned a non-OK status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgla.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m gated_linear_attention_gla_gb300.build` "
+                    "(or __graft_entry__.build()); there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            L.gla_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp,
+                                        _i, _i, _i, _i, _i, _i, _vp, ctypes.c_uint]
+            L.gla_chunk_fwd.restype = _i
+            L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
+                                          _i, _i, _i, _i, _vp, ctypes.c_uint]
+            L.gla_decode_step.restype = _i
+            L.gla_status_string.argtypes = [_i]
+            L.gla_status_string.restype = ctypes.c_char_p
+            L.gla_status_sync.argtypes = [_vp]
+            L.gla_status_sync.restype = _i
+            L.gla_version.argtypes = []
+            L.gla_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gla_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().gla_version().decode()
+
+
+def gla_chunk_fwd(q, k, v, g, scale, init_state, out, final_state, cu_seqlens, B, H, T, dk,
+                  dv, chunk, stream, flags) -> int:
+    """Raw call: pointers are ints (0 = NULL), ``stream`` an int handle."""
+    return lib().gla_chunk_fwd(q or None, k or None, v or None, g or None, float(scale),
+                               init_state or None, out or None, final_state or None,
+                               cu_seqlens or None, B, H, T, dk, dv, chunk, stream or None,
+                               flags)
+
+
+def gla_decode_step(q, k, v, g, scale, state_inout, out, N, H, dk, dv, stream, flags) -> int:
+    """Raw call: pointers are ints, ``stream`` an int handle."""
+    return lib().gla_decode_step(q or None, k or None, v or None, g or None, float(scale),
+                                 state_inout or None, out or None, N, H, dk, dv,
+                                 stream or None, flags)
+
+
+def gla_status_sync(stream) -> int:
+    return lib().gla_status_sync(stream or None)

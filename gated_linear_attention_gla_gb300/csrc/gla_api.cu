@@ -1,0 +1,195 @@
+// gla_api.cu -- the C ABI of libgla.so: argument checks, dispatch, status word.
+//
+// Every check below runs on the host before anything is enqueued, so a call
+// that returns an error has launched nothing.  Only cu_seqlens (a device
+// array) is checked on the device; see seq_bounds() in gla_internal.cuh.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gla.h"
+#include "gla_internal.cuh"
+
+namespace {
+
+// One status word per GPU.  It is a static __device__ variable, so the library
+// allocates nothing; kernels receive its address as a parameter.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+unsigned* g_status_ptr[kMaxDevices] = {};
+
+// Address of the current GPU's status word (nullptr and *err set on failure).
+unsigned* status_word(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_status_word);
+    if (*err != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned(const void* p, uintptr_t bytes) {
+  return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+
+bool head_size_ok(int d) { return d == 64 || d == 128; }
+
+bool flags_ok(unsigned flags) {
+  return (flags & ~(GLA_FLAG_FP32_IO | GLA_FLAG_VECTOR_GATE | GLA_FLAG_FP32_OUT)) == 0u;
+}
+
+// [a, a + na) and [b, b + nb) overlap (byte ranges).
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+constexpr long long kMaxElems = 1ll << 40;  // per tensor; keeps index arithmetic exact
+
+}  // namespace
+
+extern "C" {
+
+const char* gla_version(void) { return "0.1.0"; }
+
+const char* gla_status_string(gla_status status) {
+  switch (status) {
+    case GLA_OK: return "ok";
+    case GLA_ERR_INVALID_ARG: return "invalid argument";
+    case GLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GLA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case GLA_ERR_CUDA: return "CUDA error";
+    case GLA_ERR_TIMEOUT: return "on-device wait timed out";
+  }
+  return "unknown status";
+}
+
+gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         float scale, const float* init_state, void* out,
+                         float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                         int dk, int dv, int chunk, gla_stream_t stream, unsigned flags) {
+  if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
+    return GLA_ERR_INVALID_ARG;
+  if (!head_size_ok(dk) || !head_size_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
+  const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
+  const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
+  const bool vec = (flags & GLA_FLAG_VECTOR_GATE) != 0;
+  if (B == 0 || H == 0) return GLA_OK;
+
+  const long long rows = cu_seqlens ? (long long)T : (long long)B * T;
+  const long long esz = fp32 ? 4 : 2;
+  const long long osz = f32out ? 4 : 2;
+  const long long qk_elems = rows * H * dk, v_elems = rows * H * dv;
+  const long long st_elems = (long long)B * H * dk * dv;
+  if (qk_elems > kMaxElems || v_elems > kMaxElems || st_elems > kMaxElems)
+    return GLA_ERR_INVALID_ARG;
+  if ((long long)B * H * (dv / 64) > 0x7fffffffll) return GLA_ERR_INVALID_ARG;
+
+  if (rows > 0 && (!q || !k || !v || !g || !out)) return GLA_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr && B > 0 && T == 0 && final_state == nullptr) return GLA_OK;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(init_state, 16) || !aligned(final_state, 16) ||
+      !aligned(g, vec ? 16 : 4) || !aligned(cu_seqlens, 4))
+    return GLA_ERR_MISALIGNED;
+  // out must not overlap any input; final_state may equal init_state exactly.
+  const size_t out_b = (size_t)(v_elems * osz);
+  const size_t v_b = (size_t)(v_elems * esz);
+  const size_t qk_b = (size_t)(qk_elems * esz);
+  const size_t g_b = (size_t)(rows * H * (vec ? dk : 1) * 4);
+  const size_t st_b = (size_t)(st_elems * 4);
+  if (overlap(out, out_b, q, qk_b) || overlap(out, out_b, k, qk_b) ||
+      overlap(out, out_b, v, v_b) || overlap(out, out_b, g, g_b) ||
+      overlap(out, out_b, init_state, st_b) || overlap(out, out_b, final_state, st_b))
+    return GLA_ERR_INVALID_ARG;
+  if (final_state != init_state && overlap(final_state, st_b, init_state, st_b))
+    return GLA_ERR_INVALID_ARG;
+  if (overlap(final_state, st_b, q, qk_b) || overlap(final_state, st_b, k, qk_b) ||
+      overlap(final_state, st_b, v, v_b) || overlap(final_state, st_b, g, g_b))
+    return GLA_ERR_INVALID_ARG;
+
+  cudaError_t err;
+  unsigned* status = status_word(&err);
+  if (!status) return GLA_ERR_CUDA;
+
+  gla::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
+  a.init_state = init_state; a.out = out; a.final_state = final_state;
+  a.cu_seqlens = cu_seqlens;
+  a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec; a.status = status;
+
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!fp32 && chunk == 128 && rows > 0 && gla::chunk_tc_supported(a))
+    err = gla::launch_chunk_tc(a, s);
+  else
+    err = gla::launch_chunk_simt(a, s);
+  return err == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           float scale, float* state_inout, void* out, int N, int H, int dk,
+                           int dv, gla_stream_t stream, unsigned flags) {
+  if (!flags_ok(flags) || N < 0 || H < 0 || !std::isfinite(scale)) return GLA_ERR_INVALID_ARG;
+  if (!head_size_ok(dk) || !head_size_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (N == 0 || H == 0) return GLA_OK;
+  const long long units = (long long)N * H;
+  if (units > 0x7fffffffll || units * dk * dv > kMaxElems) return GLA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !g || !state_inout || !out) return GLA_ERR_INVALID_ARG;
+  const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
+  const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
+  const bool vec = (flags & GLA_FLAG_VECTOR_GATE) != 0;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(state_inout, 16) || !aligned(g, 4))
+    return GLA_ERR_MISALIGNED;
+  const long long esz = fp32 ? 4 : 2;
+  const size_t st_b = (size_t)(units * dk * dv * 4);
+  const size_t out_b = (size_t)(units * dv * (f32out ? 4 : 2));
+  const size_t v_b = (size_t)(units * dv * esz);
+  const size_t qk_b = (size_t)(units * dk * esz);
+  const size_t g_b = (size_t)(units * (vec ? dk : 1) * 4);
+  if (overlap(out, out_b, state_inout, st_b) || overlap(out, out_b, q, qk_b) ||
+      overlap(out, out_b, k, qk_b) || overlap(out, out_b, v, v_b) ||
+      overlap(out, out_b, g, g_b) || overlap(state_inout, st_b, q, qk_b) ||
+      overlap(state_inout, st_b, k, qk_b) || overlap(state_inout, st_b, v, v_b) ||
+      overlap(state_inout, st_b, g, g_b))
+    return GLA_ERR_INVALID_ARG;
+
+  gla::DecodeArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
+  a.state = state_inout; a.out = out;
+  a.N = N; a.H = H; a.dk = dk; a.dv = dv;
+  a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec;
+  const cudaError_t err = gla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_status_sync(gla_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GLA_ERR_CUDA;
+  cudaError_t err;
+  unsigned* p = status_word(&err);
+  if (!p) return GLA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GLA_ERR_CUDA;
+  if (word != 0 && cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) return GLA_ERR_CUDA;
+  if (word & gla::kDevTimeout) return GLA_ERR_TIMEOUT;
+  if (word & gla::kDevBadSeqlens) return GLA_ERR_INVALID_ARG;
+  return GLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// gla_internal.cuh -- declarations shared by the translation units of libgla.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gla {
+
+// Bits of the per-GPU device status word (see gla_status_sync in gla.h).
+enum : unsigned {
+  kDevBadSeqlens = 1u << 0,  // a cu_seqlens entry was out of order or out of range
+  kDevTimeout = 1u << 1,     // a bounded mbarrier wait gave up
+};
+
+// Log-decays below -kGateClamp are raised to it before in-chunk cumulative
+// sums, so that differences of sums stay finite (exp(-30) ~ 9.4e-14).
+constexpr float kGateClamp = 30.0f;
+
+struct ChunkArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  float scale;
+  const float* init_state;
+  void* out;
+  float* final_state;
+  const int32_t* cu_seqlens;
+  int B, H, T, dk, dv, chunk;
+  bool fp32_io;      // q, k, v (and out) fp32
+  bool fp32_out;     // out fp32 with bf16 q, k, v
+  bool vector_gate;
+  unsigned* status;  // device status word
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  float scale;
+  float* state;
+  void* out;
+  int N, H, dk, dv;
+  bool fp32_io;
+  bool fp32_out;
+  bool vector_gate;
+};
+
+// Kernel launchers (one per translation unit).  They assume validated arguments
+// and a non-empty problem, and return the launch error.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
+bool chunk_tc_supported(const ChunkArgs& a);
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_state_copy(const ChunkArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Small device helpers shared by the kernels.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Sequence bounds for sequence s: dense batches own rows [s*T, s*T+T); packed
+// batches read cu_seqlens.  Returns false (and flags the status word) for a
+// malformed entry.
+__device__ __forceinline__ bool seq_bounds(const int32_t* cu, int s, int B, int T,
+                                           long long* start, int* len, unsigned* status) {
+  if (cu == nullptr) {
+    *start = (long long)s * T;
+    *len = T;
+    return true;
+  }
+  const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
+  const int first = __ldg(cu), last = __ldg(cu + B);
+  if (first != 0 || last != T || a < 0 || b < a || b > T) {
+    if (status) atomicOr(status, kDevBadSeqlens);
+    return false;
+  }
+  *start = a;
+  *len = b - a;
+  return true;
+}
+
+}  // namespace gla

@@ -1,0 +1,161 @@
+/*
+ * gla.h -- C ABI of libgla.so: gated linear attention (GLA) on one NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The method (the "i14 Laplace 3B on AWS Trainium2" blog page, section
+ * "i14 and the Laplace 3B architecture", paragraph "GLA mixer"): every head
+ * keeps a dk x dv matrix state S that decays and absorbs one rank-1
+ * key/value write per token, and the query reads the state after the write:
+ *
+ *     S_t = diag(exp g_t) S_{t-1} + k_t^T v_t
+ *     o_t = scale * q_t S_t
+ *
+ * g_t is a log-decay, either one value per (token, head) -- the page's
+ * "Simple GLA" with a per-head decay -- or one value per (token, head, key
+ * channel), where row i of S decays by exp(g_t[i]).
+ *
+ * Two serving forms are exported:
+ *   gla_chunk_fwd    prefill: the chunked form of the same page's section
+ *                    "Challenge 1" (Figure 3) -- per chunk a decay-masked
+ *                    causal Q K^T then V, plus the running state's share,
+ *                    then one state step with the decay compounded over the
+ *                    chunk; emits the final state.
+ *   gla_decode_step  one token for each of N concurrent sequences, each with a
+ *                    fixed-size state page updated in place (section
+ *                    "Inference optimization on Trainium2": one fixed page per
+ *                    sequence).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees them; it keeps only one device status word per
+ *     GPU (a static __device__ variable) and no other state.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Host-side
+ *     argument checks happen before anything is enqueued: a call that returns
+ *     an error has launched nothing and written nothing.
+ *   - Layouts are dense, row-major, token-major ("[B, T, H, d]": d fastest).
+ *   - bf16 is IEEE-style bfloat16 (1-8-7); outputs are rounded to nearest even
+ *     from fp32.  States are always fp32.  Accumulation is fp32.
+ *   - Errors detected on the device (a malformed cu_seqlens, an internal wait
+ *     that ran out) set bits in the status word; the affected (sequence, head)
+ *     writes nothing.  gla_status_sync() reports and clears them.
+ *   - Thread safety: calls may come from any host thread; the device status
+ *     word is shared by all streams of a GPU.
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *gla_stream_t;
+
+typedef enum gla_status {
+    GLA_OK = 0,
+    GLA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad flags, bad cu_seqlens */
+    GLA_ERR_UNSUPPORTED = 2,  /* valid but not implemented: head size, chunk size */
+    GLA_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned */
+    GLA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    GLA_ERR_TIMEOUT = 5       /* a bounded on-device wait gave up (reported by gla_status_sync) */
+} gla_status;
+
+/* flags */
+#define GLA_FLAG_FP32_IO (1u << 0)     /* q, k, v and out are fp32 (default bf16) */
+#define GLA_FLAG_VECTOR_GATE (1u << 1) /* g has one value per key channel (default per head) */
+#define GLA_FLAG_FP32_OUT (1u << 2)    /* out is fp32 while q, k, v stay bf16; the bf16 output of
+                                          the same call is exactly this result rounded to
+                                          nearest-even (same kernels, only the store differs) */
+
+/*
+ * gla_chunk_fwd -- chunked prefill over a batch of sequences.
+ *
+ * Source: "i14 Laplace 3B" page, section "Challenge 1: Using native PyTorch
+ * on Trainium for GLA" (chunked intra-chunk output, chunked state update,
+ * Figure 3), with the recurrence of the "GLA mixer" paragraph.  Chunks start
+ * at each sequence start; the last chunk of a sequence may be partial.  The
+ * chunk size changes only the rounding, not the result.
+ *
+ * Arguments
+ *   q, k        [B, T, H, dk] (dense) or [R, H, dk] (packed), bf16 or fp32
+ *   v           [B, T, H, dv] or [R, H, dv], same dtype as q
+ *   g           fp32 log-decay, [B, T, H] / [R, H], or with
+ *               GLA_FLAG_VECTOR_GATE [B, T, H, dk] / [R, H, dk].  Values must be
+ *               <= 0 or -inf; values below -30 act as -30 (exp(-30) ~ 1e-13).
+ *   scale       readout scale (finite), usually dk^-0.5
+ *   init_state  fp32 [B, H, dk, dv] state before the first token, or NULL (zeros)
+ *   out         [B, T, H, dv] / [R, H, dv], same dtype as q (fp32 with
+ *               GLA_FLAG_FP32_OUT); must not overlap any input
+ *   final_state fp32 [B, H, dk, dv] state after the last token, or NULL (not
+ *               written).  May alias init_state exactly (in-place update).
+ *   cu_seqlens  NULL for a dense batch of B sequences of T tokens; otherwise a
+ *               DEVICE int32 [B+1] array of packed sequence offsets with
+ *               cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = T = R (the
+ *               number of packed token rows).  Checked on the device: a
+ *               violation sets GLA_ERR_INVALID_ARG in the status word and the
+ *               offending sequence writes nothing.
+ *   B, H, T     batch (or number of packed sequences), heads, tokens per
+ *               sequence (or packed rows).  B, H, T >= 0; with T = 0 (or empty
+ *               sequences) final_state receives init_state (or zeros).
+ *   dk, dv      head sizes: 64 or 128 each
+ *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O), or
+ *               16, 32, 64 (fp32 SIMT path); fp32 I/O always takes the SIMT
+ *               path (chunk 16, 32, 64 or 128)
+ *   stream      CUDA stream
+ *   flags       GLA_FLAG_* bits; 0 = bf16 I/O, per-head gate
+ *
+ * Alignment: q, k, v, out, init_state, final_state must be 16-byte aligned; g
+ * 4-byte aligned (16-byte with GLA_FLAG_VECTOR_GATE).
+ */
+gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         float scale, const float *init_state, void *out,
+                         float *final_state, const int32_t *cu_seqlens, int B, int H,
+                         int T, int dk, int dv, int chunk, gla_stream_t stream,
+                         unsigned flags);
+
+/*
+ * gla_decode_step -- one recurrent step for N concurrent sequences.
+ *
+ * Source: "i14 Laplace 3B" page, paragraph "GLA mixer" (the recurrence, one
+ * token) and section "Inference optimization on Trainium2" (decode over many
+ * concurrent sequences, one fixed state page per sequence).
+ *
+ * For every (n, h): S <- diag(exp g) S + k^T v (in place), o <- scale * q S.
+ *
+ * Arguments
+ *   q, k         [N, H, dk], bf16 or fp32 (GLA_FLAG_FP32_IO)
+ *   v            [N, H, dv], same dtype
+ *   g            fp32 [N, H], or [N, H, dk] with GLA_FLAG_VECTOR_GATE; -inf allowed
+ *   scale        readout scale
+ *   state_inout  fp32 [N, H, dk, dv], read and overwritten in place
+ *   out          [N, H, dv], same dtype as q (fp32 with GLA_FLAG_FP32_OUT)
+ *   N, H         sequences and heads (>= 0; 0 does nothing)
+ *   dk, dv       64 or 128 each
+ * Alignment: every pointer 16-byte aligned except g (4-byte).
+ */
+gla_status gla_decode_step(const void *q, const void *k, const void *v, const float *g,
+                           float scale, float *state_inout, void *out, int N, int H,
+                           int dk, int dv, gla_stream_t stream, unsigned flags);
+
+/* Static English text for a status code (never NULL). */
+const char *gla_status_string(gla_status status);
+
+/*
+ * gla_status_sync -- wait for `stream`, then read and clear the current GPU's
+ * device status word.  Returns GLA_ERR_CUDA if the stream reports a CUDA error,
+ * otherwise the most severe device-side status seen since the last call
+ * (GLA_ERR_TIMEOUT over GLA_ERR_INVALID_ARG over GLA_OK).
+ */
+gla_status gla_status_sync(gla_stream_t stream);
+
+/* Library version, "major.minor.patch". */
+const char *gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H_ */

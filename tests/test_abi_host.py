@@ -1,0 +1,136 @@
+"""The C ABI library on the host: it builds, loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU (CPU only)."""
+import os
+import re
+
+import pytest
+
+from gated_linear_attention_gla_gb300 import _binding, build as glabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gla.h")
+
+A = 1 << 20  # a 16-byte-aligned fake device address; never dereferenced here
+FAKE = [A * (i + 1) for i in range(12)]
+
+
+@pytest.fixture(scope="module")
+def L():
+    glabuild.build()
+    return _binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gla_chunk_fwd", "gla_decode_step", "gla_status_string", "gla_status_sync"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in gla.h but not exported"
+
+
+def test_no_torch_in_the_library(L):
+    # the boundary is a plain C library: it must not need libtorch/libc10
+    import subprocess
+    out = subprocess.run(["ldd", _binding.LIB_PATH], capture_output=True, text=True).stdout
+    libs = [line.split()[0] for line in out.splitlines() if line.strip()]
+    assert not [x for x in libs if re.match(r"lib(torch|c10)", os.path.basename(x))]
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert _binding.status_string(s)
+    assert _binding.status_string(99) == "unknown status"
+    assert re.match(r"^\d+\.\d+\.\d+$", _binding.version())
+
+
+def chunk(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, init=FAKE[4], out=FAKE[5],
+          final=FAKE[6], cu=0, B=2, H=4, T=256, dk=128, dv=128, chunk=128, flags=0):
+    return _binding.gla_chunk_fwd(q, k, v, g, scale, init, out, final, cu, B, H, T, dk, dv,
+                                  chunk, 0, flags)
+
+
+def decode(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, state=FAKE[4], out=FAKE[5],
+           N=8, H=4, dk=128, dv=128, flags=0):
+    return _binding.gla_decode_step(q, k, v, g, scale, state, out, N, H, dk, dv, 0, flags)
+
+
+E = _binding
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=1 << 5), E.GLA_ERR_INVALID_ARG),
+    (dict(B=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(H=-3), E.GLA_ERR_INVALID_ARG),
+    (dict(T=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), E.GLA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), E.GLA_ERR_INVALID_ARG),
+    (dict(dk=96), E.GLA_ERR_UNSUPPORTED),
+    (dict(dv=256), E.GLA_ERR_UNSUPPORTED),
+    (dict(chunk=100), E.GLA_ERR_UNSUPPORTED),
+    (dict(chunk=256), E.GLA_ERR_UNSUPPORTED),
+    (dict(q=0), E.GLA_ERR_INVALID_ARG),
+    (dict(g=0), E.GLA_ERR_INVALID_ARG),
+    (dict(out=0), E.GLA_ERR_INVALID_ARG),
+    (dict(q=FAKE[0] + 8), E.GLA_ERR_MISALIGNED),
+    (dict(out=FAKE[5] + 2), E.GLA_ERR_MISALIGNED),
+    (dict(init=FAKE[4] + 4), E.GLA_ERR_MISALIGNED),
+    (dict(g=FAKE[3] + 2), E.GLA_ERR_MISALIGNED),
+    (dict(g=FAKE[3] + 4, flags=E.GLA_FLAG_VECTOR_GATE), E.GLA_ERR_MISALIGNED),
+    (dict(cu=FAKE[7] + 2), E.GLA_ERR_MISALIGNED),
+    (dict(out=FAKE[0]), E.GLA_ERR_INVALID_ARG),          # out aliases q
+    (dict(out=FAKE[2] + 64), E.GLA_ERR_INVALID_ARG),     # out overlaps v
+    (dict(final=FAKE[4] + 16), E.GLA_ERR_INVALID_ARG),   # final partially overlaps init
+    (dict(final=FAKE[1]), E.GLA_ERR_INVALID_ARG),        # final overlaps k
+    (dict(B=1 << 20, T=1 << 20), E.GLA_ERR_INVALID_ARG),  # size overflow
+])
+def test_chunk_fwd_rejects_before_launch(L, kw, status):
+    assert chunk(**kw) == status
+
+
+def test_chunk_fwd_empty_problems_are_no_ops(L):
+    # nothing to compute and nothing to write: returns before any CUDA call
+    assert chunk(B=0) == E.GLA_OK
+    assert chunk(H=0) == E.GLA_OK
+    assert chunk(T=0, final=0, q=0, k=0, v=0, g=0, out=0) == E.GLA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=1 << 7), E.GLA_ERR_INVALID_ARG),
+    (dict(N=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), E.GLA_ERR_INVALID_ARG),
+    (dict(dk=32), E.GLA_ERR_UNSUPPORTED),
+    (dict(dv=192), E.GLA_ERR_UNSUPPORTED),
+    (dict(state=0), E.GLA_ERR_INVALID_ARG),
+    (dict(k=0), E.GLA_ERR_INVALID_ARG),
+    (dict(v=FAKE[2] + 4), E.GLA_ERR_MISALIGNED),
+    (dict(state=FAKE[4] + 8), E.GLA_ERR_MISALIGNED),
+    (dict(g=FAKE[3] + 1), E.GLA_ERR_MISALIGNED),
+    (dict(out=FAKE[4]), E.GLA_ERR_INVALID_ARG),          # out inside the state
+    (dict(state=FAKE[0]), E.GLA_ERR_INVALID_ARG),        # state overlaps q
+    (dict(N=1 << 20, H=1 << 12), E.GLA_ERR_INVALID_ARG),  # too many units
+])
+def test_decode_step_rejects_before_launch(L, kw, status):
+    assert decode(**kw) == status
+
+
+def test_decode_step_empty_is_no_op(L):
+    assert decode(N=0) == E.GLA_OK
+    assert decode(H=0) == E.GLA_OK
+
+
+def test_ctypes_signatures_match_header(L):
+    """The binding's argument counts equal the header's parameter counts."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_status_sync", "gla_status_string"):
+        m = re.search(name + r"\s*\(([^)]*)\)", text)
+        nparams = len([p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"])
+        assert len(getattr(L, name).argtypes) == nparams, name

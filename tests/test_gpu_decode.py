@@ -1,0 +1,104 @@
+"""GPU decode step (gla_decode_step) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gla_inputs
+import oracle
+from parity import TOL_STATE, check_bf16_rounding, cuda, out_tol, rel_max, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _gla():
+    import gated_linear_attention_gla_gb300 as gla
+    return gla
+
+
+def _inputs(N, H, dk, dv, io, gate, steps, seed=7):
+    w = gla_inputs.WORKLOADS["decode"]
+    return gla_inputs.decode_inputs(w, seed=seed, N=N, H=H, dk=dk, dv=dv, io=io, gate=gate,
+                                    steps=steps)
+
+
+@pytest.mark.parametrize("io", ["bf16", "fp32"])
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (64, 128), (128, 64)])
+def test_decode_steps_match_oracle(cuda_ok, io, gate, dk, dv):
+    gla = _gla()
+    x = _inputs(37, 3, dk, dv, io, gate, steps=3)
+    S_ref = to_np(x["state"])
+    S = cuda(x["state"]).clone()
+    for t in range(3):
+        args = (cuda(x["q"][t]), cuda(x["k"][t]), cuda(x["v"][t]), cuda(x["g"][t]))
+        if io == "bf16":
+            # same step twice from the same state: bf16 output, then fp32 output
+            S2 = S.clone()
+            out16 = gla.decode_step(*args, S2, scale=x["scale"])
+            out = gla.decode_step(*args, S, scale=x["scale"], out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            check_bf16_rounding(out16, out)
+            assert torch.equal(S, S2)
+        else:
+            out = gla.decode_step(*args, S, scale=x["scale"])
+        o_ref, S_ref = oracle.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t],
+                                          x["scale"], S_ref)
+        torch.cuda.synchronize()
+        assert rel_max(to_np(out), o_ref) <= out_tol(x["q"].dtype), t
+        tol_s = TOL_STATE if io == "bf16" else 1e-5
+        assert rel_max(to_np(S), S_ref) <= tol_s, t
+
+
+def test_decode_minus_inf_gate_resets_state(cuda_ok):
+    gla = _gla()
+    x = _inputs(5, 2, 128, 128, "fp32", "scalar", steps=1)
+    g = torch.full_like(x["g"][0], float("-inf"))
+    S = cuda(x["state"]).clone()
+    out = gla.decode_step(cuda(x["q"][0]), cuda(x["k"][0]), cuda(x["v"][0]), cuda(g), S,
+                          scale=1.0)
+    kv = torch.einsum("nhi,nhj->nhij", x["k"][0].double(), x["v"][0].double())
+    # 0 * S + k v^T is exact in fp32 when k_i v_j is (products of fp32 rounded once)
+    assert rel_max(to_np(S), kv.numpy()) < 1e-6
+    o_ref = torch.einsum("nhi,nhij->nhj", x["q"][0].double(), kv)
+    assert rel_max(to_np(out), o_ref.numpy()) < 1e-5
+
+
+def test_decode_in_place_on_a_view_of_a_state_pool(cuda_ok):
+    """The state argument may be a contiguous slice of a larger pool (one page
+    per sequence); pages outside it are untouched."""
+    gla = _gla()
+    x = _inputs(6, 2, 64, 64, "bf16", "scalar", steps=1)
+    pool = torch.randn(10, 2, 64, 64, device="cuda")
+    before = pool.clone()
+    pool[2:8] = cuda(x["state"])
+    gla.decode_step(cuda(x["q"][0]), cuda(x["k"][0]), cuda(x["v"][0]), cuda(x["g"][0]),
+                    pool[2:8], scale=x["scale"])
+    _, S_ref = oracle.decode_step(x["q"][0], x["k"][0], x["v"][0], x["g"][0], x["scale"],
+                                  x["state"])
+    torch.cuda.synchronize()
+    assert torch.equal(pool[:2], before[:2]) and torch.equal(pool[8:], before[8:])
+    assert rel_max(to_np(pool[2:8]), S_ref) <= TOL_STATE
+
+
+def test_decode_full_size_sampled(cuda_ok):
+    """N=1280, H=16, dk=dv=128, two consecutive steps; a sample of (n, h) pages
+    is recomputed by the oracle."""
+    gla = _gla()
+    w = gla_inputs.WORKLOADS["decode"]
+    x = gla_inputs.decode_inputs(w, steps=2)
+    S = cuda(x["state"]).clone()
+    outs = []
+    for t in range(2):
+        outs.append(gla.decode_step(cuda(x["q"][t]), cuda(x["k"][t]), cuda(x["v"][t]),
+                                    cuda(x["g"][t]), S, scale=x["scale"],
+                                    out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    ns = rng.choice(w.N, 24, replace=False)
+    ns = np.concatenate([ns, [0, w.N - 1]])
+    S_ref = to_np(x["state"][ns])
+    for t in range(2):
+        o_ref, S_ref = oracle.decode_step(x["q"][t][ns], x["k"][t][ns], x["v"][t][ns],
+                                          x["g"][t][ns], x["scale"], S_ref)
+        assert rel_max(to_np(outs[t][ns]), o_ref) <= out_tol(torch.bfloat16)
+    assert rel_max(to_np(S[ns]), S_ref) <= TOL_STATE
