@@ -132,8 +132,10 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec; a.status = status;
 
+  // bf16 I/O with chunk 128 runs on the tensor cores whenever that kernel covers
+  // the shape; if it cannot be launched the call fails (no quiet substitution).
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!fp32 && chunk == 128 && rows > 0 && gla::chunk_tc_supported(a))
+  if (rows > 0 && gla::chunk_tc_supported(a))
     err = gla::launch_chunk_tc(a, s);
   else
     err = gla::launch_chunk_simt(a, s);
