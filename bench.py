@@ -1,0 +1,546 @@
+#!/usr/bin/env python
+"""Throughput of the GLA hot path on GB300: chunked prefill and decode.
+
+One bench step is one pass of the serving hot path over synthetic inputs:
+
+* one ``gla_chunk_fwd`` call over the prefill workload -- B=4 sequences of
+  T=2048 tokens, H=16, dk=dv=128, chunk 128, bf16 I/O, fp32 initial and final
+  states -- whose tokens/s is the headline ``value``;
+* 64 consecutive ``gla_decode_step`` calls over the decode workload -- N=1280
+  concurrent sequences, H=16, dk=dv=128, fp32 states updated in place --
+  reported as ``decode`` (sequence-steps/s).
+
+Prefill and decode are timed separately with CUDA events on the stream that
+launches them.  Four prefill input sets (572 MB together, L2 is 129 MB) are
+rotated so no step reads its inputs from L2; the decode state alone is 1.34 GB.
+``roofline`` gives the prefill kernel's achieved HBM bandwidth against the
+measured copy bandwidth; ``decode.roofline`` the decode kernel's.
+
+``--impl reference`` times the fp64 CPU oracle (the reference for parity, a
+deliberately plain program) on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own replica (the (sequence, head)
+units are independent, so there is no data-path collective); the process
+group is used only for the barrier and the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gla_inputs  # noqa: E402
+
+METRIC = "GLA prefill tokens/s & decode seq-steps/s on 1 GB300; % of tensor/HBM roofline"
+N_SETS = 4
+DECODE_STEPS = 64
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------- workloads
+def prefill_bytes(w, B, T) -> int:
+    """Algorithmic HBM bytes of one prefill call: read q, k, v (bf16), g (fp32),
+    the initial state (fp32); write out (bf16) and the final state (fp32)."""
+    rows = B * T
+    io = 2 * rows * w.H * (2 * w.dk + w.dv) + 4 * rows * w.H + 2 * rows * w.H * w.dv
+    states = 2 * 4 * B * w.H * w.dk * w.dv
+    return io + states
+
+
+def prefill_flops(w, B, T) -> int:
+    """Tensor-core flops of the chunked form as computed (full C x C tiles):
+    per token and head 2 * (C * (dk + dv) + 2 * dk * dv)."""
+    return 2 * (w.chunk * (w.dk + w.dv) + 2 * w.dk * w.dv) * B * T * w.H
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic HBM bytes of one decode step: fp32 state read + write, q, k,
+    v (bf16), g (fp32) read, out (bf16) write."""
+    units = w.N * w.H
+    return units * (8 * w.dk * w.dv + 2 * (2 * w.dk + w.dv) + 4 + 2 * w.dv)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "gated_linear_attention_gla_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(summary: str, source: str):
+    """DRAM bytes per launch recorded in a committed ncu summary, or None when
+    the summary is missing or the kernel source changed since it was taken."""
+    path = os.path.join(PROFILE_DIR, summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash(source):
+        return None
+    return float(m_t.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smmax=float(parts[2]),
+                                 power=float(parts[3]), util=float(parts[4]),
+                                 reasons=[n for n, v in zip(
+                                     ("hw_slowdown", "hw_thermal_slowdown",
+                                      "sw_thermal_slowdown", "sw_power_cap"), parts[5:9])
+                                     if v.lower().startswith("active")]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        loaded = [r for r in rows if r["util"] > 0] or rows
+        if not loaded:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({x for r in loaded for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smmax"] for r in loaded), "reasons": reasons,
+                "samples": len(loaded), "power_w_max": max(r["power"] for r in loaded)}
+
+
+# --------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local, backend="nccl"):
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(budget_s: float = 10.0):
+    """The fp64 oracle on this host's cores, as it stands: the whole prefill
+    workload repeated until ``budget_s`` has passed (at least once), and one
+    decode step over all 1280 sequences repeated likewise."""
+    import oracle
+    wp = gla_inputs.WORKLOADS["prefill"]
+    x = gla_inputs.prefill_inputs(wp)
+    cores = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"], init_state=x["init_state"])
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    prefill = dict(value=wp.B * wp.T * reps / dt, unit="tokens/s", cores=cores, kind="oracle",
+                   sample=f"full prefill workload (B={wp.B}, T={wp.T}, H={wp.H}, d={wp.dk}) "
+                          f"x {reps}, fp64 token-by-token recurrence, {dt:.1f} s")
+    wd = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(wd, steps=1)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(d["q"][0], d["k"][0], d["v"][0], d["g"][0], d["scale"], d["state"])
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s / 2:
+            break
+    dt = time.perf_counter() - t0
+    decode = dict(value=wd.N * reps / dt, unit="seq*steps/s", cores=cores, kind="oracle",
+                  sample=f"one decode step over N={wd.N}, H={wd.H} x {reps}, fp64, {dt:.1f} s")
+    return prefill, decode
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gla(args, world, rank, local):
+    import gated_linear_attention_gla_gb300 as gla
+    from gated_linear_attention_gla_gb300 import build as glabuild
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    glabuild.build()
+    gla.lib()  # loud failure if the library is missing
+
+    wp, wd = gla_inputs.WORKLOADS["prefill"], gla_inputs.WORKLOADS["decode"]
+    B, T, H = wp.B, wp.T, wp.H
+    sets = []
+    for i in range(N_SETS):
+        x = gla_inputs.prefill_inputs(wp, seed=wp.seed + 7919 * i + 104729 * rank)
+        sets.append({n: (x[n].to(dev) if x[n] is not None else None)
+                     for n in ("q", "k", "v", "g", "init_state")})
+    scale = wp.dk ** -0.5
+    outs = [torch.empty(B, T, H, wp.dv, dtype=torch.bfloat16, device=dev) for _ in range(N_SETS)]
+    finals = [torch.empty(B, H, wp.dk, wp.dv, dtype=torch.float32, device=dev)
+              for _ in range(N_SETS)]
+    d = gla_inputs.decode_inputs(wd, steps=DECODE_STEPS, seed=wd.seed + 104729 * rank)
+    d_state = d["state"].to(dev)
+    d_q, d_k, d_v, d_g = (d[n].to(dev) for n in ("q", "k", "v", "g"))
+    d_out = torch.empty(DECODE_STEPS, wd.N, wd.H, wd.dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill(i):
+        s = sets[i % N_SETS]
+        gla.chunk_fwd(s["q"], s["k"], s["v"], s["g"], scale=scale, init_state=s["init_state"],
+                      chunk=wp.chunk, out=outs[i % N_SETS], final_state=finals[i % N_SETS])
+
+    def decode64():
+        for t in range(DECODE_STEPS):
+            gla.decode_step(d_q[t], d_k[t], d_v[t], d_g[t], d_state, scale=wd.dk ** -0.5,
+                            out=d_out[t])
+
+    for i in range(args.warmup):
+        prefill(i)
+        decode64()
+    gla.status_sync()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local if world > 1 else dev.index)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        prefill(i)
+        e1.record(stream)
+        decode64()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    gla.status_sync()
+
+    pre_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    pre_s = max_over_ranks(sum(pre_ms) / 1e3, world)
+    dec_s = max_over_ranks(sum(dec_ms) / 1e3, world)
+    step_s = max_over_ranks(wall / args.steps, world)
+    tokens = sum_over_ranks(B * T * args.steps, world)
+    seq_steps = sum_over_ranks(wd.N * DECODE_STEPS * args.steps, world)
+
+    # ---------------------------------------------------------------- e2e
+    # Host buffers in, host buffers out: each step copies its inputs from
+    # pinned host memory, runs, and copies the outputs back.
+    host = {n: x[n].pin_memory() if x[n] is not None else None
+            for n in ("q", "k", "v", "g", "init_state")}
+    h_out = torch.empty(B, T, H, wp.dv, dtype=torch.bfloat16).pin_memory()
+    h_fin = torch.empty(B, H, wp.dk, wp.dv, dtype=torch.float32).pin_memory()
+    dsets = sets[N_SETS - 1]
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = h_out.numel() * 2 + h_fin.numel() * 4
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_prefill():
+        for n, t in host.items():
+            if t is not None:
+                dsets[n].copy_(t, non_blocking=True)
+        prefill(N_SETS - 1)
+        h_out.copy_(outs[N_SETS - 1], non_blocking=True)
+        h_fin.copy_(finals[N_SETS - 1], non_blocking=True)
+
+    hd = {n: d[n][0].pin_memory() for n in ("q", "k", "v", "g")}
+    hd_out = torch.empty(wd.N, wd.H, wd.dv, dtype=torch.bfloat16).pin_memory()
+    d_h2d = sum(t.numel() * t.element_size() for t in hd.values())
+    d_d2h = hd_out.numel() * 2
+
+    def e2e_decode():
+        for n, dst in (("q", d_q[0]), ("k", d_k[0]), ("v", d_v[0]), ("g", d_g[0])):
+            dst.copy_(hd[n], non_blocking=True)
+        gla.decode_step(d_q[0], d_k[0], d_v[0], d_g[0], d_state, scale=wd.dk ** -0.5,
+                        out=d_out[0])
+        hd_out.copy_(d_out[0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_prefill()
+        e2e_decode()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_prefill()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_pre_s = max_over_ranks(a.elapsed_time(b) / 1e3, world)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_decode()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_dec_s = max_over_ranks(a.elapsed_time(b) / 1e3, world)
+    barrier(world)
+    gla.status_sync()
+
+    if rank != 0:
+        return None
+
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    pb = prefill_bytes(wp, B, T)
+    pf = prefill_flops(wp, B, T)
+    pre_launch_s = statistics.mean(pre_ms) / 1e3
+    pre_gbs = pb / pre_launch_s / 1e9
+    db = decode_bytes(wd)
+    dec_launch_s = statistics.mean(dec_ms) / 1e3 / DECODE_STEPS
+    dec_gbs = db / dec_launch_s / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": tokens / pre_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded normal q, k, v; logsigmoid gates; no dataset)",
+        "config": {
+            "workload": f"simple-GLA chunked prefill B={B} H={H} T={T} dk=dv={wp.dk} "
+                        f"chunk={wp.chunk} bf16 I/O, fp32 states",
+            "global_batch": B * world, "seq_len": T, "heads": H, "dk": wp.dk, "dv": wp.dv,
+            "chunk": wp.chunk, "parallelism": f"replicas x{world}",
+            "l2": f"{N_SETS} rotating prefill input sets "
+                  f"({N_SETS * pb / 1e6:.0f} MB > 129 MB L2); decode state 1.34 GB",
+        },
+        "prefill": {"ms_per_call": statistics.mean(pre_ms), "tokens_per_call": B * T,
+                    "calls": args.steps},
+        "roofline": {
+            "kernel": "chunk_tc_kernel", "bound": "hbm", "achieved": pre_gbs, "peak": hbm,
+            "unit": "GB/s", "frac": pre_gbs / hbm, "peak_kind": peak_kind,
+            "traffic": profiled_traffic("chunk_tc_kernel.prefill_b4_h16_t2048.md",
+                                        "gla_chunk_tc.cu"),
+            "algorithmic_bytes_per_launch": pb,
+            "tensor": {"achieved_tflops": pf / pre_launch_s / 1e12, "peak_tflops": tf_burst,
+                       "frac": pf / pre_launch_s / 1e12 / tf_burst,
+                       "flops_per_launch": pf},
+        },
+        "decode": {
+            "value": seq_steps / dec_s, "unit": "seq*steps/s",
+            "workload": f"decode step N={wd.N} H={wd.H} dk=dv={wd.dk}, fp32 state in place, "
+                        f"{DECODE_STEPS} consecutive steps per timing",
+            "ms_per_step": dec_launch_s * 1e3,
+            "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": dec_gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
+                         "peak_kind": peak_kind,
+                         "traffic": profiled_traffic("decode_kernel.decode_n1280_h16.md",
+                                                     "gla_decode.cu"),
+                         "algorithmic_bytes_per_launch": db},
+        },
+        "e2e": {"value": B * T * e2e_steps * world / e2e_pre_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "decode": {"value": wd.N * e2e_steps * world / e2e_dec_s,
+                           "unit": "seq*steps/s", "h2d_bytes_per_step": d_h2d,
+                           "d2h_bytes_per_step": d_d2h}},
+        "gpu_launches": args.steps * (1 + DECODE_STEPS),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        pre_cpu, dec_cpu = cpu_baseline(args.cpu_budget)
+        line["cpu_baseline"] = pre_cpu
+        line["decode"]["cpu_baseline"] = dec_cpu
+    return line
+
+
+# ------------------------------------------------------------- profile cases
+def run_profile_case(args):
+    """One kernel alone, for Nsight Compute captures: W warm-up launches, then K
+    timed launches of the prefill or the decode kernel.  Prints one JSON line."""
+    import gated_linear_attention_gla_gb300 as gla
+    from gated_linear_attention_gla_gb300 import build as glabuild
+    glabuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.profile == "prefill":
+        w = gla_inputs.WORKLOADS["prefill"]
+        x = gla_inputs.prefill_inputs(w)
+        q, k, v, g, s0 = (x[n].to(dev) for n in ("q", "k", "v", "g", "init_state"))
+
+        def call():
+            gla.chunk_fwd(q, k, v, g, scale=x["scale"], init_state=s0, chunk=w.chunk)
+        nbytes = prefill_bytes(w, w.B, w.T)
+    else:
+        w = gla_inputs.WORKLOADS["decode"]
+        d = gla_inputs.decode_inputs(w, steps=1, N=args.decode_n)
+        q, k, v, g = (d[n][0].to(dev) for n in ("q", "k", "v", "g"))
+        st = d["state"].to(dev)
+        w = gla_inputs.dataclasses.replace(w, N=args.decode_n)
+
+        def call():
+            gla.decode_step(q, k, v, g, st, scale=d["scale"])
+        nbytes = decode_bytes(w)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    gla.status_sync()
+    ms = a.elapsed_time(b) / args.steps
+    print(json.dumps({"profile": args.profile, "ms_per_launch": ms,
+                      "algorithmic_bytes": nbytes, "gbs": nbytes / ms / 1e6}), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    wp = gla_inputs.WORKLOADS["prefill"]
+    x = gla_inputs.prefill_inputs(wp)
+    cores = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.recurrent(x["q"][:1, :256], x["k"][:1, :256], x["v"][:1, :256],
+                         x["g"][:1, :256], x["scale"], init_state=x["init_state"][:1])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"], init_state=x["init_state"])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = wp.B * wp.T * args.steps / total
+    sample = (f"full prefill workload (B={wp.B}, T={wp.T}, H={wp.H}, d={wp.dk}) per step, "
+              f"fp64 token-by-token recurrence")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded normal q, k, v; logsigmoid gates; no dataset)",
+        "config": {"workload": f"simple-GLA chunked prefill B={wp.B} H={wp.H} T={wp.T} "
+                               f"dk=dv={wp.dk} chunk={wp.chunk} bf16 I/O, fp32 states",
+                   "global_batch": wp.B, "seq_len": wp.T, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gla", "reference"], default="gla")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run one kernel alone (for ncu captures) instead of the bench")
+    ap.add_argument("--decode-n", type=int, default=1280,
+                    help="sequences for --profile decode")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.profile:
+        run_profile_case(args)
+        return
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        dist_init(world, local)
+        line = run_gla(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,7 +36,10 @@ class GlaError(RuntimeError):
 
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if status == GLA_ERR_CUDA:
+            msg += f": {lib().gla_last_error_string().decode()}"
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:
@@ -62,6 +65,10 @@ def lib() -> ctypes.CDLL:
             L.gla_status_sync.restype = _i
             L.gla_version.argtypes = []
             L.gla_version.restype = ctypes.c_char_p
+            L.gla_chunk_fwd_kernel.argtypes = [_i, _i, _i, ctypes.c_uint]
+            L.gla_chunk_fwd_kernel.restype = ctypes.c_char_p
+            L.gla_last_error_string.argtypes = []
+            L.gla_last_error_string.restype = ctypes.c_char_p
             _lib = L
     return _lib
 
@@ -88,6 +95,12 @@ def gla_decode_step(q, k, v, g, scale, state_inout, out, N, H, dk, dv, stream, f
     return lib().gla_decode_step(q or None, k or None, v or None, g or None, float(scale),
                                  state_inout or None, out or None, N, H, dk, dv,
                                  stream or None, flags)
+
+
+def chunk_fwd_kernel(dk, dv, chunk, flags):
+    """Name of the kernel gla_chunk_fwd would run ("tensor_core" / "cuda_core"), or None."""
+    r = lib().gla_chunk_fwd_kernel(dk, dv, chunk, flags)
+    return None if r is None else r.decode()
 
 
 def gla_status_sync(stream) -> int:

@@ -59,11 +59,35 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 constexpr long long kMaxElems = 1ll << 40;  // per tensor; keeps index arithmetic exact
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Map a CUDA result to a status, remembering the error for gla_last_error_string.
+gla_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return GLA_OK;
+  g_last_cuda_error = e;
+  return GLA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
 const char* gla_version(void) { return "0.1.0"; }
+
+const char* gla_last_error_string(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
+}
+
+const char* gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags) {
+  if (!flags_ok(flags) || !head_size_ok(dk) || !head_size_ok(dv)) return nullptr;
+  if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return nullptr;
+  gla::ChunkArgs a{};
+  a.dk = dk; a.dv = dv; a.chunk = chunk;
+  a.fp32_io = (flags & GLA_FLAG_FP32_IO) != 0;
+  a.fp32_out = a.fp32_io || (flags & GLA_FLAG_FP32_OUT) != 0;
+  a.vector_gate = (flags & GLA_FLAG_VECTOR_GATE) != 0;
+  return gla::chunk_tc_supported(a) ? "tensor_core" : "cuda_core";
+}
 
 const char* gla_status_string(gla_status status) {
   switch (status) {
@@ -123,7 +147,7 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
 
   cudaError_t err;
   unsigned* status = status_word(&err);
-  if (!status) return GLA_ERR_CUDA;
+  if (!status) return cuda_status(err);
 
   gla::ChunkArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
@@ -139,7 +163,7 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     err = gla::launch_chunk_tc(a, s);
   else
     err = gla::launch_chunk_simt(a, s);
-  return err == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+  return cuda_status(err);
 }
 
 gla_status gla_decode_step(const void* q, const void* k, const void* v, const float* g,
@@ -175,20 +199,19 @@ gla_status gla_decode_step(const void* q, const void* k, const void* v, const fl
   a.state = state_inout; a.out = out;
   a.N = N; a.H = H; a.dk = dk; a.dv = dv;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec;
-  const cudaError_t err = gla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+  return cuda_status(gla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gla_status gla_status_sync(gla_stream_t stream) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return GLA_ERR_CUDA;
-  cudaError_t err;
+  cudaError_t err = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_status(err);
   unsigned* p = status_word(&err);
-  if (!p) return GLA_ERR_CUDA;
+  if (!p) return cuda_status(err);
   unsigned word = 0;
-  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return GLA_ERR_CUDA;
-  if (word != 0 && cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) return GLA_ERR_CUDA;
+  err = cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_status(err);
+  if (word != 0 && (err = cudaMemset(p, 0, sizeof(unsigned))) != cudaSuccess)
+    return cuda_status(err);
   if (word & gla::kDevTimeout) return GLA_ERR_TIMEOUT;
   if (word & gla::kDevBadSeqlens) return GLA_ERR_INVALID_ARG;
   return GLA_OK;

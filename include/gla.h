@@ -140,6 +140,14 @@ gla_status gla_decode_step(const void *q, const void *k, const void *v, const fl
                            float scale, float *state_inout, void *out, int N, int H,
                            int dk, int dv, gla_stream_t stream, unsigned flags);
 
+/*
+ * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call
+ * with these head sizes, chunk size and flags: "tensor_core" (the tcgen05
+ * kernel), "cuda_core" (the fp32 CUDA-core kernel), or NULL when the call
+ * would be rejected.  Pure host function: launches nothing.
+ */
+const char *gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags);
+
 /* Static English text for a status code (never NULL). */
 const char *gla_status_string(gla_status status);
 
@@ -150,6 +158,10 @@ const char *gla_status_string(gla_status status);
  * (GLA_ERR_TIMEOUT over GLA_ERR_INVALID_ARG over GLA_OK).
  */
 gla_status gla_status_sync(gla_stream_t stream);
+
+/* Text of the CUDA error behind the calling thread's most recent GLA_ERR_CUDA
+ * (static storage, never NULL; "no error" if there was none). */
+const char *gla_last_error_string(void);
 
 /* Library version, "major.minor.patch". */
 const char *gla_version(void);

