@@ -16,10 +16,10 @@
  *
  * Two serving forms are exported:
  *   gla_chunk_fwd    prefill: the chunked form of the same page's section
- *                    "Challenge 1" (Figure 3) -- per chunk a decay-masked
- *                    causal Q K^T then V, plus the running state's share,
- *                    then one state step with the decay compounded over the
- *                    chunk; emits the final state.
+ *                    "Challenge 1" (Figure 3) -- per chunk a causal Q K^T
+ *                    weighted by the decays, times V, plus the carried-in
+ *                    state's share, then one state step with the chunk's
+ *                    total decay; emits the final state.
  *   gla_decode_step  one token for each of N concurrent sequences, each with a
  *                    fixed-size state page updated in place (section
  *                    "Inference optimization on Trainium2": one fixed page per

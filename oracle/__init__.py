@@ -10,14 +10,14 @@ section "i14 and the Laplace 3B architecture" (paragraphs "GLA mixer" and
 for GLA" (the chunked form, Figure 3).  The page's equations were images and
 did not survive; the definitions below follow its prose:
 
-* state update  ``S_t = diag(exp g_t) S_{t-1} + k_t^T v_t``  -- the per-head
-  decay times the state plus "the rank-1 outer product that writes the current
-  key-value pair into the state";
-* readout       ``o_t = scale * q_t S_t`` -- "the readout queries the state",
-  taken after the update (so token t sees its own key/value);
-* chunked form  -- inside each chunk a decay-masked causal attention, plus the
-  running state's contribution; then the state advances once with the decay
-  compounded over the chunk; "only the state update is sequential".
+* state update  ``S_t = diag(exp g_t) S_{t-1} + k_t^T v_t``  -- the state
+  shrinks by the decay and gains the token's key/value pair as a rank-one term;
+* readout       ``o_t = scale * q_t S_t`` -- the query reads the state after
+  the update (so token t sees its own key/value);
+* chunked form  -- inside each chunk a causal attention with decay weights,
+  plus what the carried-in state contributes; then the state advances once
+  with the chunk's total decay; chunks are independent except for that
+  state hand-off.
 
 ``g`` is a log-decay: shape ``[..., H]`` (one per token and head: the page's
 Simple GLA) or ``[..., H, dk]`` (one per key channel: row i of S decays by

@@ -11,12 +11,12 @@
  * What is computed (the page's equation images were lost; the prose fixes the
  * shape of each step, and the gate is generalised to a per-token log-decay):
  *
- *   S_t = diag(exp g_t) S_{t-1} + k_t^T v_t      ("GLA mixer": fixed per-head
- *                                                 decay times the state, plus
- *                                                 the rank-1 outer product that
- *                                                 writes the current key/value)
- *   o_t = scale * q_t S_t                        ("the readout queries the
- *                                                 state", after the update)
+ *   S_t = diag(exp g_t) S_{t-1} + k_t^T v_t      (the old state shrinks by the
+ *                                                 head's decay and the token's
+ *                                                 key/value pair is added as a
+ *                                                 rank-one matrix)
+ *   o_t = scale * q_t S_t                        (the query reads the state
+ *                                                 once this token is in it)
  *
  * g_t is either one number per (token, head) -- every row of S decays alike,
  * the page's Simple GLA -- or one number per (token, head, key channel), in
@@ -32,10 +32,10 @@
  *
  * Three entry points:
  *   gla_oracle_recurrent_f64  token-by-token recurrence (the definition)
- *   gla_oracle_chunked_f64    the page's chunked form: per chunk, decay-masked
- *                             causal attention inside the chunk plus the
- *                             running state's contribution, then one state
- *                             step with the decay compounded over the chunk
+ *   gla_oracle_chunked_f64    the page's chunked form: per chunk, causal
+ *                             attention with decay weights inside the chunk
+ *                             plus what the carried-in state contributes,
+ *                             then one state step with the chunk's total decay
  *   gla_oracle_decode_step_f64 one recurrent step for N independent states
  *
  * Return value: 0 on success, -1 on a bad argument (nothing is written).
