@@ -2,53 +2,57 @@
 //
 // Method: the chunked form of the "i14 Laplace 3B on AWS Trainium2" page
 // (section "Challenge 1", Figure 3) with per-token log-decays g.  For a chunk
-// of C = 128 tokens, G_t = sum of g over the chunk up to and including t:
-//     A   = Q K^T                                       (C x C)
-//     P   = A * exp(G_t - G_j) for j <= t, 0 above       (decay-masked, causal)
-//     O   = scale * ( P V + diag(exp G_t) Q S )          (intra + running state)
-//     S'  = exp(G_last) S + K^T diag(exp(G_last - G_j)) V
+// of C = 128 tokens, G_t = sum of g over the chunk up to and including t, and
+// L the chunk's last token:
+//     S'  = exp(G_L) S + K^T (W V),        W_j = exp(G_L - G_j)  (<= 1)
+//     O   = scale * ( sum_{j<=t} A_tj exp(G_t - G_j) V_j + exp(G_t) (Q S)_t )
+// with A = Q K^T.  Writing exp(G_t - G_j) = exp(G_t - G_L) W_j, the
+// intra-chunk term becomes exp(G_t - G_L) * (causal(A) . (W V))_t: the same
+// decayed values W V that update the state also serve the output, and the
+// mask is a plain causal mask.  This is exact while the chunk's decay span
+// exp(G_0 - G_L) stays inside 2^96 (so W V and the row factor stay in the
+// normal bf16/fp32 range); a chunk with a wider span takes the explicit path:
+// P = A * exp(G_t - G_j) on the causal part, times the raw V.
 //
-// One CTA owns one (sequence, head, 64-wide slice of dv) and walks the
-// sequence's chunks in order.  The state slice S (dk x 64, fp32) lives in
-// tensor memory (TMEM) for the whole sequence: before each chunk the state
-// group scales it by exp(G_last) in place, and the chunk's K^T (W V) product
-// accumulates straight into it.  Four tensor-core contractions per chunk, all
-// bf16 x bf16 -> fp32 into TMEM:
-//     MMA1  A   = Q K^T           M=128 (t) N=128 (j) K=dk   A,B K-major
-//     MMA4  S  += K^T (W V)       M=dk (i)  N=64      K=128  A,B MN-major
-//     MMA3  O2  = Q S_bf16        M=128 (t) N=64      K=dk   B MN-major
-//     MMA2  O1  = P V             M=128 (t) N=64      K=128  B MN-major
-// W V (W_j = exp(G_last - G_j)) is rounded to bf16 as hi + lo.  The lo term
-// only matters through the final state, and only while enough of it survives
-// the decay still to come: a chunk whose remaining decay to the end of the
-// sequence is below 2^-16 (known two chunks ahead) skips it.  MMA3 reads the
-// state through a bf16 copy in shared memory.
+// One CTA owns one (sequence, head, 64-wide slice of dv) and walks the chunks
+// in order.  The state slice S (dk x 64, fp32) lives in tensor memory (TMEM)
+// for the whole sequence: the state group scales it by exp(G_L) in place and
+// the chunk's K^T (W V) accumulates into it.  Four tcgen05 contractions per
+// chunk, bf16 x bf16 -> fp32 in TMEM:
+//     MMA1  A   = Q K^T              M=128 (t) N=128 (j) K=dk  A,B smem K-major
+//     MMA4  S  += K^T (W V)          M=dk (i)  N=64      K=128 A,B smem MN-major
+//     MMA3  O2  = Q S_bf16           M=128 (t) N=64      K=dk  B smem MN-major
+//     MMA2  O1  = P' (W V)           M=128 (t) N=64      K=128 A = P' in TMEM,
+//                                                                three passes
+// W V is carried as two bf16 tiles, hi + lo (hi = W V rounded, lo = the
+// rest), and both MMA4 and MMA2 take the two passes.  P' = causal(A) is
+// rounded to bf16 once, except on the four 32 x 32 diagonal blocks, where the
+// largest terms of a row sit under strong decay: there P' also has a lo part,
+// taken in a third MMA2 pass against (W V)_hi.  P' overwrites A in TMEM:
+// block b (32 fp32 columns) becomes 16 columns of bf16 pairs at column 16 b,
+// and the diagonal lo parts fill columns 64 .. 127 (block b at 64 + 16 b,
+// zero off the row's own diagonal block); every fp32 block a row needs is
+// read by then.
 //
-// The only true recurrence is S_c = exp(G_last) S_{c-1} + dS_c; everything
-// else in a chunk overlaps its neighbours.  Roles (16 warps):
-//   warp 0       TMA producer: Q, K (two 64-column panels) and the V slice of
-//                each chunk into a 2-stage ring, 128-byte swizzled
+// Resources and their release points (the chunk pipeline):
+//   Q, K tiles      2-stage ring, free once MMA3 of the chunk has run
+//   V tile          single buffer, free once the W V split has read it (wide
+//                   chunks: once MMA2 has run)
+//   (W V) hi, lo    2 buffers each, free once MMA2 (and MMA4) have run
+//   S_bf16          1 buffer (B operand of MMA3)
+// Roles (16 warps):
+//   warp 0       TMA producer
 //   warp 1       TMEM allocator; issues MMA1, MMA4, MMA3 (the "front")
-//   warp 2       issues MMA2 (the "back"), so P V never blocks the state chain
-//   warp 3       gate warp: prefix sums of g and the per-column decay factors,
-//                two chunks ahead, into a 6-slot ring
-//   warps 4..11  mask group: the decay-masked P (written over the chunk's K
-//                tile, dead once MMA4 has run), then the output of the previous
-//                chunk; two warps per TMEM lane quadrant (warp % 4), one for the
-//                even and one for the odd 32-column blocks of P and one
-//                32-column half of the output
-//   warps 12..15 state group: W V split, the in-place decay of S, the bf16
-//                copy of S for MMA3, the final state
-// TMEM: A 2x128, O1 64, O2 2x64, S 64 = 512 columns.  Every wait on an
-// mbarrier is bounded in wall time; on timeout the kernel flags the device
-// status word, stops issuing work, releases TMEM and returns.
-//
-// Decay mask: for a column block (32 columns) strictly below the diagonal
-// block of row t, exp(G_t - G_j) = exp(G_t - G_e) * exp(G_e - G_j) with e the
-// block's last column; both factors are <= 1 because g <= 0, so the product
-// costs two multiplies and cannot overflow.  On the diagonal block the
-// reference is the block's first column s, exp(G_s - G_j) >= 1, used when the
-// block's decay span is below 2^64; otherwise each element takes its own exp.
+//   warp 2       issues MMA2 (the "back")
+//   warp 3       gate warp: prefix sums of g and the chunk's flags, ahead
+//   warps 4..7   mask group: P' from A (thread t owns token row t), then the
+//                output of the previous chunk
+//   warps 8..15  state group: W V split, in-place decay of S, the bf16 copy of
+//                S for MMA3, the final state; two warps per TMEM lane
+//                quadrant, each owning 32 of the 64 state columns
+// TMEM: A/P' 2x128, O1 64, O2 2x64, S 64 = 512 columns.  Every mbarrier wait
+// is bounded in wall time; on timeout the kernel flags the device status word,
+// stops issuing work, releases TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -65,48 +69,49 @@ constexpr int kC = 128;        // chunk (tokens)
 constexpr int kDK = 128;       // key head size handled by this kernel
 constexpr int kDVS = 64;       // value columns per CTA
 constexpr int kThreads = 512;  // 16 warps
-constexpr int kMaskWarps = 8;
-constexpr int kStateWarps = 4;
+constexpr int kMaskWarps = 4;
+constexpr int kStateWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kSpanLimit = 64.f;     // log2 span allowed for the diagonal factorization
-constexpr float kLoCutoff = -16.f;     // log2 of the remaining decay below which lo is dropped
-constexpr int kLookahead = 2;          // chunks the gate warp runs ahead
-constexpr int kSlots = 6;              // gate ring depth (>= kLookahead + 3)
+constexpr float kWideSpan = 96.f;      // log2 chunk decay span above which a chunk is "wide"
+constexpr int kSlots = 3;              // gate ring: chunks c (mask), c + 1 (split), c + 2 (gate)
+constexpr uint32_t kBarState = 2;      // named barrier of the state group
 
 // shared memory map (offsets from the 1024-byte-aligned base)
 constexpr uint32_t kPanel = kC * 128;                 // 128 rows x 128 B
 constexpr uint32_t kQBytes = kPanel * (kDK / 64);     // 32 KB
 constexpr uint32_t kKBytes = kPanel * (kDK / 64);     // 32 KB
-constexpr uint32_t kVBytes = kPanel;                  // 16 KB (64 columns)
-constexpr uint32_t kStageBytes = kQBytes + kKBytes + kVBytes;
-constexpr uint32_t kOffVhi = 2 * kStageBytes;
-constexpr uint32_t kOffVlo = kOffVhi + kVBytes;
-constexpr uint32_t kOffSb = kOffVlo + kVBytes;        // dk rows x 128 B
-// gate slot (floats): G2[128] | total, need_lo, -, - | wE[128] | wS[128] | diag_ok[4]
-constexpr int kSlotG2 = 0, kSlotTotal = 128, kSlotNeedLo = 129, kSlotWE = 132, kSlotWS = 260,
-              kSlotDiag = 388, kSlotFloats = 392;
+constexpr uint32_t kQKStage = kQBytes + kKBytes;      // 64 KB
+constexpr uint32_t kTile = kPanel;                    // 16 KB: 128 rows x 64 columns bf16
+constexpr uint32_t kOffV = 2 * kQKStage;
+constexpr uint32_t kOffVhi = kOffV + kTile;           // 2 buffers
+constexpr uint32_t kOffVlo = kOffVhi + 2 * kTile;     // 2 buffers
+constexpr uint32_t kOffSb = kOffVlo + 2 * kTile;      // dk rows x 128 B
+// gate slot (floats): G2[128] | total, wide, -, -
+constexpr int kSlotG2 = 0, kSlotTotal = 128, kSlotWide = 129, kSlotFloats = 132;
 constexpr uint32_t kOffGate = kOffSb + kDK * 128;
 constexpr uint32_t kOffBar = kOffGate + kSlots * kSlotFloats * 4;
-constexpr uint32_t kOffMisc = kOffBar + 256;          // tmem base, abort flag
-constexpr uint32_t kSmemUsed = kOffMisc + 64;
+constexpr uint32_t kBarBytes = 320;
+constexpr uint32_t kOffMisc = kOffBar + kBarBytes;    // tmem base, abort flag
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffBar % 8 == 0 && kOffGate % 16 == 0, "alignment");
 
 // TMEM column map
-constexpr uint32_t kColA = 0;      // 2 x 128
+constexpr uint32_t kColA = 0;      // 2 x 128: A = Q K^T (fp32), then P' (bf16 pairs) in place
 constexpr uint32_t kColO1 = 256;   // 64
 constexpr uint32_t kColO2 = 320;   // 2 x 64
 constexpr uint32_t kColS = 448;    // 64: the running state slice, fp32
 
 enum Bar {
-  kFull0 = 0, kFull1, kEmpty0, kEmpty1, kAFull0, kAFull1, kAFree0, kAFree1,
-  kPFull, kVtFull, kSFull, kSReady, kSbFull, kSbFree, kOFull, kO1Free,
-  kO2Free0, kO2Free1, kO2Full0, kO2Full1, kGReady0, kGFree0 = kGReady0 + kSlots,
-  kNumBars = kGFree0 + kSlots
+  kQKFull0 = 0, kQKFull1, kQKEmpty0, kQKEmpty1, kVFull, kVEmpty, kAFull0, kAFull1,
+  kAFree0, kAFree1, kPFull, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady, kSbFull,
+  kSbFree, kO1Full, kO1Free, kO2Full0, kO2Full1, kO2Free0, kO2Free1, kGReady0,
+  kGFree0 = kGReady0 + kSlots, kNumBars = kGFree0 + kSlots
 };
-static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
 constexpr uint32_t kIdQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdQS = idesc_bf16(128, kDVS, false, true);
@@ -126,6 +131,67 @@ struct TcParams {
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// P' of token row r (lane quadrant q4) from A = Q K^T in TMEM, in place.  A
+// row is read one 32-column block at a time, the next block's load in flight;
+// P' of block cb goes to columns 16 cb .. 16 cb + 15 (already read), and the
+// lo part of the row's diagonal block to 64 + 16 q4 (the other three lo
+// blocks are zero).  WIDE: explicit decay exp(G_t - G_j) <= 1 on the causal
+// part (G2s: the chunk's log2 prefix sums); otherwise the plain causal mask.
+// The two variants are separate bodies so that neither pays for the other.
+template <bool WIDE>
+__device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float G2,
+                                        const float* G2s) {
+  uint32_t a[32], dlo[16];
+  tmem_ld_32x32b_x32(a_row, a);
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t pk[16];
+    if (cb > q4) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = 0u;
+    } else if (cb < q4) {
+      tmem_ld_wait_x32(a);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float x0 = __uint_as_float(a[2 * e]), x1 = __uint_as_float(a[2 * e + 1]);
+        if constexpr (WIDE) {
+          x0 *= exp2f(G2 - G2s[32 * cb + 2 * e]);
+          x1 *= exp2f(G2 - G2s[32 * cb + 2 * e + 1]);
+        }
+        pk[e] = pack_bf16x2(x0, x1);
+      }
+      tmem_ld_32x32b_x32(a_row + 32 * (cb + 1), a);
+    } else {
+      // diagonal block: causal mask (diagonal kept), bf16 hi + lo
+      tmem_ld_wait_x32(a);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = 32 * cb + 2 * e;
+        float x0 = j <= r ? __uint_as_float(a[2 * e]) : 0.f;
+        float x1 = j + 1 <= r ? __uint_as_float(a[2 * e + 1]) : 0.f;
+        if constexpr (WIDE) {
+          x0 = j <= r ? x0 * exp2f(G2 - G2s[j]) : 0.f;
+          x1 = j + 1 <= r ? x1 * exp2f(G2 - G2s[j + 1]) : 0.f;
+        }
+        pk[e] = pack_bf16x2(x0, x1);
+        dlo[e] = pack_bf16x2(x0 - bf16lo(pk[e]), x1 - bf16hi(pk[e]));
+      }
+    }
+    tmem_st_32x32b_x16(a_row + 16 * cb, pk);
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    if (b == q4) {
+      tmem_st_32x32b_x16(a_row + 64 + 16 * b, dlo);
+    } else {
+      uint32_t z[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      tmem_st_32x32b_x16(a_row + 64 + 16 * b, z);
+    }
+  }
+}
 
 template <bool OUTF32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -156,12 +222,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = 0; i < kNumBars; ++i) {
       // group barriers take one arrival per warp (see warp_arrive)
       uint32_t cnt = 1;
-      if (i == kAFree0 || i == kAFree1 || i == kPFull || i == kO1Free || i == kO2Free0 ||
-          i == kO2Free1)
-        cnt = kMaskWarps;
-      if (i == kVtFull || i == kSReady || i == kSbFull) cnt = kStateWarps;
-      if (i == kEmpty0 || i == kEmpty1) cnt = 2;  // MMA3 (front) and MMA2 (back) done
-      if (i >= kGFree0 && i < kGFree0 + kSlots) cnt = kMaskWarps + kStateWarps;
+      if (i == kPFull || i == kO1Free || i == kO2Free0 || i == kO2Free1) cnt = kMaskWarps;
+      if (i == kVtFull0 || i == kVtFull1 || i == kSReady || i == kSbFull) cnt = kStateWarps;
+      // gate slots are released by both groups and the MMA2 issuer
+      if (i >= kGFree0 && i < kGFree0 + kSlots) cnt = kMaskWarps + kStateWarps + 1;
       mbar_init(&bars[i], cnt);
     }
     *abort_flag = 0;
@@ -195,81 +259,79 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[b]);
   };
+  auto slot_of = [&](int c) -> float* { return gate_ring + (c % kSlots) * kSlotFloats; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const int bidx = packed ? 0 : s;
       for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
-        if (c >= 2 && !wait(kEmpty0 + st, ph((c >> 1) - 1))) break;
-        uint8_t* q_s = smem + st * kStageBytes;
-        uint8_t* k_s = q_s + kQBytes;
-        uint8_t* v_s = k_s + kKBytes;
         const int row = packed ? (int)(start + (long long)c * kC) : c * kC;
-        const int bidx = packed ? 0 : s;
-        mbar_arrive_expect_tx(&bars[kFull0 + st], kStageBytes);
+        if (c >= 2 && !wait(kQKEmpty0 + st, ph((c >> 1) - 1))) break;
+        uint8_t* q_s = smem + st * kQKStage;
+        uint8_t* k_s = q_s + kQBytes;
+        mbar_arrive_expect_tx(&bars[kQKFull0 + st], kQKStage);
 #pragma unroll
         for (int pn = 0; pn < kDK / 64; ++pn) {
-          tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kFull0 + st], pn * 64, h, row, bidx);
-          tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kFull0 + st], pn * 64, h, row, bidx);
+          tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
+          tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
         }
-        tma_load_4d(v_s, &tmV, &bars[kFull0 + st], sl * kDVS, h, row, bidx);
+        if (c >= 1 && !wait(kVEmpty, ph(c - 1))) break;
+        mbar_arrive_expect_tx(&bars[kVFull], kTile);
+        tma_load_4d(smem + kOffV, &tmV, &bars[kVFull], sl * kDVS, h, row, bidx);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------- MMA front: 1, 4, 3
-    // Order: MMA1(0); then per chunk c: MMA4(c), MMA3(c), MMA1(c+1), so the
-    // next chunk's Q K^T never sits in the tensor pipe ahead of the state chain.
+    // Order: MMA1(0); then per chunk c: MMA4(c), MMA3(c), MMA1(c+1).
     if (lane == 0) {
-      const uint32_t sb = sbase + kOffSb, vhi = sbase + kOffVhi, vlo = sbase + kOffVlo;
+      const uint32_t sb = sbase + kOffSb;
       auto mma1 = [&](int c) -> bool {
         const int st = c & 1;
-        const uint32_t q_s = sbase + st * kStageBytes;
+        const uint32_t q_s = sbase + st * kQKStage;
         const uint32_t k_s = q_s + kQBytes;
-        if (!wait(kFull0 + st, ph(c >> 1))) return false;
+        if (!wait(kQKFull0 + st, ph(c >> 1))) return false;
         if (c >= 2 && !wait(kAFree0 + st, ph((c >> 1) - 1))) return false;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kDK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
           mma_bf16(tmem + kColA + st * 128, sdesc_sw128(q_s + off, 16, 1024),
                    sdesc_sw128(k_s + off, 16, 1024), kIdQK, kk > 0);
         }
+        mma_commit(&bars[kAFull0 + st]);
         return true;
       };
       bool ok = nch == 0 || mma1(0);
       for (int c = 0; c < nch && ok; ++c) {
         const int st = c & 1;
-        const uint32_t q_s = sbase + st * kStageBytes;
+        const uint32_t q_s = sbase + st * kQKStage;
         const uint32_t k_s = q_s + kQBytes;
-        if (!wait(kVtFull, ph(c))) break;
-        if (!wait(kSReady, ph(c))) break;  // S holds exp(G_last) S_{c-1}
+        const uint32_t vhi = sbase + kOffVhi + st * kTile;
+        const uint32_t vlo = sbase + kOffVlo + st * kTile;
+        if (!wait(kVtFull0 + st, ph(c >> 1))) break;
+        if (!wait(kSReady, ph(c))) break;  // S holds exp(G_L) S_{c-1}
         tc_fence_after();
-        const bool need_lo = gate_ring[(c % kSlots) * kSlotFloats + kSlotNeedLo] != 0.f;
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(tmem + kColS, sdesc_sw128(k_s + kk * 2048, kPanel, 1024),
-                   sdesc_sw128(vhi + kk * 2048, kPanel, 1024), kIdKV, 1);
-        if (need_lo) {
-#pragma unroll
-          for (int kk = 0; kk < kC / 16; ++kk)
-            mma_bf16(tmem + kColS, sdesc_sw128(k_s + kk * 2048, kPanel, 1024),
-                     sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdKV, 1);
+#pragma unroll 1
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t adesc = sdesc_sw128(k_s + kk * 2048, kPanel, 1024);
+          mma_bf16(tmem + kColS, adesc, sdesc_sw128(vhi + kk * 2048, kPanel, 1024), kIdKV, 1);
+          mma_bf16(tmem + kColS, adesc, sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdKV, 1);
         }
-        mma_commit(&bars[kSFull]);         // S = S_c
-        mma_commit(&bars[kAFull0 + st]);  // A ready and K no longer read: P may overwrite K
+        mma_commit(&bars[kSFull]);  // S = S_c
         if (!wait(kSbFull, ph(c))) break;
         if (c >= 2 && !wait(kO2Free0 + st, ph((c >> 1) - 1))) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kDK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
           mma_bf16(tmem + kColO2 + st * kDVS, sdesc_sw128(q_s + off, 16, 1024),
                    sdesc_sw128(sb + kk * 2048, kPanel, 1024), kIdQS, kk > 0);
         }
-        mma_commit(&bars[kSbFree]);        // S_{c-1} (bf16) read
-        mma_commit(&bars[kO2Full0 + st]);  // O2(c) complete
-        mma_commit(&bars[kEmpty0 + st]);   // Q(c) no longer read
+        mma_commit(&bars[kSbFree]);         // S_{c-1} (bf16) read
+        mma_commit(&bars[kO2Full0 + st]);   // O2(c) complete
+        mma_commit(&bars[kQKEmpty0 + st]);  // Q(c), K(c) no longer read
         if (c + 1 < nch) ok = mma1(c + 1);
       }
     }
@@ -278,19 +340,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0) {
       for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
-        const uint32_t p_s = sbase + st * kStageBytes + kQBytes;  // P over the K tile
-        const uint32_t v_s = p_s + kKBytes;
         if (!wait(kPFull, ph(c))) break;
         if (c >= 1 && !wait(kO1Free, ph(c - 1))) break;
+        if (!wait(kVtFull0 + st, ph(c >> 1))) break;  // W V (and V) of chunk c ready
         tc_fence_after();
-#pragma unroll
+        const bool wide = slot_of(c)[kSlotWide] != 0.f;
+        mbar_arrive(&bars[kGFree0 + c % kSlots]);
+        const uint32_t a_p = tmem + kColA + st * 128;  // P': k-step kk at column 8 kk
+        // P' hi at column 8 kk, the diagonal lo parts at 64 + 8 kk; B is the raw V
+        // on a wide chunk, else (W V) hi and lo
+        const uint32_t vhi = wide ? sbase + kOffV : sbase + kOffVhi + st * kTile;
+        const uint32_t vlo = sbase + kOffVlo + st * kTile;
+#pragma unroll 1
         for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-          mma_bf16(tmem + kColO1, sdesc_sw128(p_s + off, 16, 1024),
-                   sdesc_sw128(v_s + kk * 2048, kPanel, 1024), kIdPV, kk > 0);
+          const uint64_t bhi = sdesc_sw128(vhi + kk * 2048, kPanel, 1024);
+          mma_bf16_tmem_a(tmem + kColO1, a_p + 8 * kk, bhi, kIdPV, kk > 0);
+          mma_bf16_tmem_a(tmem + kColO1, a_p + 64 + 8 * kk, bhi, kIdPV, 1);
+          if (!wide)
+            mma_bf16_tmem_a(tmem + kColO1, a_p + 8 * kk,
+                            sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdPV, 1);
         }
-        mma_commit(&bars[kOFull]);
-        mma_commit(&bars[kEmpty0 + st]);
+        mma_commit(&bars[kO1Full]);
+        mma_commit(&bars[kAFree0 + st]);   // A/P' buffer
+        mma_commit(&bars[kVtFree0 + st]);  // (W V) hi/lo buffers
+        if (wide) mma_commit(&bars[kVEmpty]);
       }
     }
   } else if (warp == 3) {
@@ -304,25 +377,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                      : 0.f;
       }
     };
-    float totals[kLookahead + 1];  // chunk totals (log2) of chunks c-kLookahead .. c
-#pragma unroll
-    for (int i = 0; i <= kLookahead; ++i) totals[i] = 0.f;
-    // publish chunk d: remaining decay after it decides whether MMA4 needs lo
-    auto publish = [&](int d, float remaining) {
-      float* slot = gate_ring + (d % kSlots) * kSlotFloats;
-      if (lane == 0) slot[kSlotNeedLo] = (remaining < kLoCutoff) ? 0.f : 1.f;
-      warp_arrive(kGReady0 + d % kSlots);
-    };
     float gnext[4];
     load4(0, gnext);
-    bool ok = true;
     for (int c = 0; c < nch; ++c) {
       float gv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) gv[i] = gnext[i];
       load4(c + 1, gnext);
-      if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) { ok = false; break; }
-      float* slot = gate_ring + (c % kSlots) * kSlotFloats;
+      if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) break;
+      float* slot = slot_of(c);
       float run[4];
       run[0] = gv[0];
 #pragma unroll
@@ -338,74 +401,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       float G2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) G2[i] = (excl + run[i]) * kLog2e;
-      *reinterpret_cast<float4*>(slot + kSlotG2 + 4 * lane) = make_float4(G2[0], G2[1], G2[2], G2[3]);
-      // block of my columns: 32 * (lane / 8) .. +31; its first column is lane 8k's
-      // first token, its last column is lane 8k+7's last token
-      const float Gb = __shfl_sync(0xffffffffu, G2[0], lane & ~7);
-      const float Ge = __shfl_sync(0xffffffffu, G2[3], lane | 7);
-      float wE[4], wS[4], span = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        wE[i] = exp2f(Ge - G2[i]);
-        wS[i] = exp2f(Gb - G2[i]);
-        span = fmaxf(span, fabsf(Gb - G2[i]));
+      *reinterpret_cast<float4*>(slot + kSlotG2 + 4 * lane) =
+          make_float4(G2[0], G2[1], G2[2], G2[3]);
+      const float first = __shfl_sync(0xffffffffu, G2[0], 0);
+      if (lane == 0) {
+        slot[kSlotTotal] = total;
+        slot[kSlotWide] = (first - total > kWideSpan) ? 1.f : 0.f;
       }
-      *reinterpret_cast<float4*>(slot + kSlotWE + 4 * lane) = make_float4(wE[0], wE[1], wE[2], wE[3]);
-      *reinterpret_cast<float4*>(slot + kSlotWS + 4 * lane) = make_float4(wS[0], wS[1], wS[2], wS[3]);
-#pragma unroll
-      for (int off = 1; off < 8; off <<= 1)
-        span = fmaxf(span, __shfl_xor_sync(0xffffffffu, span, off));
-      if ((lane & 7) == 0) reinterpret_cast<int*>(slot)[kSlotDiag + (lane >> 3)] =
-          span < kSpanLimit ? 1 : 0;
-      if (lane == 0) slot[kSlotTotal] = total;
-#pragma unroll
-      for (int i = 0; i < kLookahead; ++i) totals[i] = totals[i + 1];
-      totals[kLookahead] = total;
-      if (c >= kLookahead) {
-        float rem = 0.f;
-#pragma unroll
-        for (int i = 1; i <= kLookahead; ++i) rem += totals[i];
-        publish(c - kLookahead, rem);
-      }
+      warp_arrive(kGReady0 + c % kSlots);
     }
-    if (ok && !*abort_flag) {
-      // the last kLookahead chunks: the remaining decay is known exactly
-      for (int d = max(0, nch - kLookahead); d < nch; ++d) {
-        float rem = 0.f;
-#pragma unroll
-        for (int i = 0; i <= kLookahead; ++i) {
-          const int chunk = nch - 1 - kLookahead + i;  // totals[i] belongs to this chunk
-          if (chunk > d) rem += totals[i];
-        }
-        publish(d, rem);
-      }
-    }
-  } else if (warp < 12) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ mask group
     const int q4 = warp & 3;
-    const int mh = (warp - 4) >> 2;       // column-block parity, and output half
     const int r = 32 * q4 + lane;         // token row
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const float scale = p.scale;
 
-    // output of chunk c: o = scale (O1 + exp(G_t) O2[c & 1]), columns 32 mh .. +31,
-    // in two 16-column passes
-    auto output = [&](int c, float G2t) -> bool {
-      if (!wait(kOFull, ph(c))) return false;                  // MMA2(c): O1
-      if (!wait(kO2Full0 + (c & 1), ph(c >> 1))) return false; // MMA3(c): O2
+    // output of chunk c: o = scale (f_t O1 + exp(G_t) O2[c & 1]), f_t = exp(G_t - G_L)
+    // (1 on wide chunks, whose O1 already carries the decay)
+    auto output = [&](int c, float G2t, float f) -> bool {
+      if (!wait(kO1Full, ph(c))) return false;                  // MMA2(c)
+      if (!wait(kO2Full0 + (c & 1), ph(c >> 1))) return false;  // MMA3(c)
       tc_fence_after();
       const int n = min(kC, len - c * kC);
-      const float se = scale * exp2f(G2t);
+      const float s1 = scale * f, s2 = scale * exp2f(G2t);
       const long long rowbase = start + (long long)c * kC;
-      const size_t off =
-          ((size_t)(rowbase + r) * p.H + h) * p.DV + (size_t)sl * kDVS + 32 * mh;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      const size_t off = ((size_t)(rowbase + r) * p.H + h) * p.DV + (size_t)sl * kDVS;
+#pragma unroll 1
+      for (int part = 0; part < 4; ++part) {
         uint32_t o1[16], o2[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + kColO1 + 32 * mh + 16 * part, o1);
-        tmem_ld_32x32b_x16(tmem + lane_off + kColO2 + (c & 1) * kDVS + 32 * mh + 16 * part, o2);
+        tmem_ld_32x32b_x16(tmem + lane_off + kColO1 + 16 * part, o1);
+        tmem_ld_32x32b_x16(tmem + lane_off + kColO2 + (c & 1) * kDVS + 16 * part, o2);
         tmem_ld_wait();
-        if (part == 1) {
+        if (part == 3) {
           tc_fence_before();
           warp_arrive(kO1Free);
           warp_arrive(kO2Free0 + (c & 1));
@@ -413,7 +441,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         float o[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          o[j] = fmaf(se, __uint_as_float(o2[j]), scale * __uint_as_float(o1[j]));
+          o[j] = fmaf(s2, __uint_as_float(o2[j]), s1 * __uint_as_float(o1[j]));
         if (r < n) {
           if constexpr (OUTF32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off) + 4 * part;
@@ -435,144 +463,63 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       return true;
     };
 
-    float G2prev = 0.f;
+    float G2prev = 0.f, fprev = 1.f;
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const int st = c & 1;
-      const float* slot = gate_ring + (c % kSlots) * kSlotFloats;
-      uint8_t* p_s = smem + st * kStageBytes + kQBytes;  // P over the K tile
+      const float* slot = slot_of(c);
       if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) { ok = false; break; }
       const float G2 = slot[kSlotG2 + r];
+      const float total = slot[kSlotTotal];
+      const bool wide = slot[kSlotWide] != 0.f;
       if (!wait(kAFull0 + st, ph(c >> 1))) { ok = false; break; }
       tc_fence_after();
-      // this warp's blocks: cb = mh and cb = mh + 2; blocks above the diagonal
-      // block (cb > q4) are zero and need no TMEM read
-      const uint32_t a_base = tmem + lane_off + kColA + st * 128;
-      const float* G2s = slot + kSlotG2;
-      uint32_t a[2][32];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        if (mh + 2 * i <= q4) tmem_ld_32x32b_x32(a_base + 32 * (mh + 2 * i), a[i]);
-      tmem_ld_wait();
+      const uint32_t a_row = tmem + lane_off + kColA + st * 128;
+      if (wide)
+        build_p<true>(a_row, q4, r, G2, slot + kSlotG2);
+      else
+        build_p<false>(a_row, q4, r, G2, slot + kSlotG2);
+      tmem_st_wait();
       tc_fence_before();
-      warp_arrive(kAFree0 + st);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int cb = mh + 2 * i;
-        uint32_t pk[16];
-        if (cb < q4 || (cb == q4 && reinterpret_cast<const int*>(slot)[kSlotDiag + cb] != 0)) {
-          // factorised decay: u (per row and block) times w (per column)
-          const bool diag = (cb == q4);
-          const float u = exp2f(G2 - (diag ? G2s[32 * cb] : G2s[32 * cb + 31]));
-          const float* wv = slot + (diag ? kSlotWS : kSlotWE) + 32 * cb;
-#pragma unroll
-          for (int jj = 0; jj < 32; jj += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wv + jj);
-            const int j = 32 * cb + jj;
-            float p0 = __uint_as_float(a[i][jj]) * (u * w4.x);
-            float p1 = __uint_as_float(a[i][jj + 1]) * (u * w4.y);
-            float p2 = __uint_as_float(a[i][jj + 2]) * (u * w4.z);
-            float p3 = __uint_as_float(a[i][jj + 3]) * (u * w4.w);
-            if (diag) {
-              p0 = (j <= r) ? p0 : 0.f;
-              p1 = (j + 1 <= r) ? p1 : 0.f;
-              p2 = (j + 2 <= r) ? p2 : 0.f;
-              p3 = (j + 3 <= r) ? p3 : 0.f;
-            }
-            pk[jj / 2] = pack_bf16x2(p0, p1);
-            pk[jj / 2 + 1] = pack_bf16x2(p2, p3);
-          }
-        } else if (cb == q4) {
-          // diagonal block with a decay span too wide to factorise: one exp each
-#pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            const int j = 32 * cb + jj;
-            const float p0 = (j <= r) ? __uint_as_float(a[i][jj]) * exp2f(G2 - G2s[j]) : 0.f;
-            const float p1 =
-                (j + 1 <= r) ? __uint_as_float(a[i][jj + 1]) * exp2f(G2 - G2s[j + 1]) : 0.f;
-            pk[jj / 2] = pack_bf16x2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = 0u;
-        }
-        uint8_t* panel = p_s + (cb >> 1) * kPanel;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-          *reinterpret_cast<uint4*>(panel + sw128_offset(r, (cb & 1) * 4 + m)) =
-              make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
-      }
-      fence_proxy_async_smem();
       warp_arrive(kPFull);
-      // output of the previous chunk (its MMA2 ran while P was built)
-      if (c >= 1) {
-        ok = output(c - 1, G2prev);
-        warp_arrive(kGFree0 + (c - 1) % kSlots);
-        if (!ok) break;
-      }
+      warp_arrive(kGFree0 + c % kSlots);
+      // output of the previous chunk (its MMA2 ran while this P' was built)
+      if (c >= 1 && !output(c - 1, G2prev, fprev)) { ok = false; break; }
       G2prev = G2;
+      fprev = wide ? 1.f : exp2f(G2 - total);
     }
-    if (ok && nch >= 1 && output(nch - 1, G2prev))
-      warp_arrive(kGFree0 + (nch - 1) % kSlots);
+    if (ok && nch >= 1) output(nch - 1, G2prev, fprev);
   } else {
     // ----------------------------------------------------------- state group
     const int q4 = warp & 3;
+    const int half = (warp - 8) >> 2;     // which 32 of the 64 state / V columns
     const int r = 32 * q4 + lane;         // state row i (key channel), token row for W V
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const size_t st_off = ((size_t)s * p.H + h) * (size_t)kDK * p.DV + (size_t)r * p.DV +
-                          (size_t)sl * kDVS;
+                          (size_t)sl * kDVS + 32 * half;
     uint8_t* sb_row = smem + kOffSb;
+    float* final_row = p.final_state ? p.final_state + st_off : nullptr;
 
-    // S_c (in TMEM) -> bf16 copy for MMA3 (optional) and, scaled by `decay`,
-    // back into TMEM for the next MMA4 (optional) or to the final state.
-    auto pass_state = [&](float decay, bool to_sb, bool rescale, float* final_row) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 16 columns at a time
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + kColS + 16 * q, v);
-        tmem_ld_wait();
-        if (to_sb) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
-            *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 2 * q + cc)) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-        }
-        if (final_row) {
-          float4* dst = reinterpret_cast<float4*>(final_row) + 4 * q;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        }
-        if (rescale) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(decay * __uint_as_float(v[j]));
-          tmem_st_32x32b_x16(tmem + lane_off + kColS + 16 * q, v);
-        }
-      }
-      if (rescale) tmem_st_wait();
-    };
-
-    // W V split of chunk c into bf16 hi (+ lo); thread r handles token row r.
-    // Returns the chunk's total log2 decay through `total`.
+    // W V split of chunk c (this thread: token row r, V columns 32 half .. +31)
+    // into bf16 hi and lo (buffers c & 1).  Returns the chunk's total log2 decay.
     auto split_wv = [&](int c, float& total) -> bool {
-      const int st = c & 1;
       const int n = min(kC, len - c * kC);
       if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) return false;
-      const float* slot = gate_ring + (c % kSlots) * kSlotFloats;
+      const float* slot = slot_of(c);
       const float G2r = slot[kSlotG2 + r];
       total = slot[kSlotTotal];
-      const bool need_lo = slot[kSlotNeedLo] != 0.f;
+      const bool wide = slot[kSlotWide] != 0.f;
       warp_arrive(kGFree0 + c % kSlots);
-      if (!wait(kFull0 + st, ph(c >> 1))) return false;
-      const uint8_t* v_s = smem + st * kStageBytes + kQBytes + kKBytes;
+      // MMA2(c-2) done; MMA4(c-2) is done too (its S was passed before this call)
+      if (c >= 2 && !wait(kVtFree0 + (c & 1), ph((c >> 1) - 1))) return false;
+      if (!wait(kVFull, ph(c))) return false;
+      const uint8_t* v_s = smem + kOffV;
+      uint8_t* hi_s = smem + kOffVhi + (c & 1) * kTile;
+      uint8_t* lo_s = smem + kOffVlo + (c & 1) * kTile;
       const float w = (r < n) ? exp2f(total - G2r) : 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint32_t off = sw128_offset(r, cc);
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint32_t off = sw128_offset(r, 4 * half + cc);
         const uint4 raw = *reinterpret_cast<const uint4*>(v_s + off);
         const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t hi[4], lo[4];
@@ -582,31 +529,68 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           hi[e] = pack_bf16x2(x0, x1);
           lo[e] = pack_bf16x2(x0 - bf16lo(hi[e]), x1 - bf16hi(hi[e]));
         }
-        *reinterpret_cast<uint4*>(smem + kOffVhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if (need_lo)
-          *reinterpret_cast<uint4*>(smem + kOffVlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(hi_s + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(lo_s + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();
-      warp_arrive(kVtFull);
+      if (!wide) {
+        // the raw V tile is no longer needed (a wide chunk keeps it for MMA2)
+        named_bar_sync(kBarState, kStateWarps * 32);
+        if (warp == 8 && lane == 0) mbar_arrive(&bars[kVEmpty]);
+      }
+      warp_arrive(kVtFull0 + (c & 1));
       return true;
     };
 
+    // S (TMEM) -> bf16 copy for MMA3 (to_sb), scaled by `decay` back into TMEM
+    // for the next MMA4 (rescale), and/or out to the final state (final_out).
+    auto pass_state = [&](float decay, bool to_sb, bool rescale, float* final_out) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // 16 columns at a time
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
+        tmem_ld_wait();
+        if (to_sb) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 4 * half + 2 * q + cc)) =
+                make_uint4(
+                    pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+        }
+        if (final_out) {
+          float4* dst = reinterpret_cast<float4*>(final_out) + 4 * q;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+        if (rescale) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(decay * __uint_as_float(v[j]));
+          tmem_st_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
+        }
+      }
+      if (rescale) tmem_st_wait();
+    };
+
     bool ok = true;
-    float* final_row = p.final_state ? p.final_state + st_off : nullptr;
     if (nch == 0) {
       // empty sequence: the final state is the initial state
       if (final_row) {
 #pragma unroll 4
-        for (int j = 0; j < kDVS; ++j) final_row[j] = p.init_state ? p.init_state[st_off + j] : 0.f;
+        for (int j = 0; j < 32; ++j) final_row[j] = p.init_state ? p.init_state[st_off + j] : 0.f;
       }
     } else {
-      // S_{-1} = initial state: bf16 copy for MMA3(0); TMEM gets exp(G_last(0)) S_{-1}
+      // S_{-1} = initial state: bf16 copy for MMA3(0); TMEM gets exp(G_L(0)) S_{-1}
       float total = 0.f;
       ok = split_wv(0, total);
       if (ok) {
         const float decay = exp2f(total);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 16 columns at a time
+        for (int q = 0; q < 2; ++q) {
           uint32_t v[16];
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
@@ -619,14 +603,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
-            *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 2 * q + cc)) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+            *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 4 * half + 2 * q + cc)) =
+                make_uint4(
+                    pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                    pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(decay * __uint_as_float(v[j]));
-          tmem_st_32x32b_x16(tmem + lane_off + kColS + 16 * q, v);
+          tmem_st_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -635,13 +620,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         warp_arrive(kSReady);
       }
       for (int c = 0; c < nch && ok; ++c) {
+        // the next chunk's W V first: MMA4 of chunk c+1 needs it together with S_c
+        float next_total = 0.f;
+        if (c + 1 < nch && !split_wv(c + 1, next_total)) { ok = false; break; }
         if (!wait(kSFull, ph(c))) { ok = false; break; }  // S = S_c
         tc_fence_after();
         if (c + 1 < nch) {
-          // W V of the next chunk first (the W V buffers are free now)
-          if (!split_wv(c + 1, total)) { ok = false; break; }
           if (!wait(kSbFree, ph(c))) { ok = false; break; }  // MMA3(c) has read S_{c-1}
-          pass_state(exp2f(total), true, true, nullptr);
+          pass_state(exp2f(next_total), true, true, nullptr);
           fence_proxy_async_smem();
           tc_fence_before();
           warp_arrive(kSbFull);

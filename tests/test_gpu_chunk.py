@@ -147,6 +147,31 @@ def test_minus_inf_gate_inside_chunks(cuda_ok, gate):
     check(x, out, fin, *run_ref(x))
 
 
+@pytest.mark.parametrize("positions", [[5, 40, 90], [0, 1, 2, 127], [64, 65, 66, 200, 201, 202]])
+def test_several_resets_in_one_chunk(cuda_ok, positions):
+    """Three or more -inf gates in one chunk push its decay span past 2^96: the
+    kernel takes its explicit-decay path for that chunk."""
+    x = small(B=2, T=300, H=2)
+    g = x["g"].clone()
+    g[:, positions] = float("-inf")
+    x["g"] = g
+    out, fin = run_gpu(x)
+    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+    check(x, out, fin, *run_ref(x))
+
+
+@pytest.mark.parametrize("mu", [-3.0, 0.0, 8.0])
+def test_strong_and_weak_decay(cuda_ok, mu):
+    """g = logsigmoid(N(mu, 1)): mu = -3 makes every chunk's decay span far wider
+    than 2^96 (explicit path throughout), mu = 8 keeps nearly all memory (the lo
+    half of the state update matters in every chunk)."""
+    x = small(B=2, T=400, H=2)
+    gen = torch.Generator().manual_seed(5)
+    x["g"] = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
+    out, fin = run_gpu(x)
+    check(x, out, fin, *run_ref(x))
+
+
 def test_packed_sequences_with_empty_and_short_ones(cuda_ok):
     x = small(B=0, lengths=[300, 1, 0, 128, 129, 5, 700], H=3, init_std=0.05)
     out, fin = run_gpu(x)
