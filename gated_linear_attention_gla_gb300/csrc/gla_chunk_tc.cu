@@ -4,8 +4,8 @@
 // (section "Challenge 1", Figure 3) with per-token log-decays g.  For a chunk
 // of C = 128 tokens, G_t = sum of g over the chunk up to and including t, and
 // L the chunk's last token:
-//     S'  = exp(G_L) S + K^T (W V),        W_j = exp(G_L - G_j)  (<= 1)
-//     O   = scale * ( sum_{j<=t} A_tj exp(G_t - G_j) V_j + exp(G_t) (Q S)_t )
+//     S_next = exp(G_L) S + K^T (W V),     W_j = exp(G_L - G_j)  (<= 1)
+//     o_t    = scale * ( sum_{j<=t} A_tj exp(G_t - G_j) V_j + exp(G_t) (Q S)_t )
 // with A = Q K^T.  Writing exp(G_t - G_j) = exp(G_t - G_L) W_j, the
 // intra-chunk term becomes exp(G_t - G_L) * (causal(A) . (W V))_t: the same
 // decayed values W V that update the state also serve the output, and the
@@ -14,16 +14,23 @@
 // normal bf16/fp32 range); a chunk with a wider span takes the explicit path:
 // P = A * exp(G_t - G_j) on the causal part, times the raw V.
 //
+// Since exp(G_t) = exp(G_t - G_L) exp(G_L), the whole output row is
+//     o_t = scale * exp(G_t - G_L) * ( Q S' + causal(A) (W V) )_t,  S' = exp(G_L) S
+// and the two contractions share one accumulator.
+//
 // One CTA owns one (sequence, head, 64-wide slice of dv) and walks the chunks
 // in order.  The state slice S (dk x 64, fp32) lives in tensor memory (TMEM)
-// for the whole sequence: the state group scales it by exp(G_L) in place and
-// the chunk's K^T (W V) accumulates into it.  Four tcgen05 contractions per
-// chunk, bf16 x bf16 -> fp32 in TMEM:
+// for the whole sequence: the state group scales it by exp(G_L) in place (its
+// bf16 copy is S') and the chunk's K^T (W V) accumulates into it.  Four
+// tcgen05 contractions per chunk, bf16 x bf16 -> fp32 in TMEM:
 //     MMA1  A   = Q K^T              M=128 (t) N=128 (j) K=dk  A,B smem K-major
 //     MMA4  S  += K^T (W V)          M=dk (i)  N=64      K=128 A,B smem MN-major
-//     MMA3  O2  = Q S_bf16           M=128 (t) N=64      K=dk  B smem MN-major
-//     MMA2  O1  = P' (W V)           M=128 (t) N=64      K=128 A = P' in TMEM,
+//     MMA3  O   = Q S'               M=128 (t) N=64      K=dk  B smem MN-major
+//     MMA2  O  += P' (W V)           M=128 (t) N=64      K=128 A = P' in TMEM,
 //                                                                three passes
+// O is double-buffered by chunk parity, so MMA2 of a chunk never waits for
+// the previous chunk's output to be read.  A wide chunk keeps S' = S and the
+// mask group scales O's row t by exp(G_t) between MMA3 and MMA2.
 // W V is carried as two bf16 tiles, hi + lo (hi = W V rounded, lo = the
 // rest), and both MMA4 and MMA2 take the two passes.  P' = causal(A) is
 // rounded to bf16 once, except on the four 32 x 32 diagonal blocks, where the
@@ -39,20 +46,22 @@
 //   V tile          single buffer, free once the W V split has read it (wide
 //                   chunks: once MMA2 has run)
 //   (W V) hi, lo    2 buffers each, free once MMA2 (and MMA4) have run
-//   S_bf16          1 buffer (B operand of MMA3)
+//   S'              1 buffer, bf16 (B operand of MMA3)
+//   O               2 buffers in TMEM, free once the output has read them
 // Roles (16 warps):
 //   warp 0       TMA producer
 //   warp 1       TMEM allocator; issues MMA1, MMA4, MMA3 (the "front")
 //   warp 2       issues MMA2 (the "back")
 //   warp 3       gate warp: prefix sums of g and the chunk's flags, ahead
 //   warps 4..7   mask group: P' from A (thread t owns token row t), then the
-//                output of the previous chunk
+//                output of the previous chunk (256-bit stores when the output
+//                is 32-byte aligned)
 //   warps 8..15  state group: W V split, in-place decay of S, the bf16 copy of
-//                S for MMA3, the final state; two warps per TMEM lane
+//                S (S') for MMA3, the final state; two warps per TMEM lane
 //                quadrant, each owning 32 of the 64 state columns
-// TMEM: A/P' 2x128, O1 64, O2 2x64, S 64 = 512 columns.  Every mbarrier wait
-// is bounded in wall time; on timeout the kernel flags the device status word,
-// stops issuing work, releases TMEM and returns.
+// TMEM: A/P' 2x128, O 2x64, S 64 (columns 384..447 unused) of 512.  Every
+// mbarrier wait is bounded in wall time; on timeout the kernel flags the
+// device status word, stops issuing work, releases TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -101,14 +110,13 @@ static_assert(kOffBar % 8 == 0 && kOffGate % 16 == 0, "alignment");
 
 // TMEM column map
 constexpr uint32_t kColA = 0;      // 2 x 128: A = Q K^T (fp32), then P' (bf16 pairs) in place
-constexpr uint32_t kColO1 = 256;   // 64
-constexpr uint32_t kColO2 = 320;   // 2 x 64
+constexpr uint32_t kColO = 256;    // 2 x 64: O = Q S' + P' (W V), per chunk parity
 constexpr uint32_t kColS = 448;    // 64: the running state slice, fp32
 
 enum Bar {
   kQKFull0 = 0, kQKFull1, kQKEmpty0, kQKEmpty1, kVFull, kVEmpty, kAFull0, kAFull1,
   kAFree0, kAFree1, kPFull, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady, kSbFull,
-  kSbFree, kO1Full, kO1Free, kO2Full0, kO2Full1, kO2Free0, kO2Free1, kGReady0,
+  kSbFree, kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kGReady0,
   kGFree0 = kGReady0 + kSlots, kNumBars = kGFree0 + kSlots
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
@@ -126,6 +134,7 @@ struct TcParams {
   float* final_state;
   const int32_t* cu_seqlens;
   int B, H, T, DV, nslices;
+  int out_v8;  // out is 32-byte aligned: 256-bit stores
   unsigned* status;
 };
 
@@ -140,8 +149,8 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 // part (G2s: the chunk's log2 prefix sums); otherwise the plain causal mask.
 // The two variants are separate bodies so that neither pays for the other.
 template <bool WIDE>
-__device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float G2,
-                                        const float* G2s) {
+__device__ __forceinline__ void build_p_body(uint32_t a_row, int q4, int r, float G2,
+                                             const float* G2s) {
   uint32_t a[32], dlo[16];
   tmem_ld_32x32b_x32(a_row, a);
 #pragma unroll 1
@@ -192,6 +201,14 @@ __device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float G2,
     }
   }
 }
+__device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float G2) {
+  build_p_body<false>(a_row, q4, r, G2, nullptr);
+}
+// wide chunks are rare: their variant stays out of line
+__device__ __noinline__ void build_p_wide(uint32_t a_row, int q4, int r, float G2,
+                                          const float* G2s) {
+  build_p_body<true>(a_row, q4, r, G2, G2s);
+}
 
 template <bool OUTF32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -222,7 +239,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = 0; i < kNumBars; ++i) {
       // group barriers take one arrival per warp (see warp_arrive)
       uint32_t cnt = 1;
-      if (i == kPFull || i == kO1Free || i == kO2Free0 || i == kO2Free1) cnt = kMaskWarps;
+      if (i == kPFull || i == kOFree0 || i == kOFree1) cnt = kMaskWarps;
       if (i == kVtFull0 || i == kVtFull1 || i == kSReady || i == kSbFull) cnt = kStateWarps;
       // gate slots are released by both groups and the MMA2 issuer
       if (i >= kGFree0 && i < kGFree0 + kSlots) cnt = kMaskWarps + kStateWarps + 1;
@@ -321,16 +338,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(&bars[kSFull]);  // S = S_c
         if (!wait(kSbFull, ph(c))) break;
-        if (c >= 2 && !wait(kO2Free0 + st, ph((c >> 1) - 1))) break;
+        if (c >= 2 && !wait(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
         tc_fence_after();
 #pragma unroll 1
         for (int kk = 0; kk < kDK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-          mma_bf16(tmem + kColO2 + st * kDVS, sdesc_sw128(q_s + off, 16, 1024),
+          mma_bf16(tmem + kColO + st * kDVS, sdesc_sw128(q_s + off, 16, 1024),
                    sdesc_sw128(sb + kk * 2048, kPanel, 1024), kIdQS, kk > 0);
         }
-        mma_commit(&bars[kSbFree]);         // S_{c-1} (bf16) read
-        mma_commit(&bars[kO2Full0 + st]);   // O2(c) complete
+        mma_commit(&bars[kSbFree]);         // S' (bf16) read
+        mma_commit(&bars[kO3Full0 + st]);   // O = Q S' written
         mma_commit(&bars[kQKEmpty0 + st]);  // Q(c), K(c) no longer read
         if (c + 1 < nch) ok = mma1(c + 1);
       }
@@ -341,7 +358,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
         if (!wait(kPFull, ph(c))) break;
-        if (c >= 1 && !wait(kO1Free, ph(c - 1))) break;
+        if (!wait(kO3Full0 + st, ph(c >> 1))) break;  // MMA3(c) first, then accumulate
         if (!wait(kVtFull0 + st, ph(c >> 1))) break;  // W V (and V) of chunk c ready
         tc_fence_after();
         const bool wide = slot_of(c)[kSlotWide] != 0.f;
@@ -354,13 +371,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll 1
         for (int kk = 0; kk < kC / 16; ++kk) {
           const uint64_t bhi = sdesc_sw128(vhi + kk * 2048, kPanel, 1024);
-          mma_bf16_tmem_a(tmem + kColO1, a_p + 8 * kk, bhi, kIdPV, kk > 0);
-          mma_bf16_tmem_a(tmem + kColO1, a_p + 64 + 8 * kk, bhi, kIdPV, 1);
+          const uint32_t d = tmem + kColO + st * kDVS;
+          mma_bf16_tmem_a(d, a_p + 8 * kk, bhi, kIdPV, 1);
+          mma_bf16_tmem_a(d, a_p + 64 + 8 * kk, bhi, kIdPV, 1);
           if (!wide)
-            mma_bf16_tmem_a(tmem + kColO1, a_p + 8 * kk,
-                            sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdPV, 1);
+            mma_bf16_tmem_a(d, a_p + 8 * kk, sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdPV, 1);
         }
-        mma_commit(&bars[kO1Full]);
+        mma_commit(&bars[kOFull0 + st]);
         mma_commit(&bars[kAFree0 + st]);   // A/P' buffer
         mma_commit(&bars[kVtFree0 + st]);  // (W V) hi/lo buffers
         if (wide) mma_commit(&bars[kVEmpty]);
@@ -417,78 +434,103 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const float scale = p.scale;
 
-    // output of chunk c: o = scale (f_t O1 + exp(G_t) O2[c & 1]), f_t = exp(G_t - G_L)
-    // (1 on wide chunks, whose O1 already carries the decay)
-    auto output = [&](int c, float G2t, float f) -> bool {
-      if (!wait(kO1Full, ph(c))) return false;                  // MMA2(c)
-      if (!wait(kO2Full0 + (c & 1), ph(c >> 1))) return false;  // MMA3(c)
+    // output of chunk c: o = scale f_t O[c & 1], f_t = exp(G_t - G_L) (1 on wide
+    // chunks, whose O carries the decay already)
+    auto output = [&](int c, float f) -> bool {
+      if (!wait(kOFull0 + (c & 1), ph(c >> 1))) return false;  // MMA2(c)
       tc_fence_after();
       const int n = min(kC, len - c * kC);
-      const float s1 = scale * f, s2 = scale * exp2f(G2t);
+      const float s1 = scale * f;
       const long long rowbase = start + (long long)c * kC;
       const size_t off = ((size_t)(rowbase + r) * p.H + h) * p.DV + (size_t)sl * kDVS;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {
-        uint32_t o1[16], o2[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + kColO1 + 16 * part, o1);
-        tmem_ld_32x32b_x16(tmem + lane_off + kColO2 + (c & 1) * kDVS + 16 * part, o2);
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + lane_off + kColO + (c & 1) * kDVS + 16 * part, v);
         tmem_ld_wait();
         if (part == 3) {
           tc_fence_before();
-          warp_arrive(kO1Free);
-          warp_arrive(kO2Free0 + (c & 1));
+          warp_arrive(kOFree0 + (c & 1));
         }
         float o[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          o[j] = fmaf(s2, __uint_as_float(o2[j]), s1 * __uint_as_float(o1[j]));
+        for (int j = 0; j < 16; ++j) o[j] = s1 * __uint_as_float(v[j]);
         if (r < n) {
           if constexpr (OUTF32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off) + 4 * part;
+            float* dst = static_cast<float*>(p.out) + off + 16 * part;
+            if (p.out_v8) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+              for (int j = 0; j < 2; ++j)
+                st_global_v8(dst + 8 * j, __float_as_uint(o[8 * j]), __float_as_uint(o[8 * j + 1]),
+                             __float_as_uint(o[8 * j + 2]), __float_as_uint(o[8 * j + 3]),
+                             __float_as_uint(o[8 * j + 4]), __float_as_uint(o[8 * j + 5]),
+                             __float_as_uint(o[8 * j + 6]), __float_as_uint(o[8 * j + 7]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                reinterpret_cast<float4*>(dst)[j] =
+                    make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
           } else {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off) + 2 * part;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + off + 16 * part;
+            uint32_t w[8];
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              dst[j] = make_uint4(pack_bf16x2(o[8 * j], o[8 * j + 1]),
-                                  pack_bf16x2(o[8 * j + 2], o[8 * j + 3]),
-                                  pack_bf16x2(o[8 * j + 4], o[8 * j + 5]),
-                                  pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
+            for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
+            if (p.out_v8) {
+              st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            } else {
+              reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
           }
         }
       }
       return true;
     };
 
-    float G2prev = 0.f, fprev = 1.f;
-    bool ok = true;
-    for (int c = 0; c < nch; ++c) {
-      const int st = c & 1;
-      const float* slot = slot_of(c);
-      if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) { ok = false; break; }
-      const float G2 = slot[kSlotG2 + r];
-      const float total = slot[kSlotTotal];
-      const bool wide = slot[kSlotWide] != 0.f;
-      if (!wait(kAFull0 + st, ph(c >> 1))) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t a_row = tmem + lane_off + kColA + st * 128;
-      if (wide)
-        build_p<true>(a_row, q4, r, G2, slot + kSlotG2);
-      else
-        build_p<false>(a_row, q4, r, G2, slot + kSlotG2);
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(kPFull);
-      warp_arrive(kGFree0 + c % kSlots);
-      // output of the previous chunk (its MMA2 ran while this P' was built)
-      if (c >= 1 && !output(c - 1, G2prev, fprev)) { ok = false; break; }
-      G2prev = G2;
-      fprev = wide ? 1.f : exp2f(G2 - total);
+    // iteration c: P' of chunk c, then the output of chunk c - 1 (its MMA2 ran
+    // while this P' was built)
+    float fprev = 1.f;
+    for (int c = 0; c <= nch; ++c) {
+      float f = 1.f;
+      if (c < nch) {
+        const int st = c & 1;
+        const float* slot = slot_of(c);
+        if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) break;
+        const float G2 = slot[kSlotG2 + r];
+        const float total = slot[kSlotTotal];
+        const bool wide = slot[kSlotWide] != 0.f;
+        f = wide ? 1.f : exp2f(G2 - total);
+        if (!wait(kAFull0 + st, ph(c >> 1))) break;
+        tc_fence_after();
+        const uint32_t a_row = tmem + lane_off + kColA + st * 128;
+        if (wide) {
+          build_p_wide(a_row, q4, r, G2, slot + kSlotG2);
+          // O = Q S_{c-1} so far: scale row t by exp(G_t) before MMA2 adds P V
+          if (!wait(kO3Full0 + st, ph(c >> 1))) break;
+          tc_fence_after();
+          const float e = exp2f(G2);
+          const uint32_t o_row = tmem + lane_off + kColO + st * kDVS;
+#pragma unroll 1
+          for (int part = 0; part < 4; ++part) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(o_row + 16 * part, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(e * __uint_as_float(v[j]));
+            tmem_st_32x32b_x16(o_row + 16 * part, v);
+          }
+        } else {
+          build_p(a_row, q4, r, G2);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(kPFull);
+        warp_arrive(kGFree0 + c % kSlots);
+      }
+      if (c >= 1 && !output(c - 1, fprev)) break;
+      fprev = f;
     }
-    if (ok && nch >= 1) output(nch - 1, G2prev, fprev);
   } else {
     // ----------------------------------------------------------- state group
     const int q4 = warp & 3;
@@ -502,13 +544,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     // W V split of chunk c (this thread: token row r, V columns 32 half .. +31)
     // into bf16 hi and lo (buffers c & 1).  Returns the chunk's total log2 decay.
-    auto split_wv = [&](int c, float& total) -> bool {
+    auto split_wv = [&](int c, float& total, bool& wide) -> bool {
       const int n = min(kC, len - c * kC);
       if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) return false;
       const float* slot = slot_of(c);
       const float G2r = slot[kSlotG2 + r];
       total = slot[kSlotTotal];
-      const bool wide = slot[kSlotWide] != 0.f;
+      wide = slot[kSlotWide] != 0.f;
       warp_arrive(kGFree0 + c % kSlots);
       // MMA2(c-2) done; MMA4(c-2) is done too (its S was passed before this call)
       if (c >= 2 && !wait(kVtFree0 + (c & 1), ph((c >> 1) - 1))) return false;
@@ -517,7 +559,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       uint8_t* hi_s = smem + kOffVhi + (c & 1) * kTile;
       uint8_t* lo_s = smem + kOffVlo + (c & 1) * kTile;
       const float w = (r < n) ? exp2f(total - G2r) : 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         const uint32_t off = sw128_offset(r, 4 * half + cc);
         const uint4 raw = *reinterpret_cast<const uint4*>(v_s + off);
@@ -542,56 +584,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       return true;
     };
 
-    // S (TMEM) -> bf16 copy for MMA3 (to_sb), scaled by `decay` back into TMEM
-    // for the next MMA4 (rescale), and/or out to the final state (final_out).
-    auto pass_state = [&](float decay, bool to_sb, bool rescale, float* final_out) {
-#pragma unroll
+    // One pass over this thread's 32 columns of S_c (c = -1: the initial state).
+    // Not last: exp(G_L(c+1)) S_c back into TMEM for MMA4(c+1), and its bf16
+    // copy S' for MMA3(c+1) (S_c itself when chunk c+1 is wide).  Last: S_c out
+    // to the final state.
+    auto pass_state = [&](int c, float decay, bool last, bool next_wide) {
+#pragma unroll 1
       for (int q = 0; q < 2; ++q) {  // 16 columns at a time
         uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
-        tmem_ld_wait();
-        if (to_sb) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
-            *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 4 * half + 2 * q + cc)) =
-                make_uint4(
-                    pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-        }
-        if (final_out) {
-          float4* dst = reinterpret_cast<float4*>(final_out) + 4 * q;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        }
-        if (rescale) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(decay * __uint_as_float(v[j]));
-          tmem_st_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
-        }
-      }
-      if (rescale) tmem_st_wait();
-    };
-
-    bool ok = true;
-    if (nch == 0) {
-      // empty sequence: the final state is the initial state
-      if (final_row) {
-#pragma unroll 4
-        for (int j = 0; j < 32; ++j) final_row[j] = p.init_state ? p.init_state[st_off + j] : 0.f;
-      }
-    } else {
-      // S_{-1} = initial state: bf16 copy for MMA3(0); TMEM gets exp(G_L(0)) S_{-1}
-      float total = 0.f;
-      ok = split_wv(0, total);
-      if (ok) {
-        const float decay = exp2f(total);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t v[16];
+        if (c < 0) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
             const float4 x = p.init_state
@@ -601,46 +602,71 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             v[j] = __float_as_uint(x.x); v[j + 1] = __float_as_uint(x.y);
             v[j + 2] = __float_as_uint(x.z); v[j + 3] = __float_as_uint(x.w);
           }
+        } else {
+          tmem_ld_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
+          tmem_ld_wait();
+        }
+        if (last) {
+          if (final_row) {
+            float4* dst = reinterpret_cast<float4*>(final_row) + 4 * q;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        } else {
+          float sv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x = __uint_as_float(v[j]);
+            v[j] = __float_as_uint(decay * x);
+            sv[j] = next_wide ? x : __uint_as_float(v[j]);
+          }
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
             *reinterpret_cast<uint4*>(sb_row + sw128_offset(r, 4 * half + 2 * q + cc)) =
-                make_uint4(
-                    pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                    pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(decay * __uint_as_float(v[j]));
+                make_uint4(pack_bf16x2(sv[8 * cc], sv[8 * cc + 1]),
+                           pack_bf16x2(sv[8 * cc + 2], sv[8 * cc + 3]),
+                           pack_bf16x2(sv[8 * cc + 4], sv[8 * cc + 5]),
+                           pack_bf16x2(sv[8 * cc + 6], sv[8 * cc + 7]));
           tmem_st_32x32b_x16(tmem + lane_off + kColS + 32 * half + 16 * q, v);
         }
-        tmem_st_wait();
+      }
+      if (!last) tmem_st_wait();
+    };
+
+    if (nch == 0) {
+      // empty sequence: the final state is the initial state
+      if (final_row) {
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) final_row[j] = p.init_state ? p.init_state[st_off + j] : 0.f;
+      }
+    }
+    // iteration c: the W V split of chunk c + 1 first (MMA4(c+1) needs it
+    // together with S_c), then the pass over S_c
+    for (int c = -1; c < nch; ++c) {
+      const bool last = c + 1 == nch;
+      float next_total = 0.f;
+      bool next_wide = false;
+      if (!last && !split_wv(c + 1, next_total, next_wide)) break;
+      if (c >= 0) {
+        if (!wait(kSFull, ph(c))) break;  // S = S_c
+        tc_fence_after();
+        if (!last && !wait(kSbFree, ph(c))) break;  // MMA3(c) has read S_{c-1}
+      }
+      pass_state(c, last ? 1.f : exp2f(next_total), last, next_wide);
+      if (!last) {
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(kSbFull);
         warp_arrive(kSReady);
-      }
-      for (int c = 0; c < nch && ok; ++c) {
-        // the next chunk's W V first: MMA4 of chunk c+1 needs it together with S_c
-        float next_total = 0.f;
-        if (c + 1 < nch && !split_wv(c + 1, next_total)) { ok = false; break; }
-        if (!wait(kSFull, ph(c))) { ok = false; break; }  // S = S_c
-        tc_fence_after();
-        if (c + 1 < nch) {
-          if (!wait(kSbFree, ph(c))) { ok = false; break; }  // MMA3(c) has read S_{c-1}
-          pass_state(exp2f(next_total), true, true, nullptr);
-          fence_proxy_async_smem();
-          tc_fence_before();
-          warp_arrive(kSbFull);
-          warp_arrive(kSReady);
-        } else {
-          pass_state(1.f, false, false, final_row);
-        }
       }
     }
   }
 
   if (*abort_flag) {
     // give copies and MMAs that may still be in flight time to land
+#pragma unroll 1
     for (int i = 0; i < 1000; ++i) __nanosleep(1000);
   }
   tc_fence_before();
@@ -702,6 +728,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
   p.final_state = a.final_state; p.cu_seqlens = a.cu_seqlens;
   p.B = a.B; p.H = a.H; p.T = a.T; p.DV = a.dv; p.nslices = a.dv / kDVS;
   p.status = a.status;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   const long long ctas = (long long)a.B * a.H * p.nslices;
   if (a.fp32_out) {
     auto kern = chunk_tc_kernel<true>;

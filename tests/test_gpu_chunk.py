@@ -172,6 +172,26 @@ def test_strong_and_weak_decay(cuda_ok, mu):
     check(x, out, fin, *run_ref(x))
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_output_buffer_only_16_byte_aligned(cuda_ok, out_dtype):
+    """An output that is 16- but not 32-byte aligned takes 128-bit stores; the
+    result is bit-identical to the one written into a fresh (aligned) tensor."""
+    gla = _gla()
+    x = small(B=2, T=300, H=2)
+    args = (cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]))
+    kw = dict(scale=x["scale"], init_state=cuda(x["init_state"]), chunk=128)
+    ref, _ = gla.chunk_fwd(*args, out_dtype=out_dtype, **kw)
+    shift = 16 // torch.empty((), dtype=out_dtype).element_size()
+    buf = torch.full((ref.numel() + 2 * shift,), float("nan"), dtype=out_dtype, device="cuda")
+    out = buf[shift:shift + ref.numel()].view(ref.shape)
+    assert out.data_ptr() % 32 == 16
+    got, _ = gla.chunk_fwd(*args, out=out, out_dtype=out_dtype, **kw)
+    gla.status_sync()
+    assert got.data_ptr() == out.data_ptr()
+    assert torch.equal(got, ref)
+    assert torch.isnan(buf[:shift]).all() and torch.isnan(buf[shift + ref.numel():]).all()
+
+
 def test_packed_sequences_with_empty_and_short_ones(cuda_ok):
     x = small(B=0, lengths=[300, 1, 0, 128, 129, 5, 700], H=3, init_std=0.05)
     out, fin = run_gpu(x)
