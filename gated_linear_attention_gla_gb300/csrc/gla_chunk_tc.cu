@@ -42,17 +42,22 @@
 // read by then.
 //
 // Resources and their release points (the chunk pipeline):
-//   Q, K tiles      2-stage ring, free once MMA3 of the chunk has run
+//   Q, K tiles      2-stage ring, free once MMA1 and MMA3/MMA4 of the chunk
+//                   have run (one commit from each issuer)
 //   V tile          single buffer, free once the W V split has read it (wide
 //                   chunks: once MMA2 has run)
 //   (W V) hi, lo    2 buffers each, free once MMA2 (and MMA4) have run
-//   S'              1 buffer, bf16 (B operand of MMA3)
+//   S'              1 buffer, bf16 (B operand of MMA3), rewritten once MMA4
+//                   (issued after MMA3) has completed
 //   O               2 buffers in TMEM, free once the output has read them
 // Roles (16 warps):
-//   warp 0       TMA producer
-//   warp 1       TMEM allocator; issues MMA1, MMA4, MMA3 (the "front")
-//   warp 2       issues MMA2 (the "back")
-//   warp 3       gate warp: prefix sums of g and the chunk's flags, ahead
+//   warp 0       producer: prefix sums of g and the chunk's flags (all lanes,
+//                into a 3-slot ring), then the TMA loads (lane 0)
+//   warp 1       TMEM allocator; issues MMA1
+//   warp 2       issues MMA2
+//   warp 3       issues MMA3 then MMA4 (the state chain)
+// Each MMA issuer waits only for its own operands, so no chain holds up
+// another one's issue.
 //   warps 4..7   mask group: P' from A (thread t owns token row t), then the
 //                output of the previous chunk (256-bit stores when the output
 //                is 32-byte aligned)
@@ -115,8 +120,8 @@ constexpr uint32_t kColS = 448;    // 64: the running state slice, fp32
 
 enum Bar {
   kQKFull0 = 0, kQKFull1, kQKEmpty0, kQKEmpty1, kVFull, kVEmpty, kAFull0, kAFull1,
-  kAFree0, kAFree1, kPFull, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady, kSbFull,
-  kSbFree, kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kGReady0,
+  kAFree0, kAFree1, kPFull, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady,
+  kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kGReady0,
   kGFree0 = kGReady0 + kSlots, kNumBars = kGFree0 + kSlots
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
@@ -240,7 +245,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // group barriers take one arrival per warp (see warp_arrive)
       uint32_t cnt = 1;
       if (i == kPFull || i == kOFree0 || i == kOFree1) cnt = kMaskWarps;
-      if (i == kVtFull0 || i == kVtFull1 || i == kSReady || i == kSbFull) cnt = kStateWarps;
+      if (i == kVtFull0 || i == kVtFull1 || i == kSReady) cnt = kStateWarps;
+      // both MMA issuers that read Q and K commit to the stage's empty barrier
+      if (i == kQKEmpty0 || i == kQKEmpty1) cnt = 2;
       // gate slots are released by both groups and the MMA2 issuer
       if (i >= kGFree0 && i < kGFree0 + kSlots) cnt = kMaskWarps + kStateWarps + 1;
       mbar_init(&bars[i], cnt);
@@ -279,113 +286,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   auto slot_of = [&](int c) -> float* { return gate_ring + (c % kSlots) * kSlotFloats; };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int bidx = packed ? 0 : s;
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        const int row = packed ? (int)(start + (long long)c * kC) : c * kC;
-        if (c >= 2 && !wait(kQKEmpty0 + st, ph((c >> 1) - 1))) break;
-        uint8_t* q_s = smem + st * kQKStage;
-        uint8_t* k_s = q_s + kQBytes;
-        mbar_arrive_expect_tx(&bars[kQKFull0 + st], kQKStage);
-#pragma unroll
-        for (int pn = 0; pn < kDK / 64; ++pn) {
-          tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
-          tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
-        }
-        if (c >= 1 && !wait(kVEmpty, ph(c - 1))) break;
-        mbar_arrive_expect_tx(&bars[kVFull], kTile);
-        tma_load_4d(smem + kOffV, &tmV, &bars[kVFull], sl * kDVS, h, row, bidx);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------- MMA front: 1, 4, 3
-    // Order: MMA1(0); then per chunk c: MMA4(c), MMA3(c), MMA1(c+1).
-    if (lane == 0) {
-      const uint32_t sb = sbase + kOffSb;
-      auto mma1 = [&](int c) -> bool {
-        const int st = c & 1;
-        const uint32_t q_s = sbase + st * kQKStage;
-        const uint32_t k_s = q_s + kQBytes;
-        if (!wait(kQKFull0 + st, ph(c >> 1))) return false;
-        if (c >= 2 && !wait(kAFree0 + st, ph((c >> 1) - 1))) return false;
-        tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kDK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-          mma_bf16(tmem + kColA + st * 128, sdesc_sw128(q_s + off, 16, 1024),
-                   sdesc_sw128(k_s + off, 16, 1024), kIdQK, kk > 0);
-        }
-        mma_commit(&bars[kAFull0 + st]);
-        return true;
-      };
-      bool ok = nch == 0 || mma1(0);
-      for (int c = 0; c < nch && ok; ++c) {
-        const int st = c & 1;
-        const uint32_t q_s = sbase + st * kQKStage;
-        const uint32_t k_s = q_s + kQBytes;
-        const uint32_t vhi = sbase + kOffVhi + st * kTile;
-        const uint32_t vlo = sbase + kOffVlo + st * kTile;
-        if (!wait(kVtFull0 + st, ph(c >> 1))) break;
-        if (!wait(kSReady, ph(c))) break;  // S holds exp(G_L) S_{c-1}
-        tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t adesc = sdesc_sw128(k_s + kk * 2048, kPanel, 1024);
-          mma_bf16(tmem + kColS, adesc, sdesc_sw128(vhi + kk * 2048, kPanel, 1024), kIdKV, 1);
-          mma_bf16(tmem + kColS, adesc, sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdKV, 1);
-        }
-        mma_commit(&bars[kSFull]);  // S = S_c
-        if (!wait(kSbFull, ph(c))) break;
-        if (c >= 2 && !wait(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
-        tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kDK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-          mma_bf16(tmem + kColO + st * kDVS, sdesc_sw128(q_s + off, 16, 1024),
-                   sdesc_sw128(sb + kk * 2048, kPanel, 1024), kIdQS, kk > 0);
-        }
-        mma_commit(&bars[kSbFree]);         // S' (bf16) read
-        mma_commit(&bars[kO3Full0 + st]);   // O = Q S' written
-        mma_commit(&bars[kQKEmpty0 + st]);  // Q(c), K(c) no longer read
-        if (c + 1 < nch) ok = mma1(c + 1);
-      }
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------------- MMA back: 2
-    if (lane == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (!wait(kPFull, ph(c))) break;
-        if (!wait(kO3Full0 + st, ph(c >> 1))) break;  // MMA3(c) first, then accumulate
-        if (!wait(kVtFull0 + st, ph(c >> 1))) break;  // W V (and V) of chunk c ready
-        tc_fence_after();
-        const bool wide = slot_of(c)[kSlotWide] != 0.f;
-        mbar_arrive(&bars[kGFree0 + c % kSlots]);
-        const uint32_t a_p = tmem + kColA + st * 128;  // P': k-step kk at column 8 kk
-        // P' hi at column 8 kk, the diagonal lo parts at 64 + 8 kk; B is the raw V
-        // on a wide chunk, else (W V) hi and lo
-        const uint32_t vhi = wide ? sbase + kOffV : sbase + kOffVhi + st * kTile;
-        const uint32_t vlo = sbase + kOffVlo + st * kTile;
-#pragma unroll 1
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t bhi = sdesc_sw128(vhi + kk * 2048, kPanel, 1024);
-          const uint32_t d = tmem + kColO + st * kDVS;
-          mma_bf16_tmem_a(d, a_p + 8 * kk, bhi, kIdPV, 1);
-          mma_bf16_tmem_a(d, a_p + 64 + 8 * kk, bhi, kIdPV, 1);
-          if (!wide)
-            mma_bf16_tmem_a(d, a_p + 8 * kk, sdesc_sw128(vlo + kk * 2048, kPanel, 1024), kIdPV, 1);
-        }
-        mma_commit(&bars[kOFull0 + st]);
-        mma_commit(&bars[kAFree0 + st]);   // A/P' buffer
-        mma_commit(&bars[kVtFree0 + st]);  // (W V) hi/lo buffers
-        if (wide) mma_commit(&bars[kVEmpty]);
-      }
-    }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------- gate warp
-    // lane l owns tokens 4l .. 4l+3 of each chunk
+    // ------------------------------------------- producer: gate sums and TMA
+    // All lanes: prefix sums of g for chunk c (lane l owns tokens 4l .. 4l+3)
+    // into the gate ring; lane 0: the TMA loads of chunk c.
     auto load4 = [&](int c, float (&gv)[4]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -394,14 +297,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                      : 0.f;
       }
     };
+    const int bidx = packed ? 0 : s;
     float gnext[4];
     load4(0, gnext);
     for (int c = 0; c < nch; ++c) {
+      bool ok = true;
       float gv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) gv[i] = gnext[i];
       load4(c + 1, gnext);
-      if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) break;
+      if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) ok = false;
+      if (__any_sync(0xffffffffu, !ok)) break;
       float* slot = slot_of(c);
       float run[4];
       run[0] = gv[0];
@@ -426,6 +332,120 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         slot[kSlotWide] = (first - total > kWideSpan) ? 1.f : 0.f;
       }
       warp_arrive(kGReady0 + c % kSlots);
+      if (lane == 0) {
+        const int st = c & 1;
+        const int row = packed ? (int)(start + (long long)c * kC) : c * kC;
+        if (c >= 2 && !wait(kQKEmpty0 + st, ph((c >> 1) - 1))) ok = false;
+        if (ok) {
+          uint8_t* q_s = smem + st * kQKStage;
+          uint8_t* k_s = q_s + kQBytes;
+          mbar_arrive_expect_tx(&bars[kQKFull0 + st], kQKStage);
+#pragma unroll
+          for (int pn = 0; pn < kDK / 64; ++pn) {
+            tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
+            tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
+          }
+        }
+        if (ok && c >= 1 && !wait(kVEmpty, ph(c - 1))) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(&bars[kVFull], kTile);
+          tma_load_4d(smem + kOffV, &tmV, &bars[kVFull], sl * kDVS, h, row, bidx);
+        }
+      }
+      if (__any_sync(0xffffffffu, !ok)) break;
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA1 issuer
+    if (lane == 0) {
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        const uint32_t q_s = sbase + st * kQKStage;
+        const uint32_t k_s = q_s + kQBytes;
+        if (!wait(kQKFull0 + st, ph(c >> 1))) break;
+        if (c >= 2 && !wait(kAFree0 + st, ph((c >> 1) - 1))) break;
+        tc_fence_after();
+        const uint64_t qd = sdesc_sw128(q_s, 16, 1024), kd = sdesc_sw128(k_s, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kDK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+          mma_bf16(tmem + kColA + st * 128, desc_add(qd, off), desc_add(kd, off), kIdQK, kk > 0);
+        }
+        mma_commit(&bars[kAFull0 + st]);
+        mma_commit(&bars[kQKEmpty0 + st]);  // this issuer is done with Q(c), K(c)
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------- MMA back: 2
+    if (lane == 0) {
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        if (!wait(kPFull, ph(c))) break;
+        if (!wait(kO3Full0 + st, ph(c >> 1))) break;  // MMA3(c) first, then accumulate
+        if (!wait(kVtFull0 + st, ph(c >> 1))) break;  // W V (and V) of chunk c ready
+        tc_fence_after();
+        const bool wide = slot_of(c)[kSlotWide] != 0.f;
+        mbar_arrive(&bars[kGFree0 + c % kSlots]);
+        const uint32_t a_p = tmem + kColA + st * 128;  // P': k-step kk at column 8 kk
+        // P' hi at column 8 kk, the diagonal lo parts at 64 + 8 kk; B is the raw V
+        // on a wide chunk, else (W V) hi and lo
+        const uint64_t hd =
+            sdesc_sw128(wide ? sbase + kOffV : sbase + kOffVhi + st * kTile, kPanel, 1024);
+        const uint64_t ld = sdesc_sw128(sbase + kOffVlo + st * kTile, kPanel, 1024);
+        const uint32_t d = tmem + kColO + st * kDVS;
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16_tmem_a(d, a_p + 8 * kk, desc_add(hd, kk * 2048), kIdPV, 1);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16_tmem_a(d, a_p + 64 + 8 * kk, desc_add(hd, kk * 2048), kIdPV, 1);
+        if (!wide) {
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)
+            mma_bf16_tmem_a(d, a_p + 8 * kk, desc_add(ld, kk * 2048), kIdPV, 1);
+        }
+        mma_commit(&bars[kOFull0 + st]);
+        mma_commit(&bars[kAFree0 + st]);   // A/P' buffer
+        mma_commit(&bars[kVtFree0 + st]);  // (W V) hi/lo buffers
+        if (wide) mma_commit(&bars[kVEmpty]);
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------- MMA3 / MMA4 issuer
+    // MMA3(c) (O = Q S') first, so that MMA2 can follow early, then MMA4(c)
+    // (S += K^T (W V)); the commit after MMA4 covers both.
+    if (lane == 0) {
+      const uint32_t sb = sbase + kOffSb;
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        const uint32_t q_s = sbase + st * kQKStage;
+        const uint32_t k_s = q_s + kQBytes;
+        if (!wait(kQKFull0 + st, ph(c >> 1))) break;
+        if (!wait(kVtFull0 + st, ph(c >> 1))) break;
+        if (!wait(kSReady, ph(c))) break;  // S' in smem, exp(G_L) S_{c-1} in TMEM
+        if (c >= 2 && !wait(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
+        tc_fence_after();
+        {
+          const uint64_t qd = sdesc_sw128(q_s, 16, 1024), sd = sdesc_sw128(sb, kPanel, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kDK / 16; ++kk)
+            mma_bf16(tmem + kColO + st * kDVS, desc_add(qd, (kk >> 2) * kPanel + (kk & 3) * 32),
+                     desc_add(sd, kk * 2048), kIdQS, kk > 0);
+        }
+        mma_commit(&bars[kO3Full0 + st]);  // O = Q S' written
+        {
+          const uint64_t kd = sdesc_sw128(k_s, kPanel, 1024);
+          const uint64_t hd = sdesc_sw128(sbase + kOffVhi + st * kTile, kPanel, 1024);
+          const uint64_t ld = sdesc_sw128(sbase + kOffVlo + st * kTile, kPanel, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)
+            mma_bf16(tmem + kColS, desc_add(kd, kk * 2048), desc_add(hd, kk * 2048), kIdKV, 1);
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)
+            mma_bf16(tmem + kColS, desc_add(kd, kk * 2048), desc_add(ld, kk * 2048), kIdKV, 1);
+        }
+        mma_commit(&bars[kSFull]);          // S = S_c, and S' no longer read
+        mma_commit(&bars[kQKEmpty0 + st]);  // this issuer is done with Q(c), K(c)
+      }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ mask group
@@ -650,15 +670,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       bool next_wide = false;
       if (!last && !split_wv(c + 1, next_total, next_wide)) break;
       if (c >= 0) {
-        if (!wait(kSFull, ph(c))) break;  // S = S_c
+        if (!wait(kSFull, ph(c))) break;  // S = S_c; MMA3(c) has read S'
         tc_fence_after();
-        if (!last && !wait(kSbFree, ph(c))) break;  // MMA3(c) has read S_{c-1}
       }
       pass_state(c, last ? 1.f : exp2f(next_total), last, next_wide);
       if (!last) {
         fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(kSbFull);
         warp_arrive(kSReady);
       }
     }

@@ -215,6 +215,13 @@ __device__ __forceinline__ void tmem_ld_wait_x32(uint32_t (&r)[32]) {
 }
 
 // ----------------------------------------------------- descriptors (UMMA)
+// The descriptor of a tile `bytes` further on (a multiple of 16): the start
+// address field holds the shared address / 16 and does not overflow below
+// 256 KB.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4 bits 46-47 descriptor version (1)
