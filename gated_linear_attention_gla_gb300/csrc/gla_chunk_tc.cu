@@ -32,7 +32,9 @@
 // the previous chunk's output to be read.  A wide chunk keeps S' = S and the
 // mask group scales O's row t by exp(G_t) between MMA3 and MMA2.
 // W V is carried as two bf16 tiles, hi + lo (hi = W V rounded, lo = the
-// rest), and both MMA4 and MMA2 take the two passes.  P' = causal(A) is
+// rest), and MMA2 takes both passes; MMA4 takes the lo pass only while the
+// decay still to come over the next two chunks is at least 2^-16 (else the
+// final state sees this chunk's rounding shrunk below 2^-25).  P' = causal(A) is
 // rounded to bf16 once, except on the four 32 x 32 diagonal blocks, where the
 // largest terms of a row sit under strong decay: there P' also has a lo part,
 // taken in a third MMA2 pass against (W V)_hi.  P' overwrites A in TMEM:
@@ -89,6 +91,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWideSpan = 96.f;      // log2 chunk decay span above which a chunk is "wide"
+constexpr float kLoCutoff = -16.f;     // log2 decay still to come below which MMA4 skips lo
 constexpr int kSlots = 3;              // gate ring: chunks c (mask), c + 1 (split), c + 2 (gate)
 constexpr uint32_t kBarState = 2;      // named barrier of the state group
 
@@ -102,8 +105,8 @@ constexpr uint32_t kOffV = 2 * kQKStage;
 constexpr uint32_t kOffVhi = kOffV + kTile;           // 2 buffers
 constexpr uint32_t kOffVlo = kOffVhi + 2 * kTile;     // 2 buffers
 constexpr uint32_t kOffSb = kOffVlo + 2 * kTile;      // dk rows x 128 B
-// gate slot (floats): G2[128] | total, wide, -, -
-constexpr int kSlotG2 = 0, kSlotTotal = 128, kSlotWide = 129, kSlotFloats = 132;
+// gate slot (floats): G2[128] | total, wide, need_lo, -
+constexpr int kSlotG2 = 0, kSlotTotal = 128, kSlotWide = 129, kSlotNeedLo = 130, kSlotFloats = 132;
 constexpr uint32_t kOffGate = kOffSb + kDK * 128;
 constexpr uint32_t kOffBar = kOffGate + kSlots * kSlotFloats * 4;
 constexpr uint32_t kBarBytes = 320;
@@ -297,15 +300,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                      : 0.f;
       }
     };
+    // sum over the warp of a per-lane value
+    auto warp_sum = [&](float x) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      return x;
+    };
     const int bidx = packed ? 0 : s;
-    float gnext[4];
+    // g of chunks c + 1 and c + 2 are loaded one and two iterations ahead: their
+    // totals decide whether MMA4(c) needs the lo half of W V (the final state
+    // sees chunk c's rounding scaled by the decay still to come)
+    float gnext[4], gnext2[4];
     load4(0, gnext);
+    load4(1, gnext2);
     for (int c = 0; c < nch; ++c) {
       bool ok = true;
       float gv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) gv[i] = gnext[i];
-      load4(c + 1, gnext);
+      for (int i = 0; i < 4; ++i) {
+        gv[i] = gnext[i];
+        gnext[i] = gnext2[i];
+      }
+      load4(c + 2, gnext2);
+      const float rest = warp_sum(gnext[0] + gnext[1] + gnext[2] + gnext[3]) +
+                         warp_sum(gnext2[0] + gnext2[1] + gnext2[2] + gnext2[3]);
       if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) ok = false;
       if (__any_sync(0xffffffffu, !ok)) break;
       float* slot = slot_of(c);
@@ -330,6 +348,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (lane == 0) {
         slot[kSlotTotal] = total;
         slot[kSlotWide] = (first - total > kWideSpan) ? 1.f : 0.f;
+        slot[kSlotNeedLo] = (rest * kLog2e < kLoCutoff) ? 0.f : 1.f;
       }
       warp_arrive(kGReady0 + c % kSlots);
       if (lane == 0) {
@@ -423,6 +442,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!wait(kVtFull0 + st, ph(c >> 1))) break;
         if (!wait(kSReady, ph(c))) break;  // S' in smem, exp(G_L) S_{c-1} in TMEM
         if (c >= 2 && !wait(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
+        // slot c stays until MMA2(c) has run, which needs this warp's MMA3(c)
+        if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) break;
+        const bool need_lo = slot_of(c)[kSlotNeedLo] != 0.f;
         tc_fence_after();
         {
           const uint64_t qd = sdesc_sw128(q_s, 16, 1024), sd = sdesc_sw128(sb, kPanel, 1024);
@@ -439,9 +461,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < kC / 16; ++kk)
             mma_bf16(tmem + kColS, desc_add(kd, kk * 2048), desc_add(hd, kk * 2048), kIdKV, 1);
+          if (need_lo) {
 #pragma unroll
-          for (int kk = 0; kk < kC / 16; ++kk)
-            mma_bf16(tmem + kColS, desc_add(kd, kk * 2048), desc_add(ld, kk * 2048), kIdKV, 1);
+            for (int kk = 0; kk < kC / 16; ++kk)
+              mma_bf16(tmem + kColS, desc_add(kd, kk * 2048), desc_add(ld, kk * 2048), kIdKV, 1);
+          }
         }
         mma_commit(&bars[kSFull]);          // S = S_c, and S' no longer read
         mma_commit(&bars[kQKEmpty0 + st]);  // this issuer is done with Q(c), K(c)
