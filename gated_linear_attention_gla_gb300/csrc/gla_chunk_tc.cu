@@ -123,7 +123,7 @@ constexpr uint32_t kColS = 448;    // 64: the running state slice, fp32
 
 enum Bar {
   kQKFull0 = 0, kQKFull1, kQKEmpty0, kQKEmpty1, kVFull, kVEmpty, kAFull0, kAFull1,
-  kAFree0, kAFree1, kPFull, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady,
+  kAFree0, kAFree1, kPFull0, kPFull1, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady,
   kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kGReady0,
   kGFree0 = kGReady0 + kSlots, kNumBars = kGFree0 + kSlots
 };
@@ -247,7 +247,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = 0; i < kNumBars; ++i) {
       // group barriers take one arrival per warp (see warp_arrive)
       uint32_t cnt = 1;
-      if (i == kPFull || i == kOFree0 || i == kOFree1) cnt = kMaskWarps;
+      if (i == kPFull0 || i == kPFull1 || i == kOFree0 || i == kOFree1) cnt = kMaskWarps;
       if (i == kVtFull0 || i == kVtFull1 || i == kSReady) cnt = kStateWarps;
       // both MMA issuers that read Q and K commit to the stage's empty barrier
       if (i == kQKEmpty0 || i == kQKEmpty1) cnt = 2;
@@ -398,7 +398,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (lane == 0) {
       for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
-        if (!wait(kPFull, ph(c))) break;
+        // one P' barrier per chunk parity: the mask group may finish P' of chunk
+        // c + 1 before this wait (P' of chunk c + 2 needs MMA2(c) first)
+        if (!wait(kPFull0 + st, ph(c >> 1))) break;
         if (!wait(kO3Full0 + st, ph(c >> 1))) break;  // MMA3(c) first, then accumulate
         if (!wait(kVtFull0 + st, ph(c >> 1))) break;  // W V (and V) of chunk c ready
         tc_fence_after();
@@ -569,7 +571,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         tmem_st_wait();
         tc_fence_before();
-        warp_arrive(kPFull);
+        warp_arrive(kPFull0 + st);
         warp_arrive(kGFree0 + c % kSlots);
       }
       if (c >= 1 && !output(c - 1, fprev)) break;

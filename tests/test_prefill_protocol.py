@@ -1,0 +1,204 @@
+"""The tensor-core prefill kernel's mbarrier protocol, checked on the CPU.
+
+Every warp role of ``gla_chunk_tc.cu`` is restated here as the sequence of
+barrier waits and arrivals it performs per chunk (an MMA commit counts as an
+arrival that happens once the MMA has run; the model lets it happen at any
+later time the scheduler picks).  A randomised scheduler then advances one
+role at a time, with per-role speed biases so that some roles starve while
+others run ahead, and checks two properties for every chunk count and every
+pattern of "wide" chunks (the explicit-decay path):
+
+* no deadlock: every role reaches its end;
+* no parity alias: an mbarrier wait names only the parity of the phase it
+  wants, so a waiter must never fall two or more completed phases behind on
+  the barrier it waits for (it would then wait for a phase that has already
+  passed and time out).
+
+The model must be kept in step with the kernel: a role's steps appear in the
+same order as in its source.  ``test_single_p_barrier_is_caught`` plants the
+mistake of an earlier revision (one P'-ready barrier instead of one per chunk
+parity) and checks that the model finds the alias it allows.
+"""
+import random
+from collections import defaultdict
+
+import pytest
+
+SLOTS = 3          # gate ring depth
+MASK_WARPS = 4
+STATE_WARPS = 8
+
+
+def kernel_roles(nch, wide, single_p_barrier=False):
+    """Generators of ("wait", barrier, phase) / ("arrive", barrier) /
+    ("bar_sync",) steps, one per warp role (warps of a group are separate
+    roles: each arrives once per barrier phase)."""
+    K = SLOTS
+    pfull = (lambda c: ("PFull",)) if single_p_barrier else (lambda c: ("PFull", c & 1))
+    pphase = (lambda c: c) if single_p_barrier else (lambda c: c >> 1)
+
+    def producer():  # warp 0: gate sums (all lanes), then TMA (lane 0)
+        for c in range(nch):
+            if c >= K:
+                yield ("wait", ("GFree", c % K), c // K - 1)
+            yield ("arrive", ("GReady", c % K))
+            if c >= 2:
+                yield ("wait", ("QKEmpty", c & 1), (c >> 1) - 1)
+            yield ("arrive", ("QKFull", c & 1))  # the TMA transaction completes it
+            if c >= 1:
+                yield ("wait", ("VEmpty",), c - 1)
+            yield ("arrive", ("VFull",))
+
+    def mma1():  # warp 1
+        for c in range(nch):
+            st = c & 1
+            yield ("wait", ("QKFull", st), c >> 1)
+            if c >= 2:
+                yield ("wait", ("AFree", st), (c >> 1) - 1)
+            yield ("arrive", ("AFull", st))
+            yield ("arrive", ("QKEmpty", st))
+
+    def mma2():  # warp 2
+        for c in range(nch):
+            st = c & 1
+            yield ("wait", pfull(c), pphase(c))
+            yield ("wait", ("O3Full", st), c >> 1)
+            yield ("wait", ("VtFull", st), c >> 1)
+            yield ("arrive", ("GFree", c % K))
+            yield ("arrive", ("OFull", st))
+            yield ("arrive", ("AFree", st))
+            yield ("arrive", ("VtFree", st))
+            if wide(c):
+                yield ("arrive", ("VEmpty",))
+
+    def mma34():  # warp 3: MMA3 then MMA4 of each chunk
+        for c in range(nch):
+            st = c & 1
+            yield ("wait", ("QKFull", st), c >> 1)
+            yield ("wait", ("VtFull", st), c >> 1)
+            yield ("wait", ("SReady",), c)
+            if c >= 2:
+                yield ("wait", ("OFree", st), (c >> 1) - 1)
+            yield ("wait", ("GReady", c % K), c // K)
+            yield ("arrive", ("O3Full", st))
+            yield ("arrive", ("SFull",))
+            yield ("arrive", ("QKEmpty", st))
+
+    def mask():  # warps 4..7: P' of chunk c, then the output of chunk c - 1
+        for c in range(nch + 1):
+            if c < nch:
+                st = c & 1
+                yield ("wait", ("GReady", c % K), c // K)
+                yield ("wait", ("AFull", st), c >> 1)
+                if wide(c):
+                    yield ("wait", ("O3Full", st), c >> 1)
+                yield ("arrive", pfull(c))
+                yield ("arrive", ("GFree", c % K))
+            if c >= 1:
+                d = c - 1
+                yield ("wait", ("OFull", d & 1), d >> 1)
+                yield ("arrive", ("OFree", d & 1))
+
+    def state(first):  # warps 8..15: W V split of chunk c + 1, then the pass over S_c
+        def split(c):
+            yield ("wait", ("GReady", c % K), c // K)
+            yield ("arrive", ("GFree", c % K))
+            if c >= 2:
+                yield ("wait", ("VtFree", c & 1), (c >> 1) - 1)
+            yield ("wait", ("VFull",), c)
+            if not wide(c):
+                yield ("bar_sync",)
+                if first:
+                    yield ("arrive", ("VEmpty",))
+            yield ("arrive", ("VtFull", c & 1))
+
+        for c in range(-1, nch):
+            last = c + 1 == nch
+            if not last:
+                yield from split(c + 1)
+            if c >= 0:
+                yield ("wait", ("SFull",), c)
+            if not last:
+                yield ("arrive", ("SReady",))
+
+    roles = {"producer": producer(), "mma1": mma1(), "mma2": mma2(), "mma34": mma34()}
+    for w in range(MASK_WARPS):
+        roles[f"mask{w}"] = mask()
+    for w in range(STATE_WARPS):
+        roles[f"state{w}"] = state(w == 0)
+    return roles
+
+
+def arrival_counts():
+    n = {("QKEmpty", 0): 2, ("QKEmpty", 1): 2, ("PFull",): MASK_WARPS, ("PFull", 0): MASK_WARPS,
+         ("PFull", 1): MASK_WARPS, ("OFree", 0): MASK_WARPS, ("OFree", 1): MASK_WARPS,
+         ("VtFull", 0): STATE_WARPS, ("VtFull", 1): STATE_WARPS, ("SReady",): STATE_WARPS}
+    for i in range(SLOTS):
+        n[("GFree", i)] = MASK_WARPS + STATE_WARPS + 1
+    return n
+
+
+def run_schedule(nch, wide, seed, **kw):
+    """Returns None when every role finishes, else a description of the fault."""
+    rnd = random.Random(seed)
+    roles = kernel_roles(nch, wide, **kw)
+    need = arrival_counts()
+    pending, done = defaultdict(int), defaultdict(int)
+    step = {n: next(g, None) for n, g in roles.items()}
+    speed = {n: rnd.choice([0.02, 1.0, 1.0, 8.0]) for n in roles}
+    in_bar_sync = set()
+    while True:
+        live = [n for n in step if step[n] is not None]
+        if not live:
+            return None
+        if len(in_bar_sync) == STATE_WARPS:
+            for n in in_bar_sync:
+                step[n] = next(roles[n], None)
+            in_bar_sync.clear()
+            continue
+        ready = []
+        for n in live:
+            s = step[n]
+            if s[0] == "wait":
+                if done[s[1]] > s[2] + 1:
+                    return f"alias: {n} waits for phase {s[2]} of {s[1]}, {done[s[1]]} completed"
+                if done[s[1]] > s[2]:
+                    ready.append(n)
+            elif s[0] == "arrive" or n not in in_bar_sync:
+                ready.append(n)
+        if not ready:
+            return "deadlock: " + ", ".join(f"{n} at {step[n]}" for n in live)
+        n = rnd.choices(ready, weights=[speed[m] for m in ready])[0]
+        s = step[n]
+        if s[0] == "bar_sync":
+            in_bar_sync.add(n)
+            continue
+        if s[0] == "arrive":
+            pending[s[1]] += 1
+            if pending[s[1]] == need.get(s[1], 1):
+                pending[s[1]] = 0
+                done[s[1]] += 1
+        step[n] = next(roles[n], None)
+
+
+WIDE_PATTERNS = {
+    "none": lambda c: False,
+    "all": lambda c: True,
+    "odd": lambda c: c % 2 == 1,
+    "every_third": lambda c: c % 3 == 0,
+}
+
+
+@pytest.mark.parametrize("pattern", sorted(WIDE_PATTERNS))
+def test_protocol_has_no_deadlock_or_alias(pattern):
+    wide = WIDE_PATTERNS[pattern]
+    for nch in range(0, 9):
+        for seed in range(150):
+            fault = run_schedule(nch, wide, seed)
+            assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
+
+
+def test_single_p_barrier_is_caught():
+    faults = [run_schedule(nch, WIDE_PATTERNS["none"], seed, single_p_barrier=True)
+              for nch in range(2, 6) for seed in range(200)]
+    assert any(f is not None and f.startswith("alias") and "PFull" in f for f in faults)
