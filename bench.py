@@ -52,19 +52,24 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
 # ----------------------------------------------------------------- workloads
-def prefill_bytes(w, B, T) -> int:
-    """Algorithmic HBM bytes of one prefill call: read q, k, v (bf16), g (fp32),
-    the initial state (fp32); write out (bf16) and the final state (fp32)."""
-    rows = B * T
-    io = 2 * rows * w.H * (2 * w.dk + w.dv) + 4 * rows * w.H + 2 * rows * w.H * w.dv
-    states = 2 * 4 * B * w.H * w.dk * w.dv
+def prefill_bytes(w, B, T, rows=None) -> int:
+    """Algorithmic HBM bytes of one prefill call over B sequences (B * T token
+    rows, or ``rows`` when packed): read q, k, v (bf16) and g (fp32, one per
+    head or per key channel), the initial state (fp32, when the workload has
+    one); write out (bf16) and the final state (fp32)."""
+    rows = B * T if rows is None else rows
+    g_per_head = w.dk if w.gate == "vector" else 1
+    io = 2 * rows * w.H * (2 * w.dk + w.dv) + 4 * rows * w.H * g_per_head + 2 * rows * w.H * w.dv
+    n_states = 2 if (w.init_std > 0 or w.name == "prefill") else 1
+    states = n_states * 4 * B * w.H * w.dk * w.dv
     return io + states
 
 
-def prefill_flops(w, B, T) -> int:
+def prefill_flops(w, B, T, rows=None) -> int:
     """Tensor-core flops of the chunked form as computed (full C x C tiles):
     per token and head 2 * (C * (dk + dv) + 2 * dk * dv)."""
-    return 2 * (w.chunk * (w.dk + w.dv) + 2 * w.dk * w.dv) * B * T * w.H
+    rows = B * T if rows is None else rows
+    return 2 * (w.chunk * (w.dk + w.dv) + 2 * w.dk * w.dv) * rows * w.H
 
 
 def decode_bytes(w) -> int:
@@ -445,14 +450,19 @@ def run_profile_case(args):
     glabuild.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.profile == "prefill":
-        w = gla_inputs.WORKLOADS["prefill"]
+    if args.profile in ("prefill", "vector", "varlen"):
+        w = gla_inputs.WORKLOADS[args.profile]
         x = gla_inputs.prefill_inputs(w)
-        q, k, v, g, s0 = (x[n].to(dev) for n in ("q", "k", "v", "g", "init_state"))
+        q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))
+        s0 = x["init_state"].to(dev) if x["init_state"] is not None else None
+        cu = x["cu_seqlens"].to(dev) if x["cu_seqlens"] is not None else None
 
         def call():
-            gla.chunk_fwd(q, k, v, g, scale=x["scale"], init_state=s0, chunk=w.chunk)
-        nbytes = prefill_bytes(w, w.B, w.T)
+            gla.chunk_fwd(q, k, v, g, scale=x["scale"], init_state=s0, cu_seqlens=cu,
+                          chunk=w.chunk)
+        nseq = (len(x["cu_seqlens"]) - 1) if cu is not None else w.B
+        rows = q.numel() // (w.H * w.dk)
+        nbytes = prefill_bytes(w, nseq, 0, rows=rows)
     else:
         w = gla_inputs.WORKLOADS["decode"]
         d = gla_inputs.decode_inputs(w, steps=1, N=args.decode_n)
@@ -524,7 +534,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode"], default=None,
                     help="run one kernel alone (for ncu captures) instead of the bench")
     ap.add_argument("--decode-n", type=int, default=1280,
                     help="sequences for --profile decode")

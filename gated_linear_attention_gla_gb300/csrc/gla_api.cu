@@ -86,7 +86,8 @@ const char* gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags) {
   a.fp32_io = (flags & GLA_FLAG_FP32_IO) != 0;
   a.fp32_out = a.fp32_io || (flags & GLA_FLAG_FP32_OUT) != 0;
   a.vector_gate = (flags & GLA_FLAG_VECTOR_GATE) != 0;
-  return gla::chunk_tc_supported(a) ? "tensor_core" : "cuda_core";
+  return (gla::chunk_tc_supported(a) || gla::chunk_tc_vec_supported(a)) ? "tensor_core"
+                                                                        : "cuda_core";
 }
 
 const char* gla_status_string(gla_status status) {
@@ -161,6 +162,8 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (rows > 0 && gla::chunk_tc_supported(a))
     err = gla::launch_chunk_tc(a, s);
+  else if (rows > 0 && gla::chunk_tc_vec_supported(a))
+    err = gla::launch_chunk_tc_vec(a, s);
   else
     err = gla::launch_chunk_simt(a, s);
   return cuda_status(err);

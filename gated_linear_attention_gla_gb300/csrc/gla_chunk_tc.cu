@@ -93,7 +93,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWideSpan = 96.f;      // log2 chunk decay span above which a chunk is "wide"
 constexpr float kLoCutoff = -16.f;     // log2 decay still to come below which MMA4 skips lo
 constexpr int kSlots = 3;              // gate ring: chunks c (mask), c + 1 (split), c + 2 (gate)
-constexpr uint32_t kBarState = 2;      // named barrier of the state group
 
 // shared memory map (offsets from the 1024-byte-aligned base)
 constexpr uint32_t kPanel = kC * 128;                 // 128 rows x 128 B
@@ -124,7 +123,7 @@ constexpr uint32_t kColS = 448;    // 64: the running state slice, fp32
 enum Bar {
   kQKFull0 = 0, kQKFull1, kQKEmpty0, kQKEmpty1, kVFull, kVEmpty, kAFull0, kAFull1,
   kAFree0, kAFree1, kPFull0, kPFull1, kVtFull0, kVtFull1, kVtFree0, kVtFree1, kSFull, kSReady,
-  kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kGReady0,
+  kO3Full0, kO3Full1, kOFull0, kOFull1, kOFree0, kOFree1, kStateSync, kGReady0,
   kGFree0 = kGReady0 + kSlots, kNumBars = kGFree0 + kSlots
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
@@ -248,7 +247,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // group barriers take one arrival per warp (see warp_arrive)
       uint32_t cnt = 1;
       if (i == kPFull0 || i == kPFull1 || i == kOFree0 || i == kOFree1) cnt = kMaskWarps;
-      if (i == kVtFull0 || i == kVtFull1 || i == kSReady) cnt = kStateWarps;
+      if (i == kVtFull0 || i == kVtFull1 || i == kSReady || i == kStateSync) cnt = kStateWarps;
       // both MMA issuers that read Q and K commit to the stage's empty barrier
       if (i == kQKEmpty0 || i == kQKEmpty1) cnt = 2;
       // gate slots are released by both groups and the MMA2 issuer
@@ -277,6 +276,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     *abort_flag = 1;
     atomicOr(p.status, kDevTimeout);
     return false;
+  };
+  // the same, decided for the whole warp (full-warp roles never split on a wait)
+  auto wait_w = [&](int b, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, wait(b, parity));
   };
   // parity of the k-th completion (k = 0, 1, ...) of a barrier
   auto ph = [](int k) -> uint32_t { return static_cast<uint32_t>(k) & 1u; };
@@ -483,7 +486,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // output of chunk c: o = scale f_t O[c & 1], f_t = exp(G_t - G_L) (1 on wide
     // chunks, whose O carries the decay already)
     auto output = [&](int c, float f) -> bool {
-      if (!wait(kOFull0 + (c & 1), ph(c >> 1))) return false;  // MMA2(c)
+      if (!wait_w(kOFull0 + (c & 1), ph(c >> 1))) return false;  // MMA2(c)
       tc_fence_after();
       const int n = min(kC, len - c * kC);
       const float s1 = scale * f;
@@ -542,18 +545,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (c < nch) {
         const int st = c & 1;
         const float* slot = slot_of(c);
-        if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) break;
+        if (!wait_w(kGReady0 + c % kSlots, ph(c / kSlots))) break;
         const float G2 = slot[kSlotG2 + r];
         const float total = slot[kSlotTotal];
         const bool wide = slot[kSlotWide] != 0.f;
         f = wide ? 1.f : exp2f(G2 - total);
-        if (!wait(kAFull0 + st, ph(c >> 1))) break;
+        if (!wait_w(kAFull0 + st, ph(c >> 1))) break;
         tc_fence_after();
         const uint32_t a_row = tmem + lane_off + kColA + st * 128;
         if (wide) {
           build_p_wide(a_row, q4, r, G2, slot + kSlotG2);
           // O = Q S_{c-1} so far: scale row t by exp(G_t) before MMA2 adds P V
-          if (!wait(kO3Full0 + st, ph(c >> 1))) break;
+          if (!wait_w(kO3Full0 + st, ph(c >> 1))) break;
           tc_fence_after();
           const float e = exp2f(G2);
           const uint32_t o_row = tmem + lane_off + kColO + st * kDVS;
@@ -588,19 +591,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint8_t* sb_row = smem + kOffSb;
     float* final_row = p.final_state ? p.final_state + st_off : nullptr;
 
+    int nsync = 0;  // completions of the group barrier so far
     // W V split of chunk c (this thread: token row r, V columns 32 half .. +31)
     // into bf16 hi and lo (buffers c & 1).  Returns the chunk's total log2 decay.
     auto split_wv = [&](int c, float& total, bool& wide) -> bool {
       const int n = min(kC, len - c * kC);
-      if (!wait(kGReady0 + c % kSlots, ph(c / kSlots))) return false;
+      if (!wait_w(kGReady0 + c % kSlots, ph(c / kSlots))) return false;
       const float* slot = slot_of(c);
       const float G2r = slot[kSlotG2 + r];
       total = slot[kSlotTotal];
       wide = slot[kSlotWide] != 0.f;
       warp_arrive(kGFree0 + c % kSlots);
       // MMA2(c-2) done; MMA4(c-2) is done too (its S was passed before this call)
-      if (c >= 2 && !wait(kVtFree0 + (c & 1), ph((c >> 1) - 1))) return false;
-      if (!wait(kVFull, ph(c))) return false;
+      if (c >= 2 && !wait_w(kVtFree0 + (c & 1), ph((c >> 1) - 1))) return false;
+      if (!wait_w(kVFull, ph(c))) return false;
       const uint8_t* v_s = smem + kOffV;
       uint8_t* hi_s = smem + kOffVhi + (c & 1) * kTile;
       uint8_t* lo_s = smem + kOffVlo + (c & 1) * kTile;
@@ -623,7 +627,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       if (!wide) {
         // the raw V tile is no longer needed (a wide chunk keeps it for MMA2)
-        named_bar_sync(kBarState, kStateWarps * 32);
+        // all of the group is done with it (an mbarrier with a bounded wait, so a
+        // group that is aborting cannot hang the others)
+        warp_arrive(kStateSync);
+        if (!wait_w(kStateSync, ph(nsync++))) return false;
         if (warp == 8 && lane == 0) mbar_arrive(&bars[kVEmpty]);
       }
       warp_arrive(kVtFull0 + (c & 1));
@@ -696,7 +703,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       bool next_wide = false;
       if (!last && !split_wv(c + 1, next_total, next_wide)) break;
       if (c >= 0) {
-        if (!wait(kSFull, ph(c))) break;  // S = S_c; MMA3(c) has read S'
+        if (!wait_w(kSFull, ph(c))) break;  // S = S_c; MMA3(c) has read S'
         tc_fence_after();
       }
       pass_state(c, last ? 1.f : exp2f(next_total), last, next_wide);

@@ -54,6 +54,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+bool chunk_tc_vec_supported(const ChunkArgs& a);
+cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_state_copy(const ChunkArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------

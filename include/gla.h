@@ -101,9 +101,10 @@ typedef enum gla_status {
  *               sequence (or packed rows).  B, H, T >= 0; with T = 0 (or empty
  *               sequences) final_state receives init_state (or zeros).
  *   dk, dv      head sizes: 64 or 128 each
- *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O), or
- *               16, 32, 64 (fp32 SIMT path); fp32 I/O always takes the SIMT
- *               path (chunk 16, 32, 64 or 128)
+ *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O with
+ *               dk = 128: the per-head gate with dv = 64 or 128, the
+ *               per-key-channel gate with dv = 128), or 16, 32, 64 (fp32 SIMT
+ *               path); fp32 I/O and the other head sizes take the SIMT path
  *   stream      CUDA stream
  *   flags       GLA_FLAG_* bits; 0 = bf16 I/O, per-head gate
  *
@@ -142,9 +143,10 @@ gla_status gla_decode_step(const void *q, const void *k, const void *v, const fl
 
 /*
  * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call
- * with these head sizes, chunk size and flags: "tensor_core" (the tcgen05
- * kernel), "cuda_core" (the fp32 CUDA-core kernel), or NULL when the call
- * would be rejected.  Pure host function: launches nothing.
+ * with these head sizes, chunk size and flags: "tensor_core" (a tcgen05
+ * kernel: per-head or per-key-channel gate), "cuda_core" (the fp32 CUDA-core
+ * kernel), or NULL when the call would be rejected.  Pure host function:
+ * launches nothing.
  */
 const char *gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags);
 

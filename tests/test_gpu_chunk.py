@@ -114,17 +114,19 @@ def test_bf16_lengths_around_the_chunk(cuda_ok, T):
     check(x, out, fin, *run_ref(x))
 
 
-def test_bf16_no_initial_state_no_final_state(cuda_ok):
-    x = small(B=2, T=300, H=2)
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_bf16_no_initial_state_no_final_state(cuda_ok, gate):
+    x = small(B=2, T=300, H=2, gate=gate)
     out, fin = run_gpu(x, init=False, final=False)
     assert fin is None
     o_ref, _ = run_ref(x, init=False)
     check(x, out, None, o_ref, None)
 
 
-def test_final_state_in_place_over_initial_state(cuda_ok):
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_final_state_in_place_over_initial_state(cuda_ok, gate):
     gla = _gla()
-    x = small(B=2, T=260, H=2)
+    x = small(B=2, T=260, H=2, gate=gate, init_std=0.05)
     S = cuda(x["init_state"]).clone()
     out, fin = gla.chunk_fwd(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]),
                              scale=x["scale"], init_state=S, final_state=S, chunk=128,
@@ -147,11 +149,13 @@ def test_minus_inf_gate_inside_chunks(cuda_ok, gate):
     check(x, out, fin, *run_ref(x))
 
 
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
 @pytest.mark.parametrize("positions", [[5, 40, 90], [0, 1, 2, 127], [64, 65, 66, 200, 201, 202]])
-def test_several_resets_in_one_chunk(cuda_ok, positions):
+def test_several_resets_in_one_chunk(cuda_ok, positions, gate):
     """Three or more -inf gates in one chunk push its decay span past 2^96: the
-    kernel takes its explicit-decay path for that chunk."""
-    x = small(B=2, T=300, H=2)
+    per-head kernel takes its explicit-decay path for that chunk, the
+    per-key-channel kernel its token-by-token path."""
+    x = small(B=2, T=300, H=2, gate=gate)
     g = x["g"].clone()
     g[:, positions] = float("-inf")
     x["g"] = g
@@ -160,15 +164,33 @@ def test_several_resets_in_one_chunk(cuda_ok, positions):
     check(x, out, fin, *run_ref(x))
 
 
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
 @pytest.mark.parametrize("mu", [-3.0, 0.0, 8.0])
-def test_strong_and_weak_decay(cuda_ok, mu):
+def test_strong_and_weak_decay(cuda_ok, mu, gate):
     """g = logsigmoid(N(mu, 1)): mu = -3 makes every chunk's decay span far wider
-    than 2^96 (explicit path throughout), mu = 8 keeps nearly all memory (the lo
-    half of the state update matters in every chunk)."""
-    x = small(B=2, T=400, H=2)
+    than 2^96 (explicit / token-by-token path throughout), mu = 8 keeps nearly
+    all memory (the lo half of the state update matters in every chunk)."""
+    x = small(B=2, T=400, H=2, gate=gate)
     gen = torch.Generator().manual_seed(5)
     x["g"] = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
     out, fin = run_gpu(x)
+    check(x, out, fin, *run_ref(x))
+
+
+def test_vector_gate_mixed_channel_decays(cuda_ok):
+    """Per-key-channel decays from nearly none to very strong in the same head
+    (channel i: g = logsigmoid(N(mu_i, 1)), mu_i from -4 to 8), and chunks that
+    alternate between the tensor-core and the token-by-token path."""
+    x = small(B=2, T=700, H=2, gate="vector")
+    gen = torch.Generator().manual_seed(9)
+    mu = torch.linspace(-4.0, 8.0, x["g"].shape[-1])
+    g = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
+    g[:, 128:256] = torch.nn.functional.logsigmoid(
+        torch.randn(g[:, 128:256].shape, generator=gen) + 4.0)   # a mild chunk
+    g[:, 400:410] = float("-inf")                                 # a chunk with ten resets
+    x["g"] = g
+    out, fin = run_gpu(x)
+    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
     check(x, out, fin, *run_ref(x))
 
 
@@ -240,10 +262,11 @@ def test_chunk_sizes_agree(cuda_ok):
         assert rel_max(to_np(f), to_np(outs[0][1])) <= 2 * TOL_STATE
 
 
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
 @pytest.mark.parametrize("chunk", [128, 64])
-def test_prefill_equals_decode_steps(cuda_ok, chunk):
+def test_prefill_equals_decode_steps(cuda_ok, chunk, gate):
     gla = _gla()
-    x = small(B=3, T=140, H=2, chunk=chunk)
+    x = small(B=3, T=140, H=2, chunk=chunk, gate=gate, init_std=0.05)
     out, fin = run_gpu(x)
     S = cuda(x["init_state"]).clone()
     for t in range(x["q"].shape[1]):

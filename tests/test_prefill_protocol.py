@@ -1,6 +1,7 @@
-"""The tensor-core prefill kernel's mbarrier protocol, checked on the CPU.
+"""The tensor-core prefill kernels' mbarrier protocols, checked on the CPU.
 
-Every warp role of ``gla_chunk_tc.cu`` is restated here as the sequence of
+Every warp role of ``gla_chunk_tc.cu`` (per-head gate) and of
+``gla_chunk_tc_vec.cu`` (per-key-channel gate) is restated here as the sequence of
 barrier waits and arrivals it performs per chunk (an MMA commit counts as an
 arrival that happens once the MMA has run; the model lets it happen at any
 later time the scheduler picks).  A randomised scheduler then advances one
@@ -24,9 +25,10 @@ from collections import defaultdict
 
 import pytest
 
-SLOTS = 3          # gate ring depth
+SLOTS = 3          # gate ring depth (per-head kernel)
 MASK_WARPS = 4
 STATE_WARPS = 8
+GATE_WARPS = 8     # per-key-channel kernel
 
 
 def kernel_roles(nch, wide, single_p_barrier=False):
@@ -130,6 +132,7 @@ def kernel_roles(nch, wide, single_p_barrier=False):
 
 
 def arrival_counts():
+    """Arrivals per phase of the per-head kernel's barriers (default 1)."""
     n = {("QKEmpty", 0): 2, ("QKEmpty", 1): 2, ("PFull",): MASK_WARPS, ("PFull", 0): MASK_WARPS,
          ("PFull", 1): MASK_WARPS, ("OFree", 0): MASK_WARPS, ("OFree", 1): MASK_WARPS,
          ("VtFull", 0): STATE_WARPS, ("VtFull", 1): STATE_WARPS, ("SReady",): STATE_WARPS}
@@ -138,11 +141,125 @@ def arrival_counts():
     return n
 
 
-def run_schedule(nch, wide, seed, **kw):
+def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
+    """The per-key-channel kernel.  Chunks the gate group finds "wide" are
+    processed by it token by token (one group barrier per token) and skip the
+    MMAs; the others run the tensor-core path.  The gate group's barrier is an
+    mbarrier whose phases the warps count themselves."""
+    def producer():  # warp 0, lane 0
+        for c in range(nch):
+            if c >= 1:
+                yield ("wait", ("GEmpty",), c - 1)
+            yield ("arrive", ("GFull",))
+            if c >= 1:
+                yield ("wait", ("QKEmpty",), c - 1)
+            yield ("arrive", ("QKFull",))
+            if c >= 1:
+                yield ("wait", ("VEmpty",), c - 1)
+            yield ("arrive", ("VFull",))
+
+    def issuer():  # warp 1, lane 0: MMA1, MMA3, MMA4, MMA2 per tensor-core chunk
+        n = 0
+        for c in range(nch):
+            yield ("wait", ("Scaled", c & 1), c >> 1)
+            yield ("arrive", ("Ack", c & 1))
+            if wide(c):
+                continue
+            yield ("arrive", ("AFull",))
+            yield ("wait", ("SbReady",), n)
+            if n >= 2:
+                yield ("wait", ("OFree", n & 1), (n >> 1) - 1)
+            yield ("wait", ("VFull",), c)
+            yield ("arrive", ("SFull",))
+            yield ("arrive", ("QKEmpty",))
+            yield ("wait", ("PFull", n & 1), n >> 1)
+            yield ("arrive", ("OFull", n & 1))
+            yield ("arrive", ("VEmpty",))
+            n += 1
+
+    def mask():  # warps 4..7
+        n, pending = 0, False
+        for c in range(nch + 1):
+            tc = False
+            if c < nch:
+                yield ("wait", ("Scaled", c & 1), c >> 1)
+                yield ("arrive", ("Ack", c & 1))
+                tc = not wide(c)
+                if tc:
+                    yield ("wait", ("AFull",), n)
+                    yield ("arrive", ("PFull", n & 1))
+            if pending:
+                m = n - 1
+                yield ("wait", ("OFull", m & 1), m >> 1)
+                yield ("arrive", ("OFree", m & 1))
+            pending = tc
+            if tc:
+                n += 1
+
+    def gate(first):  # warps 8..15
+        k = 0  # group barrier phases
+
+        def group_sync():
+            nonlocal k
+            yield ("arrive", ("GateSync",))
+            yield ("wait", ("GateSync",), k)
+            k += 1
+
+        n, last_tc = 0, False
+        for c in range(nch):
+            yield ("wait", ("GFull",), c)
+            yield from group_sync()          # partial sums written
+            yield from group_sync()          # wide vote
+            if c >= 2:
+                yield ("wait", ("Ack", c & 1), (c - 2) >> 1)
+            yield ("wait", ("QKFull",), c)
+            if not wide(c):
+                yield from group_sync()      # done with g
+                if first:
+                    yield ("arrive", ("GEmpty",))
+                yield ("arrive", ("Scaled", c & 1))
+                if last_tc:
+                    yield ("wait", ("SFull",), n - 1)
+                yield ("arrive", ("SbReady",))
+                last_tc = True
+                n += 1
+            else:
+                yield ("arrive", ("Scaled", c & 1))
+                if last_tc:
+                    yield ("wait", ("SFull",), n - 1)
+                yield ("wait", ("VFull",), c)
+                for _ in range(tokens_in_wide_chunk):
+                    yield from group_sync()
+                yield from group_sync()      # done with g, Q, K, V
+                if first:
+                    yield ("arrive", ("GEmpty",))
+                    yield ("arrive", ("QKEmpty",))
+                    yield ("arrive", ("VEmpty",))
+                last_tc = False
+        if last_tc:
+            yield ("wait", ("SFull",), n - 1)
+
+    roles = {"producer": producer(), "issuer": issuer()}
+    for w in range(MASK_WARPS):
+        roles[f"mask{w}"] = mask()
+    for w in range(GATE_WARPS):
+        roles[f"gate{w}"] = gate(w == 0)
+    return roles
+
+
+def vector_arrival_counts():
+    n = {("Scaled", 0): GATE_WARPS, ("Scaled", 1): GATE_WARPS, ("SbReady",): GATE_WARPS,
+         ("GateSync",): GATE_WARPS, ("PFull", 0): MASK_WARPS, ("PFull", 1): MASK_WARPS,
+         ("OFree", 0): MASK_WARPS, ("OFree", 1): MASK_WARPS,
+         ("Ack", 0): 1 + MASK_WARPS, ("Ack", 1): 1 + MASK_WARPS}
+    return n
+
+
+def run_schedule(nch, wide, seed, vector=False, **kw):
     """Returns None when every role finishes, else a description of the fault."""
     rnd = random.Random(seed)
-    roles = kernel_roles(nch, wide, **kw)
-    need = arrival_counts()
+    roles = (vector_kernel_roles if vector else kernel_roles)(nch, wide, **kw)
+    need = vector_arrival_counts() if vector else arrival_counts()
     pending, done = defaultdict(int), defaultdict(int)
     step = {n: next(g, None) for n, g in roles.items()}
     speed = {n: rnd.choice([0.02, 1.0, 1.0, 8.0]) for n in roles}
@@ -195,6 +312,16 @@ def test_protocol_has_no_deadlock_or_alias(pattern):
     for nch in range(0, 9):
         for seed in range(150):
             fault = run_schedule(nch, wide, seed)
+            assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
+
+
+@pytest.mark.parametrize("pattern", sorted(WIDE_PATTERNS) + ["first_two", "runs"])
+def test_vector_protocol_has_no_deadlock_or_alias(pattern):
+    extra = {"first_two": lambda c: c < 2, "runs": lambda c: (c // 3) % 2 == 1}
+    wide = WIDE_PATTERNS.get(pattern) or extra[pattern]
+    for nch in range(0, 9):
+        for seed in range(120):
+            fault = run_schedule(nch, wide, seed, vector=True)
             assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
 
 
