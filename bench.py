@@ -241,6 +241,61 @@ def cpu_baseline(budget_s: float = 10.0):
 
 
 # ------------------------------------------------------------------ GPU arm
+# the other prefill workloads: their kernel and the profile that records its traffic
+SIDE_WORKLOADS = {
+    "vector": ("chunk_tc_vec_kernel", "chunk_tc_vec_kernel.vector_b8_h16_t4096.md",
+               "gla_chunk_tc_vec.cu"),
+    "varlen": ("chunk_tc_kernel", None, "gla_chunk_tc.cu"),
+}
+
+
+def time_side_workloads(gla, dev, hbm, peak_kind, reps=10, warmup=3):
+    """The vector-gate and packed varlen prefill workloads, each timed alone
+    (CUDA events around `reps` calls after `warmup`), with their HBM roofline."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, (kernel, profile, source) in SIDE_WORKLOADS.items():
+        w = gla_inputs.WORKLOADS[name]
+        x = gla_inputs.prefill_inputs(w)
+        q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))
+        s0 = x["init_state"].to(dev) if x["init_state"] is not None else None
+        cu = x["cu_seqlens"].to(dev) if x["cu_seqlens"] is not None else None
+        nseq = (len(x["cu_seqlens"]) - 1) if cu is not None else w.B
+        rows = q.numel() // (w.H * w.dk)
+        o = torch.empty(v.shape, dtype=torch.bfloat16, device=dev)
+        fin = torch.empty(nseq, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+        def call():
+            gla.chunk_fwd(q, k, v, g, scale=x["scale"], init_state=s0, cu_seqlens=cu,
+                          chunk=w.chunk, out=o, final_state=fin)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        gla.status_sync()
+        sec = a.elapsed_time(b) / 1e3 / reps
+        nbytes = prefill_bytes(w, nseq, 0, rows=rows)
+        gbs = nbytes / sec / 1e9
+        desc = (f"{nseq} packed sequences ({rows} tokens), " if cu is not None else
+                f"B={w.B} T={w.T} ") + (f"H={w.H} dk=dv={w.dk} chunk={w.chunk} "
+                                        f"{w.gate} gate, bf16 I/O")
+        out[name] = {
+            "workload": desc, "ms_per_call": sec * 1e3, "tokens_per_call": rows,
+            "value": rows / sec, "unit": "tokens/s", "calls": reps,
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": gbs / hbm, "peak_kind": peak_kind,
+                         "traffic": profiled_traffic(profile, source) if profile else None,
+                         "algorithmic_bytes_per_launch": nbytes}}
+        del q, k, v, g, s0, cu, o, fin
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gla(args, world, rank, local):
     import gated_linear_attention_gla_gb300 as gla
     from gated_linear_attention_gla_gb300 import build as glabuild
@@ -434,6 +489,9 @@ def run_gla(args, world, rank, local):
         "gpu_launches": args.steps * (1 + DECODE_STEPS),
         "clocks": clocks,
     }
+    if not args.no_side_workloads:
+        # timed after the step (outside ms_per_step and gpu_launches)
+        line["prefill_workloads"] = time_side_workloads(gla, dev, hbm, peak_kind)
     if world == 1 and not args.no_cpu_baseline:
         pre_cpu, dec_cpu = cpu_baseline(args.cpu_budget)
         line["cpu_baseline"] = pre_cpu
@@ -534,6 +592,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="skip timing the vector-gate and varlen prefill workloads")
     ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode"], default=None,
                     help="run one kernel alone (for ncu captures) instead of the bench")
     ap.add_argument("--decode-n", type=int, default=1280,
