@@ -246,6 +246,7 @@ SIDE_WORKLOADS = {
     "vector": ("chunk_tc_vec_kernel", "chunk_tc_vec_kernel.vector_b8_h16_t4096.md",
                "gla_chunk_tc_vec.cu"),
     "varlen": ("chunk_tc_kernel", None, "gla_chunk_tc.cu"),
+    "laplace": ("chunk_tc_kernel", None, "gla_chunk_tc.cu"),
 }
 
 
@@ -282,8 +283,8 @@ def time_side_workloads(gla, dev, hbm, peak_kind, reps=10, warmup=3):
         nbytes = prefill_bytes(w, nseq, 0, rows=rows)
         gbs = nbytes / sec / 1e9
         desc = (f"{nseq} packed sequences ({rows} tokens), " if cu is not None else
-                f"B={w.B} T={w.T} ") + (f"H={w.H} dk=dv={w.dk} chunk={w.chunk} "
-                                        f"{w.gate} gate, bf16 I/O")
+                f"B={w.B} T={w.T} ") + (f"H={w.H} dk={w.dk} dv={w.dv} chunk={w.chunk} "
+                                        f"{w.gate} gate ({w.decay} decay), bf16 I/O")
         out[name] = {
             "workload": desc, "ms_per_call": sec * 1e3, "tokens_per_call": rows,
             "value": rows / sec, "unit": "tokens/s", "calls": reps,

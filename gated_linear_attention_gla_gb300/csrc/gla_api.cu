@@ -44,7 +44,10 @@ bool aligned(const void* p, uintptr_t bytes) {
   return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
 }
 
-bool head_size_ok(int d) { return d == 64 || d == 128; }
+// key head sizes 64, 96, 128; value head sizes 64, 128, 192 (96 x 192 is the
+// Laplace 3B head of the "i14 Laplace 3B" page)
+bool dk_ok(int d) { return d == 64 || d == 96 || d == 128; }
+bool dv_ok(int d) { return d == 64 || d == 128 || d == 192; }
 
 bool flags_ok(unsigned flags) {
   return (flags & ~(GLA_FLAG_FP32_IO | GLA_FLAG_VECTOR_GATE | GLA_FLAG_FP32_OUT)) == 0u;
@@ -79,7 +82,7 @@ const char* gla_last_error_string(void) {
 }
 
 const char* gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags) {
-  if (!flags_ok(flags) || !head_size_ok(dk) || !head_size_ok(dv)) return nullptr;
+  if (!flags_ok(flags) || !dk_ok(dk) || !dv_ok(dv)) return nullptr;
   if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return nullptr;
   gla::ChunkArgs a{};
   a.dk = dk; a.dv = dv; a.chunk = chunk;
@@ -108,7 +111,7 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int dk, int dv, int chunk, gla_stream_t stream, unsigned flags) {
   if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
     return GLA_ERR_INVALID_ARG;
-  if (!head_size_ok(dk) || !head_size_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
   if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
   const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
   const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
@@ -173,7 +176,7 @@ gla_status gla_decode_step(const void* q, const void* k, const void* v, const fl
                            float scale, float* state_inout, void* out, int N, int H, int dk,
                            int dv, gla_stream_t stream, unsigned flags) {
   if (!flags_ok(flags) || N < 0 || H < 0 || !std::isfinite(scale)) return GLA_ERR_INVALID_ARG;
-  if (!head_size_ok(dk) || !head_size_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
   if (N == 0 || H == 0) return GLA_OK;
   const long long units = (long long)N * H;
   if (units > 0x7fffffffll || units * dk * dv > kMaxElems) return GLA_ERR_INVALID_ARG;

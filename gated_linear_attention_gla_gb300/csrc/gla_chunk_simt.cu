@@ -232,6 +232,9 @@ cudaError_t launch_io(const ChunkArgs& a, cudaStream_t stream) {
   if (a.dk == 128)
     return a.vector_gate ? launch_chunk<IO, OUT, 128, true>(a, stream)
                          : launch_chunk<IO, OUT, 128, false>(a, stream);
+  if (a.dk == 96)
+    return a.vector_gate ? launch_chunk<IO, OUT, 96, true>(a, stream)
+                         : launch_chunk<IO, OUT, 96, false>(a, stream);
   return a.vector_gate ? launch_chunk<IO, OUT, 64, true>(a, stream)
                        : launch_chunk<IO, OUT, 64, false>(a, stream);
 }

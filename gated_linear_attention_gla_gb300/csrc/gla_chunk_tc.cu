@@ -18,6 +18,10 @@
 //     o_t = scale * exp(G_t - G_L) * ( Q S' + causal(A) (W V) )_t,  S' = exp(G_L) S
 // and the two contractions share one accumulator.
 //
+// Head sizes: d_k = 128, or 96 run as 128 (the TMA fills channels 96..127
+// with zeros, so those state rows stay zero and are never stored); d_v = 64,
+// 128 or 192 (one CTA per 64-wide slice).
+//
 // One CTA owns one (sequence, head, 64-wide slice of dv) and walks the chunks
 // in order.  The state slice S (dk x 64, fp32) lives in tensor memory (TMEM)
 // for the whole sequence: the state group scales it by exp(G_L) in place (its
@@ -82,7 +86,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = 128;        // chunk (tokens)
-constexpr int kDK = 128;       // key head size handled by this kernel
+constexpr int kDK = 128;       // key head size of the tiles (d_k = 96 runs zero-padded)
 constexpr int kDVS = 64;       // value columns per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kMaskWarps = 4;
@@ -140,7 +144,7 @@ struct TcParams {
   void* out;
   float* final_state;
   const int32_t* cu_seqlens;
-  int B, H, T, DV, nslices;
+  int B, H, T, DK, DV, nslices;  // DK = 96 runs as 128 with zero channels 96..127
   int out_v8;  // out is 32-byte aligned: 256-bit stores
   unsigned* status;
 };
@@ -586,10 +590,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int half = (warp - 8) >> 2;     // which 32 of the 64 state / V columns
     const int r = 32 * q4 + lane;         // state row i (key channel), token row for W V
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    const size_t st_off = ((size_t)s * p.H + h) * (size_t)kDK * p.DV + (size_t)r * p.DV +
-                          (size_t)sl * kDVS + 32 * half;
+    // state rows past the key head size (d_k = 96) stay zero: their K channels
+    // are the zero columns the TMA fills in
+    const bool row_ok = r < p.DK;
+    const size_t st_off = ((size_t)s * p.H + h) * (size_t)p.DK * p.DV +
+                          (size_t)(row_ok ? r : 0) * p.DV + (size_t)sl * kDVS + 32 * half;
     uint8_t* sb_row = smem + kOffSb;
-    float* final_row = p.final_state ? p.final_state + st_off : nullptr;
+    float* final_row = (p.final_state && row_ok) ? p.final_state + st_off : nullptr;
+    const float* init_row = (p.init_state && row_ok) ? p.init_state + st_off : nullptr;
 
     int nsync = 0;  // completions of the group barrier so far
     // W V split of chunk c (this thread: token row r, V columns 32 half .. +31)
@@ -648,9 +656,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (c < 0) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
-            const float4 x = p.init_state
-                                 ? __ldg(reinterpret_cast<const float4*>(p.init_state + st_off +
-                                                                         16 * q + j))
+            const float4 x = init_row
+                                 ? __ldg(reinterpret_cast<const float4*>(init_row + 16 * q + j))
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             v[j] = __float_as_uint(x.x); v[j + 1] = __float_as_uint(x.y);
             v[j + 2] = __float_as_uint(x.z); v[j + 3] = __float_as_uint(x.w);
@@ -692,7 +699,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // empty sequence: the final state is the initial state
       if (final_row) {
 #pragma unroll 4
-        for (int j = 0; j < 32; ++j) final_row[j] = p.init_state ? p.init_state[st_off + j] : 0.f;
+        for (int j = 0; j < 32; ++j) final_row[j] = init_row ? init_row[j] : 0.f;
       }
     }
     // iteration c: the W V split of chunk c + 1 first (MMA4(c+1) needs it
@@ -761,8 +768,8 @@ bool make_map(CUtensorMap* map, const void* base, int d, int H, long long rows, 
 }  // namespace
 
 bool chunk_tc_supported(const ChunkArgs& a) {
-  return !a.fp32_io && !a.vector_gate && a.chunk == kC && a.dk == kDK &&
-         (a.dv == 64 || a.dv == 128);
+  return !a.fp32_io && !a.vector_gate && a.chunk == kC && (a.dk == 96 || a.dk == kDK) &&
+         (a.dv == 64 || a.dv == 128 || a.dv == 192);
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
@@ -777,7 +784,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
   TcParams p;
   p.g = a.g; p.scale = a.scale; p.init_state = a.init_state; p.out = a.out;
   p.final_state = a.final_state; p.cu_seqlens = a.cu_seqlens;
-  p.B = a.B; p.H = a.H; p.T = a.T; p.DV = a.dv; p.nslices = a.dv / kDVS;
+  p.B = a.B; p.H = a.H; p.T = a.T; p.DK = a.dk; p.DV = a.dv; p.nslices = a.dv / kDVS;
   p.status = a.status;
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   const long long ctas = (long long)a.B * a.H * p.nslices;

@@ -23,7 +23,8 @@
 namespace gla {
 namespace {
 
-constexpr int kDecodeThreads = 256;
+// threads per CTA: dv / 4 threads per state row times 8 (dv = 192) or more rows
+__host__ __device__ constexpr int decode_threads(int dv) { return dv == 192 ? 384 : 256; }
 
 template <typename IO> struct Vec4In;
 template <> struct Vec4In<float> {
@@ -42,14 +43,16 @@ template <> struct Vec4In<__nv_bfloat16> {
 };
 
 template <typename IO, typename OUT, int DK, int DV, bool VEC>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(decode_threads(DV), 2)
 decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
               const float* __restrict__ g, float scale, float* __restrict__ state,
               OUT* __restrict__ out) {
   constexpr int TPR = DV / 4;                   // threads per state row
-  constexpr int RPP = kDecodeThreads / TPR;     // rows per pass
+  constexpr int THREADS = decode_threads(DV);
+  constexpr int RPP = THREADS / TPR;            // rows per pass
   constexpr int PASSES = DK / RPP;              // state float4 loads per thread
-  static_assert(kDecodeThreads % TPR == 0 && DK % RPP == 0, "tile shape");
+  static_assert(THREADS % TPR == 0 && DK % RPP == 0 && THREADS >= DK && THREADS >= DV,
+                "tile shape");
 
   __shared__ float s_q[DK];
   __shared__ float s_k[DK];
@@ -111,20 +114,26 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   const long long units = (long long)a.N * a.H;
   const dim3 grid((unsigned)units);
   if (a.vector_gate)
-    decode_kernel<IO, OUT, DK, DV, true><<<grid, kDecodeThreads, 0, stream>>>(
+    decode_kernel<IO, OUT, DK, DV, true><<<grid, decode_threads(DV), 0, stream>>>(
         (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, (OUT*)a.out);
   else
-    decode_kernel<IO, OUT, DK, DV, false><<<grid, kDecodeThreads, 0, stream>>>(
+    decode_kernel<IO, OUT, DK, DV, false><<<grid, decode_threads(DV), 0, stream>>>(
         (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, (OUT*)a.out);
   return cudaGetLastError();
 }
 
+template <typename IO, typename OUT, int DK>
+cudaError_t launch_dv(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.dv == 192) return launch_typed<IO, OUT, DK, 192>(a, stream);
+  if (a.dv == 128) return launch_typed<IO, OUT, DK, 128>(a, stream);
+  return launch_typed<IO, OUT, DK, 64>(a, stream);
+}
+
 template <typename IO, typename OUT>
 cudaError_t launch_io(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.dk == 128 && a.dv == 128) return launch_typed<IO, OUT, 128, 128>(a, stream);
-  if (a.dk == 128 && a.dv == 64) return launch_typed<IO, OUT, 128, 64>(a, stream);
-  if (a.dk == 64 && a.dv == 128) return launch_typed<IO, OUT, 64, 128>(a, stream);
-  return launch_typed<IO, OUT, 64, 64>(a, stream);
+  if (a.dk == 128) return launch_dv<IO, OUT, 128>(a, stream);
+  if (a.dk == 96) return launch_dv<IO, OUT, 96>(a, stream);
+  return launch_dv<IO, OUT, 64>(a, stream);
 }
 
 }  // namespace

@@ -56,7 +56,6 @@ bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_vec_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
-cudaError_t launch_state_copy(const ChunkArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Small device helpers shared by the kernels.

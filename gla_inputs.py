@@ -19,12 +19,18 @@ varlen      16 sequences, lengths uniform in [512, 16384] packed with
             cu_seqlens, H=32, dk=dv=128, chunk 128, initial state N(0, 0.05)
 vector      B=8, H=16, T=4096, dk=dv=128, chunk 128, per-key-channel gate,
             zero initial state
+laplace     B=8, H=16, T=2048, dk=96, dv=192 (the Laplace 3B head), chunk 128,
+            the fixed geometric per-head decay (half-lives 1 .. 2048 tokens),
+            initial state N(0, 0.02)
 ==========  ===============================================================
 
 Common distributions: q, k, v ~ N(0, 1) (standard deviation 1); k is
 L2-normalised per (token, head) in fp32 before rounding; the gate is
 ``g = logsigmoid(x) / g_div`` with ``x ~ N(g_mu, 1)`` (g_mu 3, except 4 for
-varlen and 2 with g_div 4 for the vector gate); ``scale = dk ** -0.5``.
+varlen and 2 with g_div 4 for the vector gate), except for the laplace
+workload, whose gate is the page's fixed per-head decay: head h has the
+half-life T_h = 2048 ** (h / 15) tokens and g = -ln 2 / T_h for every token;
+``scale = dk ** -0.5``.
 """
 from __future__ import annotations
 
@@ -44,6 +50,7 @@ class Workload:
     dv: int
     io: str = "bf16"            # "bf16" or "fp32": dtype of q, k, v and out
     gate: str = "scalar"        # "scalar" ([.., H]) or "vector" ([.., H, dk])
+    decay: str = "random"       # "random" (logsigmoid of a normal) or "schedule" (fixed per head)
     g_mu: float = 3.0
     g_div: float = 1.0
     B: int = 0                  # dense prefill batch
@@ -75,6 +82,8 @@ WORKLOADS = {
                        init_std=0.05, nseq=16, len_lo=512, len_hi=16384),
     "vector": Workload("vector", 4, H=16, dk=128, dv=128, gate="vector", g_mu=2.0,
                        g_div=4.0, B=8, T=4096, chunk=128),
+    "laplace": Workload("laplace", 5, H=16, dk=96, dv=192, decay="schedule", B=8, T=2048,
+                        chunk=128, init_std=0.02),
 }
 
 
@@ -84,6 +93,15 @@ def _normal(gen, shape, std=1.0):
 
 
 def _gate(gen, shape, w: Workload):
+    if w.decay == "schedule":
+        # fixed per-head log-decay: half-lives spread geometrically over 1 .. 2048
+        # tokens across the heads, the same value for every token
+        h = torch.arange(w.H, dtype=torch.float64)
+        half_life = 2048.0 ** (h / max(w.H - 1, 1))
+        g_h = (-torch.log(torch.tensor(2.0, dtype=torch.float64)) / half_life).float()
+        shape_h = [1] * (len(shape) - 1) + [w.H] if w.gate == "scalar" else \
+            [1] * (len(shape) - 2) + [w.H, 1]
+        return g_h.reshape(shape_h).expand(shape).contiguous()
     x = _normal(gen, shape) + w.g_mu
     return (F.logsigmoid(x) / w.g_div).contiguous()
 

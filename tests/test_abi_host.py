@@ -73,7 +73,8 @@ E = _binding
     (dict(T=-1), E.GLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), E.GLA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), E.GLA_ERR_INVALID_ARG),
-    (dict(dk=96), E.GLA_ERR_UNSUPPORTED),
+    (dict(dk=80), E.GLA_ERR_UNSUPPORTED),
+    (dict(dk=192), E.GLA_ERR_UNSUPPORTED),
     (dict(dv=256), E.GLA_ERR_UNSUPPORTED),
     (dict(chunk=100), E.GLA_ERR_UNSUPPORTED),
     (dict(chunk=256), E.GLA_ERR_UNSUPPORTED),
@@ -108,7 +109,8 @@ def test_chunk_fwd_empty_problems_are_no_ops(L):
     (dict(N=-1), E.GLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), E.GLA_ERR_INVALID_ARG),
     (dict(dk=32), E.GLA_ERR_UNSUPPORTED),
-    (dict(dv=192), E.GLA_ERR_UNSUPPORTED),
+    (dict(dv=96), E.GLA_ERR_UNSUPPORTED),
+    (dict(dv=256), E.GLA_ERR_UNSUPPORTED),
     (dict(state=0), E.GLA_ERR_INVALID_ARG),
     (dict(k=0), E.GLA_ERR_INVALID_ARG),
     (dict(v=FAKE[2] + 4), E.GLA_ERR_MISALIGNED),

@@ -87,7 +87,7 @@ def test_fp32_path_chunk_sizes(cuda_ok, chunk, gate):
     check(x, out, fin, *run_ref(x))
 
 
-@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64), (96, 192)])
 def test_fp32_path_head_sizes(cuda_ok, dk, dv):
     x = small("tiny", B=1, T=150, H=2, dk=dk, dv=dv, init_std=0.1, chunk=64)
     out, fin = run_gpu(x)
@@ -99,7 +99,7 @@ def test_fp32_path_head_sizes(cuda_ok, dk, dv):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("chunk", [128, 64])
 @pytest.mark.parametrize("gate", ["scalar", "vector"])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 64), (64, 128)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 64), (64, 128), (96, 192)])
 def test_bf16_small(cuda_ok, chunk, gate, dk, dv):
     x = small(B=2, T=333, H=3, dk=dk, dv=dv, gate=gate, chunk=chunk,
               g_div=4.0 if gate == "vector" else 1.0)
@@ -110,6 +110,14 @@ def test_bf16_small(cuda_ok, chunk, gate, dk, dv):
 @pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 256, 257])
 def test_bf16_lengths_around_the_chunk(cuda_ok, T):
     x = small(B=2, T=T, H=2)
+    out, fin = run_gpu(x)
+    check(x, out, fin, *run_ref(x))
+
+
+def test_laplace_head_with_the_fixed_decay_schedule(cuda_ok):
+    """The Laplace 3B head (d_k = 96, d_v = 192) with the page's fixed per-head
+    decays, several chunks and a ragged tail, on the tensor-core path."""
+    x = small("laplace", B=2, T=333, H=16)
     out, fin = run_gpu(x)
     check(x, out, fin, *run_ref(x))
 
@@ -333,7 +341,7 @@ def _sampled_check(x, out, fin, pairs):
     assert max(errs_s) <= TOL_STATE, errs_s
 
 
-@pytest.mark.parametrize("name", ["prefill", "vector", "varlen"])
+@pytest.mark.parametrize("name", ["prefill", "vector", "varlen", "laplace"])
 def test_full_size_workload_sampled(cuda_ok, name):
     w = gla_inputs.WORKLOADS[name]
     x = gla_inputs.prefill_inputs(w)

@@ -23,7 +23,7 @@ def _inputs(N, H, dk, dv, io, gate, steps, seed=7):
 
 @pytest.mark.parametrize("io", ["bf16", "fp32"])
 @pytest.mark.parametrize("gate", ["scalar", "vector"])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (64, 128), (128, 64), (96, 192), (128, 192)])
 def test_decode_steps_match_oracle(cuda_ok, io, gate, dk, dv):
     gla = _gla()
     x = _inputs(37, 3, dk, dv, io, gate, steps=3)

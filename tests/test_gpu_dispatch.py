@@ -35,7 +35,13 @@ def L():
     (128, 64, 128, VEC, "cuda_core"),
     (128, 128, 64, VEC, "cuda_core"),
     (128, 128, 128, VEC | F32, "cuda_core"),
-    (96, 128, 128, 0, None),
+    (96, 192, 128, 0, "tensor_core"),
+    (96, 128, 128, 0, "tensor_core"),
+    (128, 192, 128, 0, "tensor_core"),
+    (96, 192, 128, VEC, "cuda_core"),
+    (96, 192, 64, 0, "cuda_core"),
+    (80, 128, 128, 0, None),
+    (128, 96, 128, 0, None),
     (128, 128, 100, 0, None),
     (128, 128, 128, 1 << 9, None),
 ])

@@ -18,6 +18,7 @@ import tempfile
 import numpy as np
 import pytest
 
+import gla_inputs
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -417,3 +418,14 @@ def test_planted_mistake_is_caught(name):
     with tempfile.TemporaryDirectory() as tmp:
         run = _ctypes_runner(_build_mutant(name, tmp))
         assert not _pins_pass(run), f"mutant {name} slipped through the pins"
+
+
+def test_laplace_workload_gate_is_the_decay_schedule():
+    """The laplace input recipe writes g = log(lambda_h) for every token; its
+    per-head values agree with the oracle's decay schedule (itself pinned to
+    the page's printed lambda_0 and lambda_15), an independent restatement."""
+    x = gla_inputs.prefill_inputs(gla_inputs.WORKLOADS["laplace"], B=1, T=3)
+    lam = oracle.decay_schedule(16, 1.0, 2048.0)
+    g = x["g"].double().numpy()
+    assert g.shape == (1, 3, 16)
+    np.testing.assert_allclose(np.exp(g[0]), np.broadcast_to(lam, (3, 16)), rtol=1e-6)
