@@ -112,10 +112,14 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
 
 
 def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stream=None,
-                out_dtype=None):
+                out_dtype=None, slots=None):
     """One recurrent step for N sequences; ``state [N, H, dk, dv]`` (fp32) is
     updated in place.  ``q, k [N, H, dk]``, ``v [N, H, dv]``, ``g [N, H]`` or
-    ``[N, H, dk]``.  Returns ``out [N, H, dv]`` in q's dtype (or fp32)."""
+    ``[N, H, dk]``.  Returns ``out [N, H, dv]`` in q's dtype (or fp32).
+
+    With ``slots`` (int32 [N] on the GPU) ``state`` is a pool
+    ``[num_slots, H, dk, dv]`` and row n uses page ``slots[n]`` (-1: a padding
+    row that does nothing; see gla_decode_step_slots)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("state", state)):
         _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     _check(q.dim() == 3 and k.shape == q.shape and v.shape[:-1] == q.shape[:-1],
@@ -123,18 +127,32 @@ def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stre
     _check(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v share one dtype")
     N, H, dk = q.shape
     dv = v.shape[-1]
-    _check(state.dtype == torch.float32 and tuple(state.shape) == (N, H, dk, dv),
-           f"state must be fp32 [{N}, {H}, {dk}, {dv}]")
+    if slots is None:
+        _check(state.dtype == torch.float32 and tuple(state.shape) == (N, H, dk, dv),
+               f"state must be fp32 [{N}, {H}, {dk}, {dv}]")
+    else:
+        _check(slots.is_cuda and slots.dtype == torch.int32 and slots.is_contiguous() and
+               tuple(slots.shape) == (N,), f"slots must be contiguous int32 [{N}] on the GPU")
+        _check(state.dtype == torch.float32 and state.dim() == 4 and
+               tuple(state.shape[1:]) == (H, dk, dv),
+               f"the state pool must be fp32 [num_slots, {H}, {dk}, {dv}]")
     out_dtype = _out_dtype(q, out, out_dtype)
     flags = _io_flags(q, g, (N, H), (N, H, dk), out_dtype)
     if scale is None:
         scale = dk ** -0.5
     if out is None:
         out = torch.empty((N, H, dv), dtype=out_dtype, device=q.device)
-    rc = _binding.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(state),
-                                  _ptr(out), N, H, dk, dv, _stream(stream), flags)
+    if slots is None:
+        rc = _binding.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(state),
+                                      _ptr(out), N, H, dk, dv, _stream(stream), flags)
+        name = "gla_decode_step"
+    else:
+        rc = _binding.gla_decode_step_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale,
+                                            _ptr(state), state.shape[0], _ptr(slots), _ptr(out),
+                                            N, H, dk, dv, _stream(stream), flags)
+        name = "gla_decode_step_slots"
     if rc != 0:
-        raise GlaError(rc, "gla_decode_step")
+        raise GlaError(rc, name)
     return out
 
 

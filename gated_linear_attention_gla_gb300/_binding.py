@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
             L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                           _i, _i, _i, _i, _vp, ctypes.c_uint]
             L.gla_decode_step.restype = _i
+            L.gla_decode_step_slots.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i, _vp,
+                                                _vp, _i, _i, _i, _i, _vp, ctypes.c_uint]
+            L.gla_decode_step_slots.restype = _i
             L.gla_status_string.argtypes = [_i]
             L.gla_status_string.restype = ctypes.c_char_p
             L.gla_status_sync.argtypes = [_vp]
@@ -95,6 +98,14 @@ def gla_decode_step(q, k, v, g, scale, state_inout, out, N, H, dk, dv, stream, f
     return lib().gla_decode_step(q or None, k or None, v or None, g or None, float(scale),
                                  state_inout or None, out or None, N, H, dk, dv,
                                  stream or None, flags)
+
+
+def gla_decode_step_slots(q, k, v, g, scale, state_pool, num_slots, slots, out, N, H, dk, dv,
+                          stream, flags) -> int:
+    """Raw call: pointers are ints, ``stream`` an int handle."""
+    return lib().gla_decode_step_slots(q or None, k or None, v or None, g or None, float(scale),
+                                       state_pool or None, num_slots, slots or None,
+                                       out or None, N, H, dk, dv, stream or None, flags)
 
 
 def chunk_fwd_kernel(dk, dv, chunk, flags):

@@ -172,40 +172,73 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   return cuda_status(err);
 }
 
-gla_status gla_decode_step(const void* q, const void* k, const void* v, const float* g,
-                           float scale, float* state_inout, void* out, int N, int H, int dk,
-                           int dv, gla_stream_t stream, unsigned flags) {
+namespace {
+
+// The decode step over N sequences whose state pages are either the N pages of
+// `state` (slots == nullptr) or pages slots[n] of a pool of num_slots pages.
+gla_status decode_common(const void* q, const void* k, const void* v, const float* g,
+                         float scale, float* state, int num_slots, const int32_t* slots,
+                         void* out, int N, int H, int dk, int dv, gla_stream_t stream,
+                         unsigned flags) {
   if (!flags_ok(flags) || N < 0 || H < 0 || !std::isfinite(scale)) return GLA_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (slots && num_slots < 0) return GLA_ERR_INVALID_ARG;
   if (N == 0 || H == 0) return GLA_OK;
   const long long units = (long long)N * H;
-  if (units > 0x7fffffffll || units * dk * dv > kMaxElems) return GLA_ERR_INVALID_ARG;
-  if (!q || !k || !v || !g || !state_inout || !out) return GLA_ERR_INVALID_ARG;
+  const long long pages = slots ? (long long)num_slots * H : units;
+  if (units > 0x7fffffffll || pages * dk * dv > kMaxElems) return GLA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !g || !state || !out) return GLA_ERR_INVALID_ARG;
   const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
   const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
   const bool vec = (flags & GLA_FLAG_VECTOR_GATE) != 0;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(state_inout, 16) || !aligned(g, 4))
+      !aligned(state, 16) || !aligned(g, 4) || !aligned(slots, 4))
     return GLA_ERR_MISALIGNED;
   const long long esz = fp32 ? 4 : 2;
-  const size_t st_b = (size_t)(units * dk * dv * 4);
+  const size_t st_b = (size_t)(pages * dk * dv * 4);
   const size_t out_b = (size_t)(units * dv * (f32out ? 4 : 2));
   const size_t v_b = (size_t)(units * dv * esz);
   const size_t qk_b = (size_t)(units * dk * esz);
   const size_t g_b = (size_t)(units * (vec ? dk : 1) * 4);
-  if (overlap(out, out_b, state_inout, st_b) || overlap(out, out_b, q, qk_b) ||
+  const size_t sl_b = slots ? (size_t)N * 4 : 0;
+  if (overlap(out, out_b, state, st_b) || overlap(out, out_b, q, qk_b) ||
       overlap(out, out_b, k, qk_b) || overlap(out, out_b, v, v_b) ||
-      overlap(out, out_b, g, g_b) || overlap(state_inout, st_b, q, qk_b) ||
-      overlap(state_inout, st_b, k, qk_b) || overlap(state_inout, st_b, v, v_b) ||
-      overlap(state_inout, st_b, g, g_b))
+      overlap(out, out_b, g, g_b) || overlap(state, st_b, q, qk_b) ||
+      overlap(state, st_b, k, qk_b) || overlap(state, st_b, v, v_b) ||
+      overlap(state, st_b, g, g_b) || overlap(out, out_b, slots, sl_b) ||
+      overlap(state, st_b, slots, sl_b))
     return GLA_ERR_INVALID_ARG;
 
+  cudaError_t err = cudaSuccess;
+  unsigned* status = nullptr;
+  if (slots) {
+    status = status_word(&err);
+    if (!status) return cuda_status(err);
+  }
   gla::DecodeArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
-  a.state = state_inout; a.out = out;
+  a.state = state; a.slots = slots; a.num_slots = num_slots; a.status = status; a.out = out;
   a.N = N; a.H = H; a.dk = dk; a.dv = dv;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec;
   return cuda_status(gla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+gla_status gla_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           float scale, float* state_inout, void* out, int N, int H, int dk,
+                           int dv, gla_stream_t stream, unsigned flags) {
+  return decode_common(q, k, v, g, scale, state_inout, 0, nullptr, out, N, H, dk, dv, stream,
+                       flags);
+}
+
+gla_status gla_decode_step_slots(const void* q, const void* k, const void* v, const float* g,
+                                 float scale, float* state_pool, int num_slots,
+                                 const int32_t* slots, void* out, int N, int H, int dk, int dv,
+                                 gla_stream_t stream, unsigned flags) {
+  if (!slots) return GLA_ERR_INVALID_ARG;
+  return decode_common(q, k, v, g, scale, state_pool, num_slots, slots, out, N, H, dk, dv,
+                       stream, flags);
 }
 
 gla_status gla_status_sync(gla_stream_t stream) {

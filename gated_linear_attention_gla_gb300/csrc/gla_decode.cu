@@ -46,6 +46,7 @@ template <typename IO, typename OUT, int DK, int DV, bool VEC>
 __global__ void __launch_bounds__(decode_threads(DV), 2)
 decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
               const float* __restrict__ g, float scale, float* __restrict__ state,
+              const int32_t* __restrict__ slots, int num_slots, unsigned* status, int H,
               OUT* __restrict__ out) {
   constexpr int TPR = DV / 4;                   // threads per state row
   constexpr int THREADS = decode_threads(DV);
@@ -64,7 +65,19 @@ decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   const int col4 = tid % TPR;
   const int row0 = tid / TPR;
 
-  float4* S = reinterpret_cast<float4*>(state + unit * (long long)(DK * DV));
+  // the state page: unit itself, or head h of pool page slots[n]
+  long long page = unit;
+  if (slots != nullptr) {
+    const long long n = unit / H;
+    const int slot = __ldg(slots + n);
+    if (slot < 0) return;  // a padding row: no state, no output
+    if (slot >= num_slots) {
+      if (tid == 0) atomicOr(status, kDevBadSeqlens);
+      return;
+    }
+    page = (long long)slot * H + (unit - n * H);
+  }
+  float4* S = reinterpret_cast<float4*>(state + page * (long long)(DK * DV));
 
   // Issue every state load of this thread first (PASSES x 16 bytes in flight).
   float4 s[PASSES];
@@ -115,10 +128,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   const dim3 grid((unsigned)units);
   if (a.vector_gate)
     decode_kernel<IO, OUT, DK, DV, true><<<grid, decode_threads(DV), 0, stream>>>(
-        (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, (OUT*)a.out);
+        (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, a.slots,
+        a.num_slots, a.status, a.H, (OUT*)a.out);
   else
     decode_kernel<IO, OUT, DK, DV, false><<<grid, decode_threads(DV), 0, stream>>>(
-        (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, (OUT*)a.out);
+        (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, a.slots,
+        a.num_slots, a.status, a.H, (OUT*)a.out);
   return cudaGetLastError();
 }
 

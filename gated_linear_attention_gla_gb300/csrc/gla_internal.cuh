@@ -11,6 +11,7 @@ namespace gla {
 enum : unsigned {
   kDevBadSeqlens = 1u << 0,  // a cu_seqlens entry was out of order or out of range
   kDevTimeout = 1u << 1,     // a bounded mbarrier wait gave up
+  // (kDevBadSeqlens also flags a decode slot index outside the state pool)
 };
 
 // Log-decays below -kGateClamp are raised to it before in-chunk cumulative
@@ -40,7 +41,10 @@ struct DecodeArgs {
   const void* v;
   const float* g;
   float scale;
-  float* state;
+  float* state;           // [N, H, dk, dv], or a pool of num_slots pages when slots is set
+  const int32_t* slots;   // device [N]: the pool page of sequence n (-1: skip it), or null
+  int num_slots;
+  unsigned* status;       // device status word (slot out of range)
   void* out;
   int N, H, dk, dv;
   bool fp32_io;

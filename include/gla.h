@@ -100,7 +100,7 @@ typedef enum gla_status {
  *   B, H, T     batch (or number of packed sequences), heads, tokens per
  *               sequence (or packed rows).  B, H, T >= 0; with T = 0 (or empty
  *               sequences) final_state receives init_state (or zeros).
- *   dk, dv      head sizes: 64 or 128 each
+ *   dk, dv      head sizes: dk 64, 96 or 128; dv 64, 128 or 192
  *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O with
  *               dk = 128: the per-head gate with dv = 64 or 128, the
  *               per-key-channel gate with dv = 128), or 16, 32, 64 (fp32 SIMT
@@ -134,12 +134,39 @@ gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const floa
  *   state_inout  fp32 [N, H, dk, dv], read and overwritten in place
  *   out          [N, H, dv], same dtype as q (fp32 with GLA_FLAG_FP32_OUT)
  *   N, H         sequences and heads (>= 0; 0 does nothing)
- *   dk, dv       64 or 128 each
+ *   dk, dv       dk 64, 96 or 128; dv 64, 128 or 192
  * Alignment: every pointer 16-byte aligned except g (4-byte).
  */
 gla_status gla_decode_step(const void *q, const void *k, const void *v, const float *g,
                            float scale, float *state_inout, void *out, int N, int H,
                            int dk, int dv, gla_stream_t stream, unsigned flags);
+
+/*
+ * gla_decode_step_slots -- the decode step with the states held in a pool of
+ * pages, sequence n using page slots[n].
+ *
+ * Source: as gla_decode_step; the page's serving setup keeps one fixed state
+ * page per sequence in a pool that the token mixer reads and writes (section
+ * "Inference optimization on Trainium2").  Indexing the pool lets sequences
+ * arrive and leave without moving state, and lets a batch be padded to a
+ * fixed width (for CUDA-graph replay) with rows that do nothing.
+ *
+ * Arguments: as gla_decode_step, except
+ *   state_pool   fp32 [num_slots, H, dk, dv]; page slots[n] is read and
+ *                overwritten in place for sequence n
+ *   num_slots    pages in the pool (>= 0)
+ *   slots        DEVICE int32 [N]: the page of each row.  -1 marks a padding
+ *                row: its state is not touched and its out row not written.
+ *                The slots of one call must be distinct (two rows on one page
+ *                race).  A slot >= num_slots is reported by gla_status_sync
+ *                as GLA_ERR_INVALID_ARG and that row does nothing.
+ * Returns GLA_ERR_INVALID_ARG for a null slots pointer; alignment as
+ * gla_decode_step (slots 4-byte aligned).
+ */
+gla_status gla_decode_step_slots(const void *q, const void *k, const void *v, const float *g,
+                                 float scale, float *state_pool, int num_slots,
+                                 const int32_t *slots, void *out, int N, int H, int dk, int dv,
+                                 gla_stream_t stream, unsigned flags);
 
 /*
  * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call

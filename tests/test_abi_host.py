@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("gla_chunk_fwd", "gla_decode_step", "gla_status_string", "gla_status_sync"):
+    for n in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots", "gla_status_string",
+              "gla_status_sync"):
         assert n in names
 
 
@@ -124,6 +125,30 @@ def test_decode_step_rejects_before_launch(L, kw, status):
     assert decode(**kw) == status
 
 
+def decode_slots(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, pool=FAKE[4],
+                 num_slots=16, slots=FAKE[6], out=FAKE[5], N=8, H=4, dk=128, dv=128, flags=0):
+    return _binding.gla_decode_step_slots(q, k, v, g, scale, pool, num_slots, slots, out, N, H,
+                                          dk, dv, 0, flags)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(slots=0), E.GLA_ERR_INVALID_ARG),
+    (dict(num_slots=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(slots=FAKE[6] + 2), E.GLA_ERR_MISALIGNED),
+    (dict(dv=96), E.GLA_ERR_UNSUPPORTED),
+    (dict(out=FAKE[4]), E.GLA_ERR_INVALID_ARG),        # out inside the pool
+    (dict(slots=FAKE[4] + 64), E.GLA_ERR_INVALID_ARG),  # slots inside the pool
+    (dict(num_slots=1 << 20, H=1 << 12), E.GLA_ERR_INVALID_ARG),  # pool too large
+])
+def test_decode_slots_rejects_before_launch(L, kw, status):
+    assert decode_slots(**kw) == status
+
+
+def test_decode_slots_empty_is_no_op(L):
+    assert decode_slots(N=0) == E.GLA_OK
+    assert decode_slots(H=0) == E.GLA_OK
+
+
 def test_decode_step_empty_is_no_op(L):
     assert decode(N=0) == E.GLA_OK
     assert decode(H=0) == E.GLA_OK
@@ -132,7 +157,8 @@ def test_decode_step_empty_is_no_op(L):
 def test_ctypes_signatures_match_header(L):
     """The binding's argument counts equal the header's parameter counts."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_status_sync", "gla_status_string"):
+    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots", "gla_status_sync",
+                 "gla_status_string"):
         m = re.search(name + r"\s*\(([^)]*)\)", text)
         nparams = len([p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"])
         assert len(getattr(L, name).argtypes) == nparams, name

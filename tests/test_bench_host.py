@@ -116,3 +116,16 @@ def test_clock_sampler_parses_nvidia_smi_rows(tmp_path, monkeypatch):
     assert c["samples"] == 2 and c["sm_max_mhz"] == 2070.0
     assert c["sm_mhz"] == pytest.approx((1995 + 2070) / 2)
     assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_decode_bucket_choice():
+    from gated_linear_attention_gla_gb300.serving import default_buckets, pick_bucket
+    assert default_buckets(1) == [1]
+    assert default_buckets(8) == [1, 2, 4, 8]
+    assert default_buckets(12) == [1, 2, 4, 8, 12]
+    b = default_buckets(12)
+    assert [pick_bucket(b, n) for n in (1, 2, 3, 5, 8, 9, 12)] == [1, 2, 4, 8, 8, 12, 12]
+    with pytest.raises(ValueError):
+        pick_bucket(b, 13)
+    with pytest.raises(ValueError):
+        default_buckets(0)

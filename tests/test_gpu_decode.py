@@ -102,3 +102,70 @@ def test_decode_full_size_sampled(cuda_ok):
                                           x["g"][t][ns], x["scale"], S_ref)
         assert rel_max(to_np(outs[t][ns]), o_ref) <= out_tol(torch.bfloat16)
     assert rel_max(to_np(S[ns]), S_ref) <= TOL_STATE
+
+
+# ---------------------------------------------------------------------------
+# Slot-indexed state pages and CUDA-graph decode buckets.
+# ---------------------------------------------------------------------------
+def test_decode_slots_match_dense_pages(cuda_ok):
+    """Rows on pool pages slots[n] give the same outputs and states as the
+    dense call on the gathered pages; pages no row names are untouched; a
+    padding row (-1) neither writes its output nor touches any page."""
+    gla = _gla()
+    w = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(w, steps=1, N=6, H=3)
+    pool = torch.randn(10, 3, w.dk, w.dv, generator=torch.Generator().manual_seed(4)) * 0.1
+    slots = torch.tensor([7, 2, -1, 9, 0, 4], dtype=torch.int32)
+    live = slots >= 0
+    pool_gpu = cuda(pool).contiguous()
+    out = torch.full((6, 3, w.dv), 7.0, dtype=torch.float32, device="cuda")
+    gla.decode_step(cuda(d["q"][0]), cuda(d["k"][0]), cuda(d["v"][0]), cuda(d["g"][0]),
+                    pool_gpu, scale=d["scale"], out=out, slots=cuda(slots))
+    gla.status_sync()
+    dense = cuda(pool[slots[live].long()]).contiguous()
+    ref = gla.decode_step(cuda(d["q"][0][live]), cuda(d["k"][0][live]), cuda(d["v"][0][live]),
+                          cuda(d["g"][0][live]), dense, scale=d["scale"],
+                          out_dtype=torch.float32)
+    gla.status_sync()
+    assert torch.equal(out[live], ref)
+    assert (out[~live] == 7.0).all()
+    assert torch.equal(pool_gpu[slots[live].long()], dense)
+    untouched = [i for i in range(10) if i not in set(slots.tolist())]
+    assert torch.equal(pool_gpu[untouched].cpu(), pool[untouched])
+
+
+def test_decode_slot_out_of_range_is_reported(cuda_ok):
+    gla = _gla()
+    w = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(w, steps=1, N=2, H=2)
+    pool = torch.zeros(4, 2, w.dk, w.dv, device="cuda")
+    with pytest.raises(gla.GlaError) as e:
+        gla.decode_step(cuda(d["q"][0]), cuda(d["k"][0]), cuda(d["v"][0]), cuda(d["g"][0]),
+                        pool, slots=cuda(torch.tensor([1, 4], dtype=torch.int32)))
+        gla.status_sync()
+    assert e.value.status == 1
+    gla.status_sync()  # cleared
+
+
+def test_decode_graph_buckets_replay_the_eager_step(cuda_ok):
+    """Steps of varying width through the captured buckets equal the eager
+    slot-indexed step on a copy of the pool, step after step."""
+    gla = _gla()
+    from gated_linear_attention_gla_gb300.serving import DecodeGraphs
+    w = gla_inputs.WORKLOADS["decode"]
+    H, S = 2, 12
+    pool = (torch.randn(S, H, w.dk, w.dv, generator=torch.Generator().manual_seed(8)) * 0.1).cuda()
+    pool_ref = pool.clone()
+    graphs = DecodeGraphs(pool, max_width=8, out_dtype=torch.float32)
+    assert graphs.buckets == [1, 2, 4, 8]
+    rng = torch.Generator().manual_seed(21)
+    for step, n in enumerate([3, 8, 1, 5, 5, 2]):
+        d = gla_inputs.decode_inputs(w, steps=1, N=n, H=H, seed=100 + step)
+        slots = torch.randperm(S, generator=rng)[:n].to(torch.int32)
+        args = [cuda(d[x][0]) for x in ("q", "k", "v", "g")]
+        got = graphs.step(*args, cuda(slots)).clone()
+        ref = gla.decode_step(*args, pool_ref, scale=w.dk ** -0.5, slots=cuda(slots),
+                              out_dtype=torch.float32)
+        gla.status_sync()
+        assert torch.equal(got, ref), step
+        assert torch.equal(pool, pool_ref), step
