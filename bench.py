@@ -297,6 +297,46 @@ def time_side_workloads(gla, dev, hbm, peak_kind, reps=10, warmup=3):
     return out
 
 
+def time_decode_graphs(gla, dev, width=64, steps=200):
+    """A small decode batch (`width` sequences, the decode workload's heads and
+    head sizes, states in a pool addressed by slot): `steps` consecutive steps
+    launched one by one from Python, then replayed from the captured CUDA graph
+    of that width (inputs in the graph's buffers).  At this size launch
+    overhead, not HBM, sets the step time (the 67 MB pool stays in L2)."""
+    from gated_linear_attention_gla_gb300.serving import DecodeGraphs
+    w = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(w, steps=1, N=width)
+    q, k, v, g = (d[n][0].to(dev) for n in ("q", "k", "v", "g"))
+    pool = d["state"].to(dev).contiguous()
+    slots = torch.arange(width, dtype=torch.int32, device=dev)
+    out = torch.empty(width, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / steps
+    eager = timed(lambda: gla.decode_step(q, k, v, g, pool, scale=d["scale"], out=out,
+                                          slots=slots))
+    graphs = DecodeGraphs(pool, max_width=width)
+    buf = graphs.buffers(width)  # the inputs written once, where a producer would write them
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("slots", slots)):
+        buf[name].copy_(t)
+    graph = timed(lambda: graphs.run(width))
+    gla.status_sync()
+    nbytes = width * w.H * (8 * w.dk * w.dv + 2 * (2 * w.dk + w.dv) + 4 + 2 * w.dv)
+    return {"workload": f"decode step N={width} H={w.H} dk=dv={w.dk}, states in a slot pool",
+            "steps": steps, "eager_us_per_step": eager, "graph_us_per_step": graph,
+            "algorithmic_bytes_per_step": nbytes, "graph_gbs": nbytes / graph / 1e3}
+
+
 def run_gla(args, world, rank, local):
     import gated_linear_attention_gla_gb300 as gla
     from gated_linear_attention_gla_gb300 import build as glabuild
@@ -493,6 +533,7 @@ def run_gla(args, world, rank, local):
     if not args.no_side_workloads:
         # timed after the step (outside ms_per_step and gpu_launches)
         line["prefill_workloads"] = time_side_workloads(gla, dev, hbm, peak_kind)
+        line["decode_graphs"] = [time_decode_graphs(gla, dev, width=n) for n in (8, 64)]
     if world == 1 and not args.no_cpu_baseline:
         pre_cpu, dec_cpu = cpu_baseline(args.cpu_budget)
         line["cpu_baseline"] = pre_cpu

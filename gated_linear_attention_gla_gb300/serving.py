@@ -11,8 +11,10 @@ copied into the first n rows of the static buffers, the remaining W - n rows
 get slot -1 (rows the kernel skips), and the graph of width W is replayed.
 
 The state pool, the dtypes and the head sizes are fixed at construction.  The
-output returned by ``step`` is a view of the static output buffer, valid until
-the next ``step``.
+fast path is ``buffers(n)`` (views of the static inputs, for the producer of
+q, k, v, g and slots to write into) followed by ``run(n)``; ``step`` copies
+given tensors in first (five extra copies per step).  The output is a view of
+the static output buffer, valid until the next step.
 """
 from __future__ import annotations
 
@@ -94,18 +96,28 @@ class DecodeGraphs:
         decode_step(self.q[:w], self.k[:w], self.v[:w], self.g[:w], self.pool,
                     scale=self.scale, out=self.out[:w], slots=self.slots[:w])
 
-    def step(self, q, k, v, g, slots):
-        """Decode one token for ``n = q.shape[0]`` rows whose states are the pool
-        pages ``slots`` (int32 [n], distinct).  Returns out [n, H, dv] (a view of
-        the static buffer, valid until the next step)."""
-        n = q.shape[0]
+    def buffers(self, n: int):
+        """Views of the first ``n`` rows of the static inputs (q, k, v, g, slots)
+        for the next ``run(n)``."""
+        pick_bucket(self.buckets, n)
+        return {"q": self.q[:n], "k": self.k[:n], "v": self.v[:n], "g": self.g[:n],
+                "slots": self.slots[:n]}
+
+    def run(self, n: int):
+        """Decode one token for the ``n`` rows already in ``buffers(n)`` (their
+        slots distinct pool pages): pad to the bucket with slot -1 rows and
+        replay its graph.  Returns out [n, H, dv]."""
         w = pick_bucket(self.buckets, n)
-        self.q[:n].copy_(q, non_blocking=True)
-        self.k[:n].copy_(k, non_blocking=True)
-        self.v[:n].copy_(v, non_blocking=True)
-        self.g[:n].copy_(g, non_blocking=True)
-        self.slots[:n].copy_(slots, non_blocking=True)
         if w > n:
             self.slots[n:w].fill_(-1)
         self.graphs[w].replay()
         return self.out[:n]
+
+    def step(self, q, k, v, g, slots):
+        """``run`` after copying q, k, v, g and slots (int32 [n]) into the
+        static buffers."""
+        n = q.shape[0]
+        b = self.buffers(n)
+        for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("slots", slots)):
+            b[name].copy_(t, non_blocking=True)
+        return self.run(n)

@@ -163,7 +163,13 @@ def test_decode_graph_buckets_replay_the_eager_step(cuda_ok):
         d = gla_inputs.decode_inputs(w, steps=1, N=n, H=H, seed=100 + step)
         slots = torch.randperm(S, generator=rng)[:n].to(torch.int32)
         args = [cuda(d[x][0]) for x in ("q", "k", "v", "g")]
-        got = graphs.step(*args, cuda(slots)).clone()
+        if step % 2:
+            got = graphs.step(*args, cuda(slots)).clone()
+        else:
+            buf = graphs.buffers(n)
+            for name, t in zip(("q", "k", "v", "g", "slots"), (*args, cuda(slots))):
+                buf[name].copy_(t)
+            got = graphs.run(n).clone()
         ref = gla.decode_step(*args, pool_ref, scale=w.dk ** -0.5, slots=cuda(slots),
                               out_dtype=torch.float32)
         gla.status_sync()
