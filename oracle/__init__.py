@@ -33,6 +33,9 @@ bruteforce    the unrolled recurrence as one O(T^2) sum per token, numpy, tiny
               inputs only
 decay_schedule  the page's fixed geometric per-head decay (paragraph "Decay
               schedule's reach")
+mixer_epilogue  what follows the readout in the page's mixer (paragraph "GLA
+              mixer", after the readout): self-augmentation, head RMSNorm,
+              SiLU output gate; numpy, fp64
 
 Every pin of these functions lives in ``tests/test_oracle_pins.py``.
 """
@@ -252,3 +255,35 @@ def decay_schedule(H: int = 16, t_min: float = 1.0, t_max: float = 2048.0):
     h = np.arange(H, dtype=np.float64)
     half_life = t_min * (t_max / t_min) ** (h / (H - 1))
     return 2.0 ** (-1.0 / half_life)
+
+
+def mixer_epilogue(o, q, k, v, aug=None, norm_w=None, eps=1e-6, z=None):
+    """The steps after the readout, per token and head, in fp64 (numpy):
+
+    * self-augmentation (when ``aug`` is given): ``o += sigmoid(q . (aug * k)) * v``
+      -- the page adds the value, gated by the query dotted with a learned
+      per-key-channel rescaling ``aug`` of the key (``aug = 0`` gives half of v);
+    * head RMSNorm (when ``norm_w`` is given): ``o = o / sqrt(mean_j o_j^2 + eps)
+      * norm_w[h]`` over the head's dv channels (heads of one decay tier share a
+      weight row: the caller lays the rows out per head);
+    * output gate (when ``z`` is given): ``o *= silu(z)`` with ``silu(x) = x *
+      sigmoid(x)``.
+
+    Shapes: ``o, v [.., H, dv]``, ``q, k [.., H, dk]``, ``aug [H, dk]``,
+    ``norm_w [H, dv]``, ``z [.., H, dv]``.  Returns a new fp64 array.
+    """
+    def sigmoid(x):  # 1 / (1 + exp(-x)), written with tanh so that no exp overflows
+        return 0.5 * (1.0 + np.tanh(0.5 * x))
+
+    o = _f64(o).copy()
+    if aug is not None:
+        q, k, v, a = _f64(q), _f64(k), _f64(v), _f64(aug)
+        s = np.sum(q * a * k, axis=-1, keepdims=True)
+        o = o + sigmoid(s) * v
+    if norm_w is not None:
+        w = _f64(norm_w)
+        o = o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * w
+    if z is not None:
+        zz = _f64(z)
+        o = o * (zz * sigmoid(zz))
+    return o

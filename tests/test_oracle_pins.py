@@ -429,3 +429,71 @@ def test_laplace_workload_gate_is_the_decay_schedule():
     g = x["g"].double().numpy()
     assert g.shape == (1, 3, 16)
     np.testing.assert_allclose(np.exp(g[0]), np.broadcast_to(lam, (3, 16)), rtol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# The mixer epilogue (self-augmentation, head RMSNorm, SiLU gate).
+# ---------------------------------------------------------------------------
+def _epi_inputs(seed=0, n=5, H=3, dk=8, dv=6):
+    r = np.random.default_rng(seed)
+    return (r.normal(size=(n, H, dv)), r.normal(size=(n, H, dk)), r.normal(size=(n, H, dk)),
+            r.normal(size=(n, H, dv)))
+
+
+def test_epilogue_augmentation_at_zero_balance_adds_half_the_value():
+    """The page: at initialisation (aug = 0) the augmentation is a
+    half-strength skip of the value."""
+    o, q, k, v = _epi_inputs()
+    got = oracle.mixer_epilogue(o, q, k, v, aug=np.zeros((3, 8)))
+    np.testing.assert_allclose(got, o + 0.5 * v, rtol=0, atol=1e-15)
+
+
+def test_epilogue_augmentation_gate_limits():
+    """A large positive (negative) q . (aug * k) passes all (none) of v; the
+    gate is the logistic function of that one number per token and head."""
+    o, q, k, v = _epi_inputs(1)
+    big = 1e3 * np.ones((3, 8))
+    s = np.sum(q * big * k, axis=-1, keepdims=True)
+    got = oracle.mixer_epilogue(o, q, k, v, aug=big)
+    np.testing.assert_allclose(got, o + np.where(s > 0, v, 0.0), atol=1e-12)
+    a = np.linspace(-1, 1, 8)[None, :].repeat(3, 0)
+    t = np.einsum("nhd,hd,nhd->nh", q, a, k)[..., None]
+    np.testing.assert_allclose(oracle.mixer_epilogue(o, q, k, v, aug=a) - o,
+                               v * (1 / (1 + np.exp(-t))), rtol=1e-13)
+
+
+def test_epilogue_rmsnorm_gives_unit_rms_and_ignores_the_row_scale():
+    o, q, k, v = _epi_inputs(2)
+    w = np.ones((3, 6))
+    y = oracle.mixer_epilogue(o, q, k, v, norm_w=w, eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)
+    y2 = oracle.mixer_epilogue(o * np.array([3.0, 0.25, 7.0])[None, :, None], q, k, v,
+                               norm_w=w, eps=0.0)
+    np.testing.assert_allclose(y2, y, rtol=1e-12)
+    # the weight multiplies channel by channel, after the normalisation
+    wv = np.arange(1, 7)[None, :].repeat(3, 0) * 1.0
+    np.testing.assert_allclose(oracle.mixer_epilogue(o, q, k, v, norm_w=wv, eps=0.0), y * wv,
+                               rtol=1e-13)
+    # eps bounds the gain of a zero row
+    assert np.all(oracle.mixer_epilogue(np.zeros_like(o), q, k, v, norm_w=w, eps=1e-6) == 0)
+
+
+def test_epilogue_silu_gate():
+    o, q, k, v = _epi_inputs(3)
+    zero = oracle.mixer_epilogue(o, q, k, v, z=np.zeros_like(o))
+    assert np.all(zero == 0)
+    big = oracle.mixer_epilogue(o, q, k, v, z=np.full_like(o, 40.0))
+    np.testing.assert_allclose(big, 40.0 * o, rtol=1e-15)
+    # silu(-x) = silu(x) - x
+    zz = np.random.default_rng(4).normal(size=o.shape)
+    np.testing.assert_allclose(oracle.mixer_epilogue(o, q, k, v, z=-zz),
+                               oracle.mixer_epilogue(o, q, k, v, z=zz) - zz * o, atol=1e-13)
+
+
+def test_epilogue_order_augment_then_normalise_then_gate():
+    o, q, k, v = _epi_inputs(5)
+    a, w, zz = np.zeros((3, 8)), np.ones((3, 6)), np.full_like(o, 40.0)
+    y = oracle.mixer_epilogue(o, q, k, v, aug=a, norm_w=w, eps=0.0, z=zz)
+    x = o + 0.5 * v
+    ref = 40.0 * x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
+    np.testing.assert_allclose(y, ref, rtol=1e-13)
