@@ -49,6 +49,24 @@ def _out_dtype(q: torch.Tensor, out, out_dtype):
     return out_dtype
 
 
+def _mixer_args(mixer, q, H, dk, dv, lead):
+    """Check the mixer epilogue options {aug [H, dk], norm_w [H, dv] (fp32),
+    eps, z [*lead, H, dv] (q's dtype)}; returns (aug, norm_w, eps, z)."""
+    if mixer is None:
+        return None, None, 0.0, None
+    unknown = set(mixer) - {"aug", "norm_w", "eps", "z"}
+    _check(not unknown, f"unknown mixer options {sorted(unknown)}")
+    aug, norm_w, z = mixer.get("aug"), mixer.get("norm_w"), mixer.get("z")
+    eps = float(mixer.get("eps", 1e-6))
+    for name, t, shape, dt in (("aug", aug, (H, dk), torch.float32),
+                               ("norm_w", norm_w, (H, dv), torch.float32),
+                               ("z", z, (*lead, H, dv), q.dtype)):
+        if t is not None:
+            _check(t.is_cuda and t.is_contiguous() and t.dtype == dt and tuple(t.shape) == shape,
+                   f"mixer {name} must be a contiguous {dt} CUDA tensor {shape}")
+    return aug, norm_w, eps, z
+
+
 def _io_flags(q: torch.Tensor, g: torch.Tensor, gate_shape_scalar, gate_shape_vector,
               out_dtype) -> int:
     _check(q.dtype in (torch.bfloat16, torch.float32), "q/k/v must be bf16 or fp32")
@@ -66,7 +84,7 @@ def _io_flags(q: torch.Tensor, g: torch.Tensor, gate_shape_scalar, gate_shape_ve
 
 def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seqlens=None,
               chunk: int = 128, out=None, final_state=None, output_final_state: bool = True,
-              stream=None, out_dtype=None):
+              stream=None, out_dtype=None, mixer=None):
     """Chunked GLA prefill; returns ``(out, final_state)``.
 
     Dense: ``q, k [B, T, H, dk]``, ``v [B, T, H, dv]``, ``g [B, T, H]`` or
@@ -74,6 +92,11 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
     with ``cu_seqlens`` int32 ``[B+1]`` on the device.  ``init_state`` and the
     returned ``final_state`` are fp32 ``[B, H, dk, dv]``.  ``out`` has q's dtype,
     or fp32 (``out_dtype=torch.float32``) for bf16 inputs.
+
+    ``mixer`` (optional dict): the steps after the readout, applied to out in
+    place by gla_mixer_epilogue -- ``aug`` fp32 [H, dk] (self-augmentation),
+    ``norm_w`` fp32 [H, dv] and ``eps`` (head RMSNorm), ``z`` [.., H, dv] in
+    q's dtype (SiLU output gate); absent keys skip their step.
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
         _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
@@ -103,23 +126,34 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
         out = torch.empty(v.shape, dtype=out_dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    aug, norm_w, eps, z = _mixer_args(mixer, q, H, dk, dv, q.shape[:-2])
     rc = _binding.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state),
                                 _ptr(out), _ptr(final_state), _ptr(cu_seqlens), B, H, T, dk,
                                 dv, chunk, _stream(stream), flags)
     if rc != 0:
         raise GlaError(rc, "gla_chunk_fwd")
+    if mixer is not None:
+        rows = q.numel() // (H * dk)
+        eflags = flags & (GLA_FLAG_FP32_IO | GLA_FLAG_FP32_OUT)
+        rc = _binding.gla_mixer_epilogue(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(aug),
+                                         _ptr(norm_w), eps, _ptr(z), rows, H, dk, dv,
+                                         _stream(stream), eflags)
+        if rc != 0:
+            raise GlaError(rc, "gla_mixer_epilogue")
     return out, final_state
 
 
 def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stream=None,
-                out_dtype=None, slots=None):
+                out_dtype=None, slots=None, mixer=None):
     """One recurrent step for N sequences; ``state [N, H, dk, dv]`` (fp32) is
     updated in place.  ``q, k [N, H, dk]``, ``v [N, H, dv]``, ``g [N, H]`` or
     ``[N, H, dk]``.  Returns ``out [N, H, dv]`` in q's dtype (or fp32).
 
     With ``slots`` (int32 [N] on the GPU) ``state`` is a pool
     ``[num_slots, H, dk, dv]`` and row n uses page ``slots[n]`` (-1: a padding
-    row that does nothing; see gla_decode_step_slots)."""
+    row that does nothing; see gla_decode_step_slots).  ``mixer``: the steps
+    after the readout, fused into the step (as for ``chunk_fwd``; ``z`` is
+    [N, H, dv])."""
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("state", state)):
         _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     _check(q.dim() == 3 and k.shape == q.shape and v.shape[:-1] == q.shape[:-1],
@@ -142,7 +176,14 @@ def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stre
         scale = dk ** -0.5
     if out is None:
         out = torch.empty((N, H, dv), dtype=out_dtype, device=q.device)
-    if slots is None:
+    if mixer is not None:
+        aug, norm_w, eps, z = _mixer_args(mixer, q, H, dk, dv, (N,))
+        rc = _binding.gla_decode_step_mixer(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(state),
+            0 if slots is None else state.shape[0], _ptr(slots), _ptr(out), N, H, dk, dv,
+            _ptr(aug), _ptr(norm_w), eps, _ptr(z), _stream(stream), flags)
+        name = "gla_decode_step_mixer"
+    elif slots is None:
         rc = _binding.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(state),
                                       _ptr(out), N, H, dk, dv, _stream(stream), flags)
         name = "gla_decode_step"

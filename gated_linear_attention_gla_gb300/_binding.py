@@ -62,6 +62,13 @@ def lib() -> ctypes.CDLL:
             L.gla_decode_step_slots.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i, _vp,
                                                 _vp, _i, _i, _i, _i, _vp, ctypes.c_uint]
             L.gla_decode_step_slots.restype = _i
+            L.gla_decode_step_mixer.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i, _vp,
+                                                _vp, _i, _i, _i, _i, _vp, _vp, ctypes.c_float,
+                                                _vp, _vp, ctypes.c_uint]
+            L.gla_decode_step_mixer.restype = _i
+            L.gla_mixer_epilogue.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                             _i, _i, _i, _i, _vp, ctypes.c_uint]
+            L.gla_mixer_epilogue.restype = _i
             L.gla_status_string.argtypes = [_i]
             L.gla_status_string.restype = ctypes.c_char_p
             L.gla_status_sync.argtypes = [_vp]
@@ -106,6 +113,22 @@ def gla_decode_step_slots(q, k, v, g, scale, state_pool, num_slots, slots, out, 
     return lib().gla_decode_step_slots(q or None, k or None, v or None, g or None, float(scale),
                                        state_pool or None, num_slots, slots or None,
                                        out or None, N, H, dk, dv, stream or None, flags)
+
+
+def gla_decode_step_mixer(q, k, v, g, scale, state, num_slots, slots, out, N, H, dk, dv, aug,
+                          norm_w, eps, z, stream, flags) -> int:
+    """Raw call: pointers are ints, ``stream`` an int handle."""
+    return lib().gla_decode_step_mixer(q or None, k or None, v or None, g or None, float(scale),
+                                       state or None, num_slots, slots or None, out or None, N,
+                                       H, dk, dv, aug or None, norm_w or None, float(eps),
+                                       z or None, stream or None, flags)
+
+
+def gla_mixer_epilogue(out, q, k, v, aug, norm_w, eps, z, rows, H, dk, dv, stream, flags) -> int:
+    """Raw call: pointers are ints, ``stream`` an int handle."""
+    return lib().gla_mixer_epilogue(out or None, q or None, k or None, v or None, aug or None,
+                                    norm_w or None, float(eps), z or None, rows, H, dk, dv,
+                                    stream or None, flags)
 
 
 def chunk_fwd_kernel(dk, dv, chunk, flags):

@@ -178,9 +178,12 @@ namespace {
 // `state` (slots == nullptr) or pages slots[n] of a pool of num_slots pages.
 gla_status decode_common(const void* q, const void* k, const void* v, const float* g,
                          float scale, float* state, int num_slots, const int32_t* slots,
-                         void* out, int N, int H, int dk, int dv, gla_stream_t stream,
+                         void* out, int N, int H, int dk, int dv, const float* aug,
+                         const float* norm_w, float eps, const void* z, gla_stream_t stream,
                          unsigned flags) {
-  if (!flags_ok(flags) || N < 0 || H < 0 || !std::isfinite(scale)) return GLA_ERR_INVALID_ARG;
+  if (!flags_ok(flags) || N < 0 || H < 0 || !std::isfinite(scale) || !std::isfinite(eps) ||
+      eps < 0.f)
+    return GLA_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
   if (slots && num_slots < 0) return GLA_ERR_INVALID_ARG;
   if (N == 0 || H == 0) return GLA_OK;
@@ -208,6 +211,15 @@ gla_status decode_common(const void* q, const void* k, const void* v, const floa
       overlap(state, st_b, g, g_b) || overlap(out, out_b, slots, sl_b) ||
       overlap(state, st_b, slots, sl_b))
     return GLA_ERR_INVALID_ARG;
+  if (!aligned(aug, 4) || !aligned(norm_w, 4) || !aligned(z, (uintptr_t)esz))
+    return GLA_ERR_MISALIGNED;
+  const size_t z_b = z ? (size_t)(units * dv * esz) : 0;
+  if (overlap(out, out_b, z, z_b) || overlap(state, st_b, z, z_b) ||
+      overlap(out, out_b, aug, aug ? (size_t)H * dk * 4 : 0) ||
+      overlap(out, out_b, norm_w, norm_w ? (size_t)H * dv * 4 : 0) ||
+      overlap(state, st_b, aug, aug ? (size_t)H * dk * 4 : 0) ||
+      overlap(state, st_b, norm_w, norm_w ? (size_t)H * dv * 4 : 0))
+    return GLA_ERR_INVALID_ARG;
 
   cudaError_t err = cudaSuccess;
   unsigned* status = nullptr;
@@ -218,6 +230,7 @@ gla_status decode_common(const void* q, const void* k, const void* v, const floa
   gla::DecodeArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
   a.state = state; a.slots = slots; a.num_slots = num_slots; a.status = status; a.out = out;
+  a.aug = aug; a.norm_w = norm_w; a.eps = eps; a.z = z;
   a.N = N; a.H = H; a.dk = dk; a.dv = dv;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec;
   return cuda_status(gla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -228,8 +241,8 @@ gla_status decode_common(const void* q, const void* k, const void* v, const floa
 gla_status gla_decode_step(const void* q, const void* k, const void* v, const float* g,
                            float scale, float* state_inout, void* out, int N, int H, int dk,
                            int dv, gla_stream_t stream, unsigned flags) {
-  return decode_common(q, k, v, g, scale, state_inout, 0, nullptr, out, N, H, dk, dv, stream,
-                       flags);
+  return decode_common(q, k, v, g, scale, state_inout, 0, nullptr, out, N, H, dk, dv, nullptr,
+                       nullptr, 0.f, nullptr, stream, flags);
 }
 
 gla_status gla_decode_step_slots(const void* q, const void* k, const void* v, const float* g,
@@ -238,7 +251,51 @@ gla_status gla_decode_step_slots(const void* q, const void* k, const void* v, co
                                  gla_stream_t stream, unsigned flags) {
   if (!slots) return GLA_ERR_INVALID_ARG;
   return decode_common(q, k, v, g, scale, state_pool, num_slots, slots, out, N, H, dk, dv,
-                       stream, flags);
+                       nullptr, nullptr, 0.f, nullptr, stream, flags);
+}
+
+gla_status gla_decode_step_mixer(const void* q, const void* k, const void* v, const float* g,
+                                 float scale, float* state, int num_slots, const int32_t* slots,
+                                 void* out, int N, int H, int dk, int dv, const float* aug,
+                                 const float* norm_w, float eps, const void* z,
+                                 gla_stream_t stream, unsigned flags) {
+  if (slots == nullptr && num_slots != 0) return GLA_ERR_INVALID_ARG;
+  return decode_common(q, k, v, g, scale, state, num_slots, slots, out, N, H, dk, dv, aug,
+                       norm_w, eps, z, stream, flags);
+}
+
+gla_status gla_mixer_epilogue(void* out, const void* q, const void* k, const void* v,
+                              const float* aug, const float* norm_w, float eps, const void* z,
+                              int rows, int H, int dk, int dv, gla_stream_t stream,
+                              unsigned flags) {
+  if ((flags & ~(GLA_FLAG_FP32_IO | GLA_FLAG_FP32_OUT)) != 0u || rows < 0 || H < 0 ||
+      !std::isfinite(eps) || eps < 0.f)
+    return GLA_ERR_INVALID_ARG;
+  if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  if (rows == 0 || H == 0) return GLA_OK;
+  const long long units = (long long)rows * H;
+  if (units * dk > kMaxElems || units * dv > kMaxElems) return GLA_ERR_INVALID_ARG;
+  if (!out || (aug && (!q || !k || !v))) return GLA_ERR_INVALID_ARG;
+  const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
+  const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
+  const size_t esz = fp32 ? 4 : 2, osz = f32out ? 4 : 2;
+  if (!aligned(out, osz) || !aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) ||
+      !aligned(z, esz) || !aligned(aug, 4) || !aligned(norm_w, 4))
+    return GLA_ERR_MISALIGNED;
+  const size_t out_b = (size_t)(units * dv) * osz;
+  const size_t qk_b = aug ? (size_t)(units * dk) * esz : 0;
+  const size_t v_b = aug ? (size_t)(units * dv) * esz : 0;
+  const size_t z_b = z ? (size_t)(units * dv) * esz : 0;
+  if (overlap(out, out_b, q, qk_b) || overlap(out, out_b, k, qk_b) ||
+      overlap(out, out_b, v, v_b) || overlap(out, out_b, z, z_b) ||
+      overlap(out, out_b, aug, aug ? (size_t)H * dk * 4 : 0) ||
+      overlap(out, out_b, norm_w, norm_w ? (size_t)H * dv * 4 : 0))
+    return GLA_ERR_INVALID_ARG;
+  if (!aug && !norm_w && !z) return GLA_OK;
+  gla::EpilogueArgs a;
+  a.out = out; a.q = q; a.k = k; a.v = v; a.aug = aug; a.norm_w = norm_w; a.eps = eps; a.z = z;
+  a.rows = rows; a.H = H; a.dk = dk; a.dv = dv; a.fp32_io = fp32; a.fp32_out = f32out;
+  return cuda_status(gla::launch_epilogue(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gla_status gla_status_sync(gla_stream_t stream) {

@@ -17,7 +17,10 @@
 //   * loads and stores carry streaming (evict-first) cache hints: the state
 //     is touched once per step;
 //   * q . S' is accumulated per column in registers across the rows a thread
-//     owns, then reduced over the row groups through shared memory.
+//     owns, then reduced over the row groups through shared memory;
+//   * optionally the mixer's steps after the readout follow in the same CTA
+//     (the page's paragraph "GLA mixer"): o += sigmoid(q . (aug * k)) v, the
+//     head RMSNorm over the dv columns, o *= silu(z) -- one thread per column.
 #include "gla_internal.cuh"
 
 namespace gla {
@@ -47,7 +50,8 @@ __global__ void __launch_bounds__(decode_threads(DV), 2)
 decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
               const float* __restrict__ g, float scale, float* __restrict__ state,
               const int32_t* __restrict__ slots, int num_slots, unsigned* status, int H,
-              OUT* __restrict__ out) {
+              OUT* __restrict__ out, const float* __restrict__ aug,
+              const float* __restrict__ norm_w, float eps, const IO* __restrict__ z) {
   constexpr int TPR = DV / 4;                   // threads per state row
   constexpr int THREADS = decode_threads(DV);
   constexpr int RPP = THREADS / TPR;            // rows per pass
@@ -59,6 +63,8 @@ decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   __shared__ float s_k[DK];
   __shared__ float s_a[VEC ? DK : 1];
   __shared__ float s_red[RPP][DV];
+  __shared__ float s_p[DK];              // q_i aug_i k_i (self-augmentation)
+  __shared__ float s_ws[THREADS / 32];   // per-warp sums of o^2 (RMSNorm)
 
   const long long unit = blockIdx.x;  // n * H + h
   const int tid = threadIdx.x;
@@ -89,6 +95,7 @@ decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     s_q[tid] = to_f32(q[unit * DK + tid]);
     s_k[tid] = to_f32(k[unit * DK + tid]);
     if constexpr (VEC) s_a[tid] = expf(__ldg(g + unit * DK + tid));
+    if (aug) s_p[tid] = s_q[tid] * __ldg(aug + (unit % H) * DK + tid) * s_k[tid];
   }
   const float4 vv = Vec4In<IO>::load(v + unit * DV + col4 * 4);
   float a_scalar = 1.0f;
@@ -114,12 +121,36 @@ decode_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   }
   *reinterpret_cast<float4*>(&s_red[row0][col4 * 4]) = acc;
   __syncthreads();
+  float o = 0.f;
   if (tid < DV) {
-    float o = 0.f;
 #pragma unroll
     for (int r = 0; r < RPP; ++r) o += s_red[r][tid];
-    out[unit * DV + tid] = from_f32<OUT>(scale * o);
+    o *= scale;
   }
+  // the mixer's steps after the readout (uniform branches: every thread takes them)
+  const int h = (int)(unit % H);
+  if (aug) {
+    float s = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < DK; ++i) s += s_p[i];
+    if (tid < DV) o = fmaf(1.f / (1.f + expf(-s)), to_f32(v[unit * DV + tid]), o);
+  }
+  if (norm_w) {
+    float x = (tid < DV) ? o * o : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if ((tid & 31) == 0) s_ws[tid >> 5] = x;
+    __syncthreads();
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) ss += s_ws[w];
+    if (tid < DV) o *= rsqrtf(ss / DV + eps) * __ldg(norm_w + h * DV + tid);
+  }
+  if (z && tid < DV) {
+    const float zz = to_f32(z[unit * DV + tid]);
+    o *= zz / (1.f + expf(-zz));
+  }
+  if (tid < DV) out[unit * DV + tid] = from_f32<OUT>(o);
 }
 
 template <typename IO, typename OUT, int DK, int DV>
@@ -129,11 +160,11 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   if (a.vector_gate)
     decode_kernel<IO, OUT, DK, DV, true><<<grid, decode_threads(DV), 0, stream>>>(
         (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, a.slots,
-        a.num_slots, a.status, a.H, (OUT*)a.out);
+        a.num_slots, a.status, a.H, (OUT*)a.out, a.aug, a.norm_w, a.eps, (const IO*)a.z);
   else
     decode_kernel<IO, OUT, DK, DV, false><<<grid, decode_threads(DV), 0, stream>>>(
         (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.g, a.scale, a.state, a.slots,
-        a.num_slots, a.status, a.H, (OUT*)a.out);
+        a.num_slots, a.status, a.H, (OUT*)a.out, a.aug, a.norm_w, a.eps, (const IO*)a.z);
   return cudaGetLastError();
 }
 

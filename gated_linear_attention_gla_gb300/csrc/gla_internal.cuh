@@ -46,15 +46,37 @@ struct DecodeArgs {
   int num_slots;
   unsigned* status;       // device status word (slot out of range)
   void* out;
+  // the mixer steps after the readout (each null = skipped): self-augmentation
+  // weights [H, dk], head RMSNorm weights [H, dv] and eps, output gate [N, H, dv]
+  const float* aug;
+  const float* norm_w;
+  float eps;
+  const void* z;
   int N, H, dk, dv;
   bool fp32_io;
   bool fp32_out;
   bool vector_gate;
 };
 
+struct EpilogueArgs {
+  void* out;              // [rows, H, dv], updated in place
+  const void* q;          // [rows, H, dk] (with aug)
+  const void* k;
+  const void* v;          // [rows, H, dv] (with aug)
+  const float* aug;       // [H, dk] or null
+  const float* norm_w;    // [H, dv] or null
+  float eps;
+  const void* z;          // [rows, H, dv] or null
+  long long rows;
+  int H, dk, dv;
+  bool fp32_io;           // q, k, v, z fp32 (else bf16)
+  bool fp32_out;          // out fp32 (else bf16)
+};
+
 // Kernel launchers (one per translation unit).  They assume validated arguments
 // and a non-empty problem, and return the launch error.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_epilogue(const EpilogueArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);

@@ -148,6 +148,23 @@ def prefill_inputs(w: Workload, seed: Optional[int] = None, **override):
                 scale=w.dk ** -0.5, chunk=w.chunk, workload=w)
 
 
+def mixer_inputs(w: Workload, lead, seed: Optional[int] = None, tiers: int = 4, **override):
+    """Synthetic weights and gate stream for the mixer's steps after the readout:
+    ``aug`` fp32 [H, dk] ~ N(0, 0.5) (the self-augmentation balance), ``norm_w``
+    fp32 [H, dv] ~ 1 + N(0, 0.1) with the heads split into ``tiers`` equal runs
+    that share one row (the head RMSNorm per decay tier), ``z`` [*lead, H, dv]
+    ~ N(0, 1) in the I/O dtype (the output gate stream), ``eps`` 1e-6."""
+    if override:
+        w = dataclasses.replace(w, **override)
+    gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 7)
+    aug = _normal(gen, (w.H, w.dk), 0.5)
+    per = -(-w.H // tiers)
+    rows = 1.0 + _normal(gen, (tiers, w.dv), 0.1)
+    norm_w = rows[torch.arange(w.H) // per].contiguous()
+    z = _normal(gen, (*lead, w.H, w.dv)).to(w.torch_dtype).contiguous()
+    return dict(aug=aug, norm_w=norm_w, eps=1e-6, z=z)
+
+
 def decode_inputs(w: Workload, seed: Optional[int] = None, **override):
     """Decode inputs: ``state [N, H, dk, dv]`` fp32 and per-step lists of
     ``q, k [N, H, dk]``, ``v [N, H, dv]`` (I/O dtype) and ``g`` ([N, H] or

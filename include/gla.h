@@ -169,6 +169,51 @@ gla_status gla_decode_step_slots(const void *q, const void *k, const void *v, co
                                  gla_stream_t stream, unsigned flags);
 
 /*
+ * gla_mixer_epilogue -- the mixer's steps after the readout, in place over a
+ * finished output (for instance the out of gla_chunk_fwd).
+ *
+ * Source: "i14 Laplace 3B" page, paragraph "GLA mixer": a self-augmentation
+ * adds the value gated by the query dotted with a learned per-key-channel
+ * rescaling of the key; the per-head outputs pass a head RMSNorm (one weight
+ * per decay tier); the result is gated by SiLU of the gate stream.  Per token
+ * and head, each step skipped when its pointer is null:
+ *     o += sigmoid(sum_i q_i aug[h][i] k_i) * v
+ *     o  = o / sqrt(mean_j o_j^2 + eps) * norm_w[h][j]
+ *     o *= z / (1 + exp(-z))
+ *
+ * Arguments
+ *   out          [rows, H, dv] bf16 (fp32 with GLA_FLAG_FP32_OUT), in place
+ *   q, k         [rows, H, dk], v [rows, H, dv]: bf16 (fp32 with
+ *                GLA_FLAG_FP32_IO); needed only with aug
+ *   aug          fp32 [H, dk] or NULL
+ *   norm_w       fp32 [H, dv] or NULL (a tier's heads carry equal rows)
+ *   eps          >= 0, added to the mean square
+ *   z            [rows, H, dv], q's dtype, or NULL
+ *   rows, H      token rows and heads (>= 0); dk, dv as gla_chunk_fwd
+ *   flags        GLA_FLAG_FP32_IO, GLA_FLAG_FP32_OUT only
+ * Alignment: element alignment.  out must not overlap any input.
+ */
+gla_status gla_mixer_epilogue(void *out, const void *q, const void *k, const void *v,
+                              const float *aug, const float *norm_w, float eps, const void *z,
+                              int rows, int H, int dk, int dv, gla_stream_t stream,
+                              unsigned flags);
+
+/*
+ * gla_decode_step_mixer -- the decode step with the mixer's steps after the
+ * readout fused into it (one CTA owns a head's whole output row).
+ *
+ * Arguments: as gla_decode_step_slots (slots NULL: state is [N, H, dk, dv]
+ * and num_slots must be 0), plus aug, norm_w, eps and z as for
+ * gla_mixer_epilogue (z [N, H, dv] in q's dtype).  Each step is skipped when
+ * its pointer is NULL.
+ */
+gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, const float *g,
+                                 float scale, float *state, int num_slots,
+                                 const int32_t *slots, void *out, int N, int H, int dk, int dv,
+                                 const float *aug, const float *norm_w, float eps,
+                                 const void *z, gla_stream_t stream, unsigned flags);
+
+/*
  * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call
  * with these head sizes, chunk size and flags: "tensor_core" (a tcgen05
  * kernel: per-head or per-key-channel gate), "cuda_core" (the fp32 CUDA-core

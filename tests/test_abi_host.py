@@ -157,8 +157,49 @@ def test_decode_step_empty_is_no_op(L):
 def test_ctypes_signatures_match_header(L):
     """The binding's argument counts equal the header's parameter counts."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots", "gla_status_sync",
+    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots",
+                 "gla_decode_step_mixer", "gla_mixer_epilogue", "gla_status_sync",
                  "gla_status_string"):
         m = re.search(name + r"\s*\(([^)]*)\)", text)
         nparams = len([p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"])
         assert len(getattr(L, name).argtypes) == nparams, name
+
+
+def epilogue(out=FAKE[5], q=FAKE[0], k=FAKE[1], v=FAKE[2], aug=FAKE[7], norm_w=FAKE[8], eps=1e-6,
+             z=FAKE[9], rows=16, H=4, dk=128, dv=128, flags=0):
+    return _binding.gla_mixer_epilogue(out, q, k, v, aug, norm_w, eps, z, rows, H, dk, dv, 0,
+                                       flags)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=E.GLA_FLAG_VECTOR_GATE), E.GLA_ERR_INVALID_ARG),   # not an epilogue flag
+    (dict(eps=-1.0), E.GLA_ERR_INVALID_ARG),
+    (dict(eps=float("inf")), E.GLA_ERR_INVALID_ARG),
+    (dict(rows=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(out=0), E.GLA_ERR_INVALID_ARG),
+    (dict(q=0), E.GLA_ERR_INVALID_ARG),              # aug needs q, k, v
+    (dict(dk=80), E.GLA_ERR_UNSUPPORTED),
+    (dict(out=FAKE[5] + 1), E.GLA_ERR_MISALIGNED),
+    (dict(aug=FAKE[7] + 2), E.GLA_ERR_MISALIGNED),
+    (dict(z=FAKE[5] + 64), E.GLA_ERR_INVALID_ARG),   # z inside out
+])
+def test_mixer_epilogue_rejects_before_launch(L, kw, status):
+    assert epilogue(**kw) == status
+
+
+def test_mixer_epilogue_trivial_calls_are_no_ops(L):
+    assert epilogue(rows=0) == E.GLA_OK
+    assert epilogue(H=0) == E.GLA_OK
+    assert epilogue(aug=0, norm_w=0, z=0) == E.GLA_OK            # nothing to apply
+    assert epilogue(aug=0, norm_w=0, z=0, q=0, k=0, v=0) == E.GLA_OK
+
+
+def test_decode_mixer_rejects_before_launch(L):
+    call = lambda **kw: _binding.gla_decode_step_mixer(
+        *[kw.get(n, d) for n, d in (("q", FAKE[0]), ("k", FAKE[1]), ("v", FAKE[2]),
+                                     ("g", FAKE[3]))], 0.1, FAKE[4], kw.get("num_slots", 0),
+        kw.get("slots", 0), FAKE[5], 8, 4, 128, 128, FAKE[7], FAKE[8], kw.get("eps", 1e-6),
+        FAKE[9], 0, 0)
+    assert call(num_slots=3) == E.GLA_ERR_INVALID_ARG      # a pool size without slots
+    assert call(eps=-0.5) == E.GLA_ERR_INVALID_ARG
+    assert call(q=0) == E.GLA_ERR_INVALID_ARG

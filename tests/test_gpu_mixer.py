@@ -1,0 +1,150 @@
+"""The mixer's steps after the readout (self-augmentation, head RMSNorm, SiLU
+output gate) on the GPU, against the fp64 oracle: after every prefill kernel
+(gla_mixer_epilogue over its output) and fused into the decode step.
+
+The check is split in two.  The readout o itself must match the oracle within
+the output tolerance (as everywhere); the epilogue, applied by the GPU to that
+o, must match the oracle's epilogue applied to the same o (the GPU's fp32
+readout, widened) within 1e-5 of the result's RMS -- fp32 arithmetic against
+fp64.  A direct comparison of the two composites would charge the epilogue
+with the readout's rounding, magnified elementwise by the gate (|silu(z)| up
+to ~4 against an RMS of ~0.8) and row by row by the normalisation."""
+import numpy as np
+import pytest
+import torch
+
+import gla_inputs
+import oracle
+from parity import TOL_STATE, cuda, out_tol, rel_max, to_np
+
+pytestmark = pytest.mark.gpu
+
+STEPS = {"aug": ("aug",), "norm": ("norm_w", "eps"), "gate": ("z",),
+         "all": ("aug", "norm_w", "eps", "z")}
+
+
+def _gla():
+    import gated_linear_attention_gla_gb300 as gla
+    return gla
+
+
+def _pick(m, which):
+    return {k: m[k] for k in STEPS[which]}
+
+
+def _ref_epilogue(o_ref, x, m, which, q=None, k=None, v=None):
+    q = x["q"] if q is None else q
+    k = x["k"] if k is None else k
+    v = x["v"] if v is None else v
+    return oracle.mixer_epilogue(o_ref, q, k, v, aug=m["aug"] if "aug" in STEPS[which] else None,
+                                 norm_w=m["norm_w"] if "norm_w" in STEPS[which] else None,
+                                 eps=m["eps"], z=m["z"] if "z" in STEPS[which] else None)
+
+
+@pytest.mark.parametrize("which", sorted(STEPS))
+@pytest.mark.parametrize("case", ["tc_scalar", "tc_vector", "laplace", "simt_fp32"])
+def test_prefill_with_mixer_epilogue(cuda_ok, case, which):
+    gla = _gla()
+    if case == "tc_scalar":
+        w, kw = gla_inputs.WORKLOADS["prefill"], dict(B=2, T=300, H=4)
+    elif case == "tc_vector":
+        w, kw = gla_inputs.WORKLOADS["vector"], dict(B=2, T=300, H=4, init_std=0.02)
+    elif case == "laplace":
+        w, kw = gla_inputs.WORKLOADS["laplace"], dict(B=2, T=300, H=16)
+    else:
+        w, kw = gla_inputs.WORKLOADS["tiny"], dict(B=2, T=150, H=2, chunk=64, init_std=0.1)
+    x = gla_inputs.prefill_inputs(w, seed=31, **kw)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=31, **{k: kw[k] for k in ("H",)})
+    mix = {k: cuda(v) if torch.is_tensor(v) else v for k, v in _pick(m, which).items()}
+    args = (cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]))
+    kw = dict(scale=x["scale"], init_state=cuda(x["init_state"]), chunk=x["chunk"],
+              out_dtype=torch.float32)
+    o, _ = gla.chunk_fwd(*args, **kw)
+    y, fin = gla.chunk_fwd(*args, mixer=mix, **kw)
+    gla.status_sync()
+    o_ref, s_ref = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                    init_state=x["init_state"])
+    tol = out_tol(x["q"].dtype)
+    assert rel_max(to_np(o), o_ref) <= tol
+    assert rel_max(to_np(fin), s_ref) <= (TOL_STATE if x["q"].dtype == torch.bfloat16 else 1e-5)
+    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, which))
+    assert e <= 1e-5, f"epilogue error {e:.3e}"
+
+
+def test_epilogue_entry_point_matches_oracle_on_a_given_output(cuda_ok):
+    """gla_mixer_epilogue alone, over an fp32 output that is the oracle's own
+    readout: only the epilogue's arithmetic is measured (fp32 vs fp64)."""
+    gla = _gla()
+    from gated_linear_attention_gla_gb300 import _binding
+    w = gla_inputs.WORKLOADS["laplace"]
+    x = gla_inputs.prefill_inputs(w, seed=5, B=1, T=64, H=16)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=5)
+    o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                init_state=x["init_state"])
+    out = torch.tensor(o_ref, dtype=torch.float32).cuda().contiguous()
+    args = {n: cuda(x[n]) for n in ("q", "k", "v")}
+    mix = {n: cuda(m[n]) for n in ("aug", "norm_w", "z")}
+    rc = _binding.gla_mixer_epilogue(out.data_ptr(), args["q"].data_ptr(), args["k"].data_ptr(),
+                                     args["v"].data_ptr(), mix["aug"].data_ptr(),
+                                     mix["norm_w"].data_ptr(), m["eps"], mix["z"].data_ptr(),
+                                     64, 16, 96, 192, torch.cuda.current_stream().cuda_stream,
+                                     _binding.GLA_FLAG_FP32_OUT)
+    assert rc == 0
+    gla.status_sync()
+    y_ref = _ref_epilogue(o_ref, x, m, "all")
+    assert rel_max(to_np(out), y_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("which", sorted(STEPS))
+@pytest.mark.parametrize("dk,dv,gate", [(128, 128, "scalar"), (96, 192, "scalar"),
+                                        (128, 128, "vector")])
+def test_decode_step_with_fused_mixer(cuda_ok, dk, dv, gate, which):
+    gla = _gla()
+    w = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(w, steps=2, N=6, H=4, dk=dk, dv=dv, gate=gate)
+    m = gla_inputs.mixer_inputs(w, (6,), seed=3, H=4, dk=dk, dv=dv)
+    mix = {k: cuda(v) if torch.is_tensor(v) else v for k, v in _pick(m, which).items()}
+    S = cuda(d["state"]).clone()
+    S_ref = d["state"].double().numpy()
+    for t in range(2):
+        args = [cuda(d[n][t]) for n in ("q", "k", "v", "g")]
+        S_plain = S.clone()
+        o = gla.decode_step(*args, S_plain, scale=d["scale"], out_dtype=torch.float32)
+        y = gla.decode_step(*args, S, scale=d["scale"], out_dtype=torch.float32, mixer=mix)
+        gla.status_sync()
+        assert torch.equal(S, S_plain), t  # the epilogue leaves the state step alone
+        o_ref, S_ref = oracle.decode_step(d["q"][t], d["k"][t], d["v"][t], d["g"][t],
+                                          d["scale"], S_ref)
+        assert rel_max(to_np(o), o_ref) <= out_tol(torch.bfloat16), t
+        y_ref = _ref_epilogue(to_np(o), None, m, which, d["q"][t], d["k"][t], d["v"][t])
+        e = rel_max(to_np(y), y_ref)
+        assert e <= 1e-5, f"step {t}: epilogue error {e:.3e}"
+    assert rel_max(to_np(S), S_ref) <= 1e-5
+
+
+def test_decode_mixer_on_slot_pages(cuda_ok):
+    """The fused epilogue with slot-indexed pages and a padding row."""
+    gla = _gla()
+    w = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(w, steps=1, N=3, H=2)
+    m = gla_inputs.mixer_inputs(w, (3,), seed=4, H=2)
+    mix = {k: cuda(v) if torch.is_tensor(v) else v for k, v in m.items()}
+    pool = torch.zeros(5, 2, w.dk, w.dv)
+    pool[[4, 1]] = d["state"][[0, 2]]
+    pool_gpu = cuda(pool).contiguous()
+    slots = cuda(torch.tensor([4, -1, 1], dtype=torch.int32))
+    args = [cuda(d[n][0]) for n in ("q", "k", "v", "g")]
+    o = torch.zeros(3, 2, w.dv, device="cuda")
+    gla.decode_step(*args, pool_gpu.clone(), scale=d["scale"], out=o, slots=slots)
+    out = torch.zeros(3, 2, w.dv, device="cuda")
+    gla.decode_step(*args, pool_gpu, scale=d["scale"], out=out, slots=slots, mixer=mix)
+    gla.status_sync()
+    live = [0, 2]
+    o_ref, _ = oracle.decode_step(d["q"][0][live], d["k"][0][live], d["v"][0][live],
+                                  d["g"][0][live], d["scale"], d["state"][live])
+    assert rel_max(to_np(o[live]), o_ref) <= out_tol(torch.bfloat16)
+    y_ref = oracle.mixer_epilogue(to_np(o[live]), d["q"][0][live], d["k"][0][live],
+                                  d["v"][0][live], aug=m["aug"], norm_w=m["norm_w"], eps=m["eps"],
+                                  z=m["z"][live])
+    assert rel_max(to_np(out[live]), y_ref) <= 1e-5
+    assert (out[1] == 0).all()
