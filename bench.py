@@ -337,6 +337,59 @@ def time_decode_graphs(gla, dev, width=64, steps=200):
             "algorithmic_bytes_per_step": nbytes, "graph_gbs": nbytes / graph / 1e3}
 
 
+def time_mixer(gla, dev, hbm, reps=20, warmup=3):
+    """The mixer's steps after the readout: the prefill workload with and without
+    the epilogue pass (gla_mixer_epilogue over its output), and the decode
+    workload's step with and without the fused epilogue; each timed alone."""
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+    res = {}
+    w = gla_inputs.WORKLOADS["prefill"]
+    x = gla_inputs.prefill_inputs(w)
+    q, k, v, g, s0 = (x[n].to(dev) for n in ("q", "k", "v", "g", "init_state"))
+    m = gla_inputs.mixer_inputs(w, q.shape[:-2])
+    mix = {n: (t.to(dev) if torch.is_tensor(t) else t) for n, t in m.items()}
+    out = torch.empty(v.shape, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty_like(s0)
+    kw = dict(scale=x["scale"], init_state=s0, chunk=w.chunk, out=out, final_state=fin)
+    plain = timed(lambda: gla.chunk_fwd(q, k, v, g, **kw))
+    fused = timed(lambda: gla.chunk_fwd(q, k, v, g, mixer=mix, **kw))
+    units = w.B * w.T * w.H
+    # epilogue bytes: read o, q, k, v, z (bf16), the weights; write o
+    epi_bytes = units * 2 * (w.dv + 2 * w.dk + w.dv + w.dv + w.dv)
+    res["prefill"] = {"workload": f"prefill B={w.B} T={w.T} H={w.H} d={w.dk}, epilogue pass "
+                                  f"over the bf16 output",
+                      "ms_plain": plain, "ms_with_epilogue": fused,
+                      "epilogue_ms": fused - plain, "epilogue_bytes": epi_bytes,
+                      "epilogue_frac_of_hbm": epi_bytes / ((fused - plain) / 1e3) / 1e9 / hbm}
+    wd = gla_inputs.WORKLOADS["decode"]
+    d = gla_inputs.decode_inputs(wd, steps=1)
+    dq, dk_, dv_, dg = (d[n][0].to(dev) for n in ("q", "k", "v", "g"))
+    st = d["state"].to(dev)
+    md = gla_inputs.mixer_inputs(wd, (wd.N,))
+    dmix = {n: (t.to(dev) if torch.is_tensor(t) else t) for n, t in md.items()}
+    dout = torch.empty(wd.N, wd.H, wd.dv, dtype=torch.bfloat16, device=dev)
+    p_ms = timed(lambda: gla.decode_step(dq, dk_, dv_, dg, st, scale=d["scale"], out=dout))
+    f_ms = timed(lambda: gla.decode_step(dq, dk_, dv_, dg, st, scale=d["scale"], out=dout,
+                                         mixer=dmix))
+    res["decode"] = {"workload": f"decode step N={wd.N} H={wd.H} d={wd.dk}, fused epilogue",
+                     "ms_plain": p_ms, "ms_fused": f_ms,
+                     "fused_overhead": f_ms / p_ms - 1.0}
+    gla.status_sync()
+    return res
+
+
 def run_gla(args, world, rank, local):
     import gated_linear_attention_gla_gb300 as gla
     from gated_linear_attention_gla_gb300 import build as glabuild
@@ -534,6 +587,7 @@ def run_gla(args, world, rank, local):
         # timed after the step (outside ms_per_step and gpu_launches)
         line["prefill_workloads"] = time_side_workloads(gla, dev, hbm, peak_kind)
         line["decode_graphs"] = [time_decode_graphs(gla, dev, width=n) for n in (8, 64)]
+        line["mixer"] = time_mixer(gla, dev, hbm)
     if world == 1 and not args.no_cpu_baseline:
         pre_cpu, dec_cpu = cpu_baseline(args.cpu_budget)
         line["cpu_baseline"] = pre_cpu
