@@ -29,6 +29,7 @@ recurrent     token-by-token recurrence in C (the definition; OpenMP over
               (sequence, head))
 chunked       the chunked form in C, any chunk size
 decode_step   one recurrent step over N independent states, in C
+backward      the gradient of the recurrence (reverse mode, token by token), in C
 bruteforce    the unrolled recurrence as one O(T^2) sum per token, numpy, tiny
               inputs only
 decay_schedule  the page's fixed geometric per-head decay (paragraph "Decay
@@ -93,6 +94,11 @@ def _load():
                 _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_double, _dp, _dp,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.gla_oracle_decode_step_f64.restype = ctypes.c_int
+            lib.gla_oracle_backward_f64.argtypes = [
+                _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_double, _dp, _dp, _dp, _dp, _dp,
+                _dp, _dp, _dp, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int]
+            lib.gla_oracle_backward_f64.restype = ctypes.c_int
             lib.gla_oracle_max_threads.argtypes = []
             lib.gla_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -204,6 +210,46 @@ def decode_step(q, k, v, g, scale, state, nthreads=0):
     if rc != 0:
         raise ValueError("oracle decode_step rejected its arguments")
     return out, S
+
+
+def backward(q, k, v, g, scale, d_out, init_state=None, d_final=None, cu_seqlens=None,
+             nthreads=0):
+    """The gradient of ``recurrent`` by reverse mode, one token at a time (in C).
+
+    For a loss with ``dL/d out = d_out`` and ``dL/d final_state = d_final``
+    (zero when None), returns ``(dq, dk, dv, dg, d_init)`` in fp64, shaped like
+    q, k, v, g and the state ``[B, H, dk, dv]``.  The reverse sweep carries
+    ``Sbar_t = dL/dS_t`` backwards:
+    ``Sbar_t = scale q_t^T do_t + diag(exp g_{t+1}) Sbar_{t+1}``, and
+    ``dq_t = scale S_t do_t^T``, ``dk_t = Sbar_t v_t^T``, ``dv_t = k_t Sbar_t``,
+    ``dg_t[i] = exp(g_t[i]) sum_j S_{t-1}[i, j] Sbar_t[i, j]`` (summed over i
+    for the per-head gate), ``d_init = diag(exp g_0) Sbar_0``.
+    """
+    q, k, v, g, do = _f64(q), _f64(k), _f64(v), _f64(g), _f64(d_out)
+    init, dfin = _f64(init_state), _f64(d_final)
+    cu = None
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int32))
+    B, T, H, dk, dv, rows, vg = _shapes(q, v, g, cu)
+    if do.shape != v.shape:
+        raise ValueError("d_out must have the shape of v")
+    st = (B, H, dk, dv)
+    for name, x in (("init_state", init), ("d_final", dfin)):
+        if x is not None and x.shape != st:
+            raise ValueError(f"{name} must be {st}")
+    dq, dkk = np.zeros(q.shape), np.zeros(k.shape)
+    dvv, dg = np.zeros(v.shape), np.zeros(g.shape)
+    d_init = np.zeros(st)
+    cu_p = None if cu is None else cu.ctypes.data_as(_ip)
+    rc = _load().gla_oracle_backward_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), vg, float(scale), _ptr(init), _ptr(do), _ptr(dfin),
+        _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(d_init), cu_p, B, H, T, dk, dv,
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle backward rejected its arguments")
+    return dq, dkk, dvv, dg, d_init
 
 
 def bruteforce(q, k, v, g, scale, init_state=None):

@@ -37,6 +37,7 @@
  *                             plus what the carried-in state contributes,
  *                             then one state step with the chunk's total decay
  *   gla_oracle_decode_step_f64 one recurrent step for N independent states
+ *   gla_oracle_backward_f64   the gradient of the recurrence (reverse mode)
  *
  * Return value: 0 on success, -1 on a bad argument (nothing is written).
  */
@@ -316,6 +317,158 @@ int gla_oracle_decode_step_f64(const double *q, const double *k, const double *v
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The gradient of the recurrence (reverse mode, one token at a time).       */
+/*                                                                           */
+/* For a loss L with dL/do_t = d_out[t] and dL/dS_final = d_final (zero when */
+/* absent), let Sbar_t = dL/dS_t, the gradient reaching the state after      */
+/* token t through every later readout and step.  Going backwards:           */
+/*   Sbar_t      = scale * q_t^T do_t + diag(exp g_{t+1}) Sbar_{t+1}          */
+/*                 (Sbar at the last token starts from d_final)              */
+/*   dq_t        = scale * S_t do_t^T           (forward sweep)              */
+/*   dk_t        = Sbar_t v_t^T                                              */
+/*   dv_t        = k_t Sbar_t                                                */
+/*   dg_t[i]     = exp(g_t[i]) * sum_j S_{t-1}[i][j] * Sbar_t[i][j]          */
+/*                 (summed over i for the per-head gate)                     */
+/*   d_init      = diag(exp g_0) Sbar_0                                      */
+/* S_{t-1} is needed in reverse order: the forward sweep keeps the state at  */
+/* the start of every BWD_SEGMENT tokens, and the reverse sweep recomputes   */
+/* one segment's states from its checkpoint before walking it backwards.     */
+/* No gate clamping: this is the exact gradient of the recurrence above.     */
+/* ------------------------------------------------------------------------- */
+#define BWD_SEGMENT 64
+
+int gla_oracle_backward_f64(const double *q, const double *k, const double *v,
+                            const double *g, int vector_gate, double scale,
+                            const double *init_state, const double *d_out,
+                            const double *d_final, double *dq, double *dk_out,
+                            double *dv_out, double *dg, double *d_init,
+                            const int32_t *cu_seqlens, int B, int H, int T, int dk, int dv,
+                            int nthreads)
+{
+    if (check_args(q, k, v, g, d_out, cu_seqlens, B, H, T, dk, dv) || !dq || !dk_out ||
+        !dv_out || !dg)
+        return -1;
+    set_threads(nthreads);
+    const long pairs = (long)B * H;
+    const size_t SD = (size_t)dk * dv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (long p = 0; p < pairs; ++p) {
+        const int s = (int)(p / H), h = (int)(p % H);
+        long start, len;
+        if (seq_bounds(cu_seqlens, s, T, &start, &len)) {
+            failed |= 1;
+            continue;
+        }
+        const long nseg = (len + BWD_SEGMENT - 1) / BWD_SEGMENT;
+        /* ckpt[m] = state before token m * BWD_SEGMENT; seg[r] = S_{t0 + r - 1} */
+        double *ckpt = (double *)malloc(sizeof(double) * SD * (size_t)(nseg + 1));
+        double *seg = (double *)malloc(sizeof(double) * SD * (BWD_SEGMENT + 1));
+        double *Sbar = (double *)malloc(sizeof(double) * SD);
+        double *S = (double *)malloc(sizeof(double) * SD);
+        if (!ckpt || !seg || !Sbar || !S) {
+            free(ckpt); free(seg); free(Sbar); free(S);
+            failed |= 1;
+            continue;
+        }
+        if (init_state)
+            memcpy(S, init_state + (size_t)p * SD, sizeof(double) * SD);
+        else
+            memset(S, 0, sizeof(double) * SD);
+
+        /* forward sweep: checkpoints and dq_t = scale * S_t do_t^T */
+        for (long t = 0; t < len; ++t) {
+            if (t % BWD_SEGMENT == 0)
+                memcpy(ckpt + SD * (size_t)(t / BWD_SEGMENT), S, sizeof(double) * SD);
+            const long row = start + t;
+            const double *kt = k + ((size_t)row * H + h) * dk;
+            const double *vt = v + ((size_t)row * H + h) * dv;
+            const double *dot = d_out + ((size_t)row * H + h) * dv;
+            double *dqt = dq + ((size_t)row * H + h) * dk;
+            for (int i = 0; i < dk; ++i) {
+                const double a = decay_factor(g, vector_gate, row, H, h, dk, i);
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    S[(size_t)i * dv + j] = a * S[(size_t)i * dv + j] + kt[i] * vt[j];
+                    acc += S[(size_t)i * dv + j] * dot[j];
+                }
+                dqt[i] = scale * acc;
+            }
+        }
+
+        /* reverse sweep */
+        if (d_final)
+            memcpy(Sbar, d_final + (size_t)p * SD, sizeof(double) * SD);
+        else
+            memset(Sbar, 0, sizeof(double) * SD);
+        for (long m = nseg - 1; m >= 0; --m) {
+            const long t0 = m * BWD_SEGMENT;
+            const long t1 = (t0 + BWD_SEGMENT < len) ? t0 + BWD_SEGMENT : len;
+            /* seg[0] = S_{t0-1} (the checkpoint), seg[r] = S_{t0+r-1} */
+            memcpy(seg, ckpt + SD * (size_t)m, sizeof(double) * SD);
+            for (long t = t0; t < t1 - 1; ++t) {
+                const long row = start + t;
+                const double *kt = k + ((size_t)row * H + h) * dk;
+                const double *vt = v + ((size_t)row * H + h) * dv;
+                const double *prev = seg + SD * (size_t)(t - t0);
+                double *next = seg + SD * (size_t)(t - t0 + 1);
+                for (int i = 0; i < dk; ++i) {
+                    const double a = decay_factor(g, vector_gate, row, H, h, dk, i);
+                    for (int j = 0; j < dv; ++j)
+                        next[(size_t)i * dv + j] = a * prev[(size_t)i * dv + j] + kt[i] * vt[j];
+                }
+            }
+            for (long t = t1 - 1; t >= t0; --t) {
+                const long row = start + t;
+                const double *qt = q + ((size_t)row * H + h) * dk;
+                const double *kt = k + ((size_t)row * H + h) * dk;
+                const double *vt = v + ((size_t)row * H + h) * dv;
+                const double *dot = d_out + ((size_t)row * H + h) * dv;
+                const double *Sprev = seg + SD * (size_t)(t - t0);   /* S_{t-1} */
+                double *dkt = dk_out + ((size_t)row * H + h) * dk;
+                double *dvt = dv_out + ((size_t)row * H + h) * dv;
+                /* Sbar <- Sbar_t: add this token's readout */
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j)
+                        Sbar[(size_t)i * dv + j] += scale * qt[i] * dot[j];
+                for (int i = 0; i < dk; ++i) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j)
+                        acc += Sbar[(size_t)i * dv + j] * vt[j];
+                    dkt[i] = acc;
+                }
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; ++i)
+                        acc += kt[i] * Sbar[(size_t)i * dv + j];
+                    dvt[j] = acc;
+                }
+                double gsum = 0.0;
+                for (int i = 0; i < dk; ++i) {
+                    const double a = decay_factor(g, vector_gate, row, H, h, dk, i);
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j)
+                        acc += Sprev[(size_t)i * dv + j] * Sbar[(size_t)i * dv + j];
+                    if (vector_gate)
+                        dg[((size_t)row * H + h) * dk + i] = a * acc;
+                    else
+                        gsum += a * acc;
+                    /* Sbar <- diag(exp g_t) Sbar: the gradient reaching S_{t-1} */
+                    for (int j = 0; j < dv; ++j)
+                        Sbar[(size_t)i * dv + j] *= a;
+                }
+                if (!vector_gate)
+                    dg[(size_t)row * H + h] = gsum;
+            }
+        }
+        if (d_init)
+            memcpy(d_init + (size_t)p * SD, Sbar, sizeof(double) * SD);
+        free(ckpt); free(seg); free(Sbar); free(S);
+    }
+    return failed ? -1 : 0;
 }
 
 /* Number of threads OpenMP would use (1 without OpenMP). */
