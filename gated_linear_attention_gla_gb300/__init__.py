@@ -6,6 +6,7 @@ library's CUDA kernels, and a missing library is an error, never a fallback.
 
     out, final = chunk_fwd(q, k, v, g, init_state=S0)          # prefill
     out = decode_step(q, k, v, g, state)                         # one token, in place
+    dq, dk, dv, dg, d_init = chunk_bwd(q, k, v, g, d_out, init_state=S0)   # training
 
 The recurrence (the "i14 Laplace 3B on AWS Trainium2" page, paragraph "GLA
 mixer"): ``S_t = diag(exp g_t) S_{t-1} + k_t^T v_t``, ``o_t = scale q_t S_t``.
@@ -20,7 +21,7 @@ from . import _binding
 from ._binding import (GLA_FLAG_FP32_IO, GLA_FLAG_FP32_OUT, GLA_FLAG_VECTOR_GATE,  # noqa: F401
                        GlaError, lib, status_string, version)
 
-__all__ = ["chunk_fwd", "decode_step", "status_sync", "GlaError", "lib", "version",
+__all__ = ["chunk_fwd", "chunk_bwd", "decode_step", "status_sync", "GlaError", "lib", "version",
            "GLA_FLAG_FP32_IO", "GLA_FLAG_FP32_OUT", "GLA_FLAG_VECTOR_GATE"]
 
 
@@ -141,6 +142,56 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
         if rc != 0:
             raise GlaError(rc, "gla_mixer_epilogue")
     return out, final_state
+
+
+def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
+              d_final_state=None, cu_seqlens=None, grad_dtype=None, need_dg: bool = True,
+              need_d_init: bool = True, stream=None):
+    """Gradient of ``chunk_fwd`` (gla_chunk_bwd); returns ``(dq, dk, dv, dg, d_init)``.
+
+    ``q, k, v, g, scale, init_state, cu_seqlens`` as given to ``chunk_fwd``;
+    ``d_out`` (q's dtype, v's shape) and ``d_final_state`` (fp32 state, or
+    None for zero) are the gradients of the loss with respect to the forward's
+    outputs.  ``dq, dk, dv`` come in q's dtype, or fp32 with
+    ``grad_dtype=torch.float32`` for bf16 inputs; ``dg`` (fp32, g's shape) and
+    ``d_init`` (fp32 state) are None when not requested.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("d_out", d_out)):
+        _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _check(k.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype,
+           "k must match q; v must have q's dtype")
+    _check(d_out.shape == v.shape and d_out.dtype == q.dtype, "d_out must match v")
+    H, dk, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    _check(v.shape[:-1] == q.shape[:-1], "v must be [..., H, dv] with q's leading dims")
+    if cu_seqlens is not None:
+        _check(cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32,
+               "cu_seqlens must be int32 on the GPU")
+        B = cu_seqlens.numel() - 1
+        T = q.numel() // (H * dk)
+    else:
+        _check(q.dim() == 4, "dense inputs are [B, T, H, d]")
+        B, T = q.shape[0], q.shape[1]
+    grad_dtype = _out_dtype(q, None, grad_dtype)
+    flags = _io_flags(q, g, q.shape[:-1], q.shape, grad_dtype)
+    if scale is None:
+        scale = dk ** -0.5
+    st = (B, H, dk, dv)
+    for name, t in (("init_state", init_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _check(t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and
+                   tuple(t.shape) == st, f"{name} must be contiguous fp32 {list(st)}")
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk_ = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv_ = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    dg = torch.empty(g.shape, dtype=torch.float32, device=q.device) if need_dg else None
+    d_init = torch.empty(st, dtype=torch.float32, device=q.device) if need_d_init else None
+    rc = _binding.gla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state),
+                                _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk_),
+                                _ptr(dv_), _ptr(dg), _ptr(d_init), _ptr(cu_seqlens), B, H, T,
+                                dk, dv, _stream(stream), flags)
+    if rc != 0:
+        raise GlaError(rc, "gla_chunk_bwd")
+    return dq, dk_, dv_, dg, d_init
 
 
 def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stream=None,

@@ -172,6 +172,68 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   return cuda_status(err);
 }
 
+gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                         float scale, const float* init_state, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk_out, void* dv_out,
+                         float* dg, float* d_init_state, const int32_t* cu_seqlens, int B,
+                         int H, int T, int dk, int dv, gla_stream_t stream, unsigned flags) {
+  if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
+    return GLA_ERR_INVALID_ARG;
+  if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
+  const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
+  const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
+  const bool vec = (flags & GLA_FLAG_VECTOR_GATE) != 0;
+  if (B == 0 || H == 0) return GLA_OK;
+
+  const long long rows = cu_seqlens ? (long long)T : (long long)B * T;
+  const long long esz = fp32 ? 4 : 2, osz = f32out ? 4 : 2;
+  const long long qk_elems = rows * H * dk, v_elems = rows * H * dv;
+  const long long st_elems = (long long)B * H * dk * dv;
+  if (qk_elems > kMaxElems || v_elems > kMaxElems || st_elems > kMaxElems)
+    return GLA_ERR_INVALID_ARG;
+  if ((long long)B * H * (dk / 32) > 0x7fffffffll) return GLA_ERR_INVALID_ARG;
+  if (rows > 0 && (!q || !k || !v || !g || !d_out || !dq || !dk_out || !dv_out))
+    return GLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(d_out, 16) ||
+      !aligned(dq, 16) || !aligned(dk_out, 16) || !aligned(dv_out, 16) ||
+      !aligned(init_state, 16) || !aligned(d_final_state, 16) || !aligned(d_init_state, 16) ||
+      !aligned(dg, 16) || !aligned(g, vec ? 16 : 4) || !aligned(cu_seqlens, 4))
+    return GLA_ERR_MISALIGNED;
+  // every output is disjoint from every input and from the other outputs
+  const size_t qk_b = (size_t)(qk_elems * esz), v_b = (size_t)(v_elems * esz);
+  const size_t dqk_b = (size_t)(qk_elems * osz), dv_b = (size_t)(v_elems * osz);
+  const size_t g_b = (size_t)(rows * H * (vec ? dk : 1) * 4);
+  const size_t st_b = (size_t)(st_elems * 4);
+  const void* in_p[] = {q, k, v, g, d_out, init_state, d_final_state, cu_seqlens};
+  const size_t in_b[] = {qk_b, qk_b, v_b, g_b, v_b, st_b, st_b,
+                         cu_seqlens ? (size_t)(B + 1) * 4 : 0};
+  const void* out_p[] = {dq, dk_out, dv_out, dg, d_init_state};
+  const size_t out_b[] = {dqk_b, dqk_b, dv_b, g_b, st_b};
+  for (int o = 0; o < 5; ++o) {
+    for (int i = 0; i < 8; ++i)
+      if (overlap(out_p[o], out_b[o], in_p[i], in_b[i])) return GLA_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 5; ++o2)
+      if (overlap(out_p[o], out_b[o], out_p[o2], out_b[o2])) return GLA_ERR_INVALID_ARG;
+  }
+  if (rows == 0 && d_init_state == nullptr) return GLA_OK;
+
+  cudaError_t err;
+  unsigned* status = status_word(&err);
+  if (!status) return cuda_status(err);
+  gla::ChunkBwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale; a.init_state = init_state;
+  a.d_out = d_out; a.d_final = d_final_state; a.dq = dq; a.dk = dk_out; a.dv = dv_out;
+  a.dg = rows > 0 ? dg : nullptr; a.d_init = d_init_state; a.cu_seqlens = cu_seqlens;
+  a.B = B; a.H = H; a.T = T; a.dk_size = dk; a.dv_size = dv;
+  a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec; a.status = status;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (vec)
+    err = fp32 ? gla::launch_chunk_bwd_chan_f32(a, s) : gla::launch_chunk_bwd_chan_bf16(a, s);
+  else
+    err = fp32 ? gla::launch_chunk_bwd_head_f32(a, s) : gla::launch_chunk_bwd_head_bf16(a, s);
+  return cuda_status(err);
+}
+
 namespace {
 
 // The decode step over N sequences whose state pages are either the N pages of

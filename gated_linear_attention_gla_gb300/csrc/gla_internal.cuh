@@ -73,6 +73,29 @@ struct EpilogueArgs {
   bool fp32_out;          // out fp32 (else bf16)
 };
 
+struct ChunkBwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  float scale;
+  const float* init_state;  // [B, H, dk, dv] or null
+  const void* d_out;        // [rows, H, dv]
+  const float* d_final;     // [B, H, dk, dv] or null
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dg;                // g's shape, or null
+  float* d_init;            // [B, H, dk, dv] or null
+  const int32_t* cu_seqlens;
+  int B, H, T;
+  int dk_size, dv_size;
+  bool fp32_io;
+  bool fp32_out;
+  bool vector_gate;
+  unsigned* status;
+};
+
 // Kernel launchers (one per translation unit).  They assume validated arguments
 // and a non-empty problem, and return the launch error.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
@@ -82,6 +105,11 @@ bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_vec_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
+// the chunked backward, one launcher per (gate, I/O dtype)
+cudaError_t launch_chunk_bwd_head_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_bwd_head_f32(const ChunkBwdArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_bwd_chan_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_bwd_chan_f32(const ChunkBwdArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Small device helpers shared by the kernels.

@@ -165,6 +165,21 @@ def mixer_inputs(w: Workload, lead, seed: Optional[int] = None, tiers: int = 4, 
     return dict(aug=aug, norm_w=norm_w, eps=1e-6, z=z)
 
 
+def grad_inputs(x, seed: Optional[int] = None, d_final_std: float = 0.1):
+    """Upstream gradients for a backward call on prefill inputs ``x`` (a dict
+    from ``prefill_inputs``): ``d_out`` ~ N(0, 1) shaped like v in the I/O
+    dtype, and ``d_final_state`` ~ N(0, d_final_std) fp32 [B, H, dk, dv]
+    (None when ``d_final_std`` is 0)."""
+    w = x["workload"]
+    gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 13)
+    d_out = _normal(gen, tuple(x["v"].shape)).to(x["v"].dtype).contiguous()
+    B = x["init_state"].shape[0] if x["init_state"] is not None else (
+        len(x["cu_seqlens"]) - 1 if x["cu_seqlens"] is not None else x["q"].shape[0])
+    H, dk, dv = x["q"].shape[-2], x["q"].shape[-1], x["v"].shape[-1]
+    d_final = _normal(gen, (B, H, dk, dv), d_final_std) if d_final_std > 0 else None
+    return dict(d_out=d_out, d_final_state=d_final)
+
+
 def decode_inputs(w: Workload, seed: Optional[int] = None, **override):
     """Decode inputs: ``state [N, H, dk, dv]`` fp32 and per-step lists of
     ``q, k [N, H, dk]``, ``v [N, H, dv]`` (I/O dtype) and ``g`` ([N, H] or

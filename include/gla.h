@@ -24,6 +24,8 @@
  *                    fixed-size state page updated in place (section
  *                    "Inference optimization on Trainium2": one fixed page per
  *                    sequence).
+ *   gla_chunk_bwd    the gradient of the prefill (dq, dk, dv, dg and the
+ *                    initial state's gradient) for training.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
@@ -212,6 +214,46 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
                                  const int32_t *slots, void *out, int N, int H, int dk, int dv,
                                  const float *aug, const float *norm_w, float eps,
                                  const void *z, gla_stream_t stream, unsigned flags);
+
+/*
+ * gla_chunk_bwd -- the gradient of gla_chunk_fwd (training), for a loss whose
+ * gradients with respect to out and final_state are d_out and d_final_state.
+ *
+ * Source: "i14 Laplace 3B" page, section "Challenge 1" (the chunked layer is
+ * trained; its backward pass runs over the chunks like the forward) with the
+ * recurrence of the "GLA mixer" paragraph.  Reverse mode through
+ * S_t = diag(exp g_t) S_{t-1} + k_t^T v_t, o_t = scale q_t S_t: with
+ * Sbar_t = dL/dS_t = scale q_t^T do_t + diag(exp g_{t+1}) Sbar_{t+1},
+ *     dq_t = scale S_t do_t^T      dk_t = Sbar_t v_t^T      dv_t = k_t Sbar_t
+ *     dg_t[i] = exp(g_t[i]) sum_j S_{t-1}[i][j] Sbar_t[i][j]  (summed over i
+ *               for the per-head gate)
+ *     d_init = diag(exp g_0) Sbar_0
+ * computed chunk by chunk (64 tokens) in fp32.  The gate is clamped at -30 as
+ * in the forward; dg is the gradient with respect to the clamped gate.
+ *
+ * Arguments
+ *   q, k, v, g, scale, init_state, cu_seqlens, B, H, T, dk, dv
+ *                 exactly as passed to gla_chunk_fwd
+ *   d_out         [B, T, H, dv] / [R, H, dv], q's dtype: dL/d out
+ *   d_final_state fp32 [B, H, dk, dv] dL/d final_state, or NULL (zero)
+ *   dq, dk_out    [.., H, dk]; dv_out [.., H, dv]: q's dtype, fp32 with
+ *                 GLA_FLAG_FP32_OUT (the bf16 results are these rounded to
+ *                 nearest-even)
+ *   dg            fp32, g's shape, or NULL (not computed).  With the per-head
+ *                 gate its terms are summed across CTAs with fp32 atomics, so
+ *                 its last bits may vary from run to run.
+ *   d_init_state  fp32 [B, H, dk, dv], or NULL (not written)
+ *   flags         GLA_FLAG_FP32_IO, GLA_FLAG_VECTOR_GATE, GLA_FLAG_FP32_OUT
+ * The outputs must not overlap one another or any input.  Empty sequences
+ * write d_init_state = d_final_state (or zeros).  Four kernel launches (a
+ * fifth, and a memset of dg, for the per-head gate's dg) on the CUDA cores.
+ * Alignment: as gla_chunk_fwd; every output 16-byte aligned.
+ */
+gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
+                         float scale, const float *init_state, const void *d_out,
+                         const float *d_final_state, void *dq, void *dk_out, void *dv_out,
+                         float *dg, float *d_init_state, const int32_t *cu_seqlens, int B,
+                         int H, int T, int dk, int dv, gla_stream_t stream, unsigned flags);
 
 /*
  * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call

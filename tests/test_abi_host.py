@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots", "gla_status_string",
-              "gla_status_sync"):
+    for n in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step", "gla_decode_step_slots",
+              "gla_status_string", "gla_status_sync"):
         assert n in names
 
 
@@ -157,7 +157,7 @@ def test_decode_step_empty_is_no_op(L):
 def test_ctypes_signatures_match_header(L):
     """The binding's argument counts equal the header's parameter counts."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    for name in ("gla_chunk_fwd", "gla_decode_step", "gla_decode_step_slots",
+    for name in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step", "gla_decode_step_slots",
                  "gla_decode_step_mixer", "gla_mixer_epilogue", "gla_status_sync",
                  "gla_status_string"):
         m = re.search(name + r"\s*\(([^)]*)\)", text)
@@ -203,3 +203,41 @@ def test_decode_mixer_rejects_before_launch(L):
     assert call(num_slots=3) == E.GLA_ERR_INVALID_ARG      # a pool size without slots
     assert call(eps=-0.5) == E.GLA_ERR_INVALID_ARG
     assert call(q=0) == E.GLA_ERR_INVALID_ARG
+
+
+def bwd(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, init=FAKE[4], d_out=FAKE[5],
+        d_final=FAKE[6], dq=FAKE[7], dk_out=FAKE[8], dv_out=FAKE[9], dg=FAKE[10],
+        d_init=FAKE[11], cu=0, B=2, H=4, T=256, dk=128, dv=128, flags=0):
+    return _binding.gla_chunk_bwd(q, k, v, g, scale, init, d_out, d_final, dq, dk_out, dv_out,
+                                  dg, d_init, cu, B, H, T, dk, dv, 0, flags)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=1 << 5), E.GLA_ERR_INVALID_ARG),
+    (dict(B=-1), E.GLA_ERR_INVALID_ARG),
+    (dict(T=-2), E.GLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), E.GLA_ERR_INVALID_ARG),
+    (dict(dk=80), E.GLA_ERR_UNSUPPORTED),
+    (dict(dv=96), E.GLA_ERR_UNSUPPORTED),
+    (dict(d_out=0), E.GLA_ERR_INVALID_ARG),
+    (dict(dq=0), E.GLA_ERR_INVALID_ARG),
+    (dict(dv_out=0), E.GLA_ERR_INVALID_ARG),
+    (dict(dq=FAKE[7] + 8), E.GLA_ERR_MISALIGNED),
+    (dict(dg=FAKE[10] + 4), E.GLA_ERR_MISALIGNED),
+    (dict(d_init=FAKE[11] + 4), E.GLA_ERR_MISALIGNED),
+    (dict(g=FAKE[3] + 4, flags=E.GLA_FLAG_VECTOR_GATE), E.GLA_ERR_MISALIGNED),
+    (dict(dq=FAKE[0]), E.GLA_ERR_INVALID_ARG),             # dq overlaps q
+    (dict(dk_out=FAKE[7] + 64), E.GLA_ERR_INVALID_ARG),    # dk overlaps dq
+    (dict(d_init=FAKE[6]), E.GLA_ERR_INVALID_ARG),         # d_init overlaps d_final
+    (dict(dg=FAKE[5] + 256), E.GLA_ERR_INVALID_ARG),       # dg inside d_out
+    (dict(B=1 << 20, T=1 << 20), E.GLA_ERR_INVALID_ARG),   # size overflow
+])
+def test_chunk_bwd_rejects_before_launch(L, kw, status):
+    assert bwd(**kw) == status
+
+
+def test_chunk_bwd_empty_problems_are_no_ops(L):
+    assert bwd(B=0) == E.GLA_OK
+    assert bwd(H=0) == E.GLA_OK
+    assert bwd(T=0, d_init=0, q=0, k=0, v=0, g=0, d_out=0, dq=0, dk_out=0, dv_out=0,
+               dg=0) == E.GLA_OK

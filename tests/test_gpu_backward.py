@@ -1,0 +1,190 @@
+"""GPU chunked backward (gla_chunk_bwd) against the fp64 oracle's gradient.
+
+The oracle's gradient (reverse mode through the recurrence, token by token)
+is itself pinned to finite differences of the forward in
+``test_oracle_backward_pins.py``.  Here the GPU path is compared with it at
+sizes the oracle finishes in seconds that span several 64-token chunks and a
+ragged tail, for both gate shapes, every head size, packed batches with empty
+sequences, fp32 I/O, the optional inputs and outputs left out, strong decays,
+and at the prefill workload's full size on sampled (sequence, head) pairs.
+
+Error norm: ``max |x - ref| / RMS(ref)`` per gradient.  Tolerances (fp32
+arithmetic throughout; no tolerance is stated for the gradient, so these are
+derived from the arithmetic): dq, dk, dv and d_init 1e-4 -- each element is an
+fp32 sum of at most 64 + d products of exactly represented inputs and decay
+factors accurate to a few ulp, so the expected error is ~1e-6 of the RMS;
+dg 1e-3 -- every dg_t is a suffix sum over up to T per-token terms, each
+itself carrying the error above.  bf16 gradients must equal the fp32 ones
+rounded once to nearest-even.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gla_inputs
+import oracle
+from parity import cuda, rel_max, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL_GRAD = 1e-4
+TOL_DG = 1e-3
+
+
+def _gla():
+    import gated_linear_attention_gla_gb300 as gla
+    return gla
+
+
+def run_gpu(x, gr, grad_dtype=None, need_dg=True, need_d_init=True, init=True, final=True):
+    gla = _gla()
+    res = gla.chunk_bwd(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]),
+                        cuda(gr["d_out"]), scale=x["scale"],
+                        init_state=cuda(x["init_state"]) if init else None,
+                        d_final_state=cuda(gr["d_final_state"]) if final else None,
+                        cu_seqlens=cuda(x["cu_seqlens"]), grad_dtype=grad_dtype,
+                        need_dg=need_dg, need_d_init=need_d_init)
+    gla.status_sync()
+    return res
+
+
+def run_ref(x, gr, init=True, final=True):
+    return oracle.backward(x["q"], x["k"], x["v"], x["g"], x["scale"], gr["d_out"],
+                           init_state=x["init_state"] if init else None,
+                           d_final=gr["d_final_state"] if final else None,
+                           cu_seqlens=x["cu_seqlens"])
+
+
+NAMES = ("dq", "dk", "dv", "dg", "d_init")
+
+
+def check(got, ref, tol=TOL_GRAD, tol_dg=TOL_DG, label=""):
+    errs = {}
+    for name, a, b in zip(NAMES, got, ref):
+        if a is None:
+            continue
+        errs[name] = rel_max(to_np(a), b)
+    print(label, {k: f"{v:.2e}" for k, v in errs.items()})
+    for name, e in errs.items():
+        lim = tol_dg if name == "dg" else tol
+        assert e <= lim, f"{label} {name} error {e:.3e} > {lim:.0e}"
+
+
+def inputs(name="prefill", seed=None, **over):
+    x = gla_inputs.prefill_inputs(gla_inputs.WORKLOADS[name], seed=seed, **over)
+    return x, gla_inputs.grad_inputs(x, seed=seed)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_backward_matches_oracle(gate):
+    # 200 tokens: three full 64-token chunks and a ragged tail of 8
+    x, gr = inputs(B=2, T=200, H=3, gate=gate, g_mu=2.0 if gate == "vector" else 3.0)
+    got = run_gpu(x, gr, grad_dtype=torch.float32)
+    check(got, run_ref(x, gr), label=gate)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_bf16_gradients_are_the_fp32_ones_rounded(gate):
+    x, gr = inputs(B=1, T=130, H=2, gate=gate)
+    g32 = run_gpu(x, gr, grad_dtype=torch.float32)
+    g16 = run_gpu(x, gr)
+    for a, b in zip(g16[:3], g32[:3]):
+        assert a.dtype == torch.bfloat16
+        assert torch.equal(a, b.to(torch.bfloat16))
+    assert torch.equal(g16[4], g32[4])
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 192), (96, 192), (96, 128), (128, 64),
+                                   (128, 192)])
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_head_sizes(dk, dv, gate):
+    x, gr = inputs(B=1, T=100, H=2, dk=dk, dv=dv, gate=gate)
+    check(run_gpu(x, gr, grad_dtype=torch.float32), run_ref(x, gr), label=f"{gate} {dk}x{dv}")
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_fp32_io(gate):
+    x, gr = inputs("tiny", B=2, T=150, gate=gate, init_std=0.05)
+    got = run_gpu(x, gr)
+    assert got[0].dtype == torch.float32
+    check(got, run_ref(x, gr), label=f"fp32 {gate}")
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_packed_with_empty_and_short_sequences(gate):
+    x, gr = inputs("varlen", lengths=[70, 0, 1, 129, 64, 5], H=2, gate=gate)
+    got = run_gpu(x, gr, grad_dtype=torch.float32)
+    ref = run_ref(x, gr)
+    check(got, ref, label=f"packed {gate}")
+    # the empty sequence hands d_final through to d_init
+    assert torch.equal(got[4][1].cpu(), gr["d_final_state"][1])
+
+
+def test_optional_inputs_and_outputs_left_out():
+    x, gr = inputs(B=2, T=90, H=2)
+    ref = run_ref(x, gr, init=False, final=False)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, init=False, final=False)
+    check(got, ref, label="no init/final")
+    dq, dk, dv, dg, d0 = run_gpu(x, gr, grad_dtype=torch.float32, need_dg=False,
+                                 need_d_init=False, init=False, final=False)
+    assert dg is None and d0 is None
+    assert torch.equal(dq, got[0]) and torch.equal(dk, got[1]) and torch.equal(dv, got[2])
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_strong_and_clamped_decays(gate):
+    """Gates around -40 (down to -125).  The kernels raise gates below -30 to
+    -30, so their gradients are those of the clamped gate: the reference is the
+    oracle's gradient at max(g, -30) (it moves dq, dk, dv by ~1e-12 but d_init,
+    the gradient through the first token's decay, by a few per cent).  dg comes
+    from suffix sums of per-token terms x_t = q_t dq_t - k_t dk_t (summed over
+    the key channels for the per-head gate) whose exact total is tiny here
+    (RMS(dg) / RMS(x) ~ 1e-4), so its error is bounded in absolute terms: each
+    x_t carries a relative error of a few 1e-6 and a suffix has up to T terms,
+    hence max |dg - ref| <= 1e-4 RMS(x)."""
+    x, gr = inputs(B=1, T=140, H=2, gate=gate, g_mu=-2.0, g_div=0.05)
+    assert float(x["g"].min()) < -30
+    xc = dict(x, g=x["g"].clamp(min=-30.0))
+    got = run_gpu(x, gr, grad_dtype=torch.float32)
+    ref = run_ref(xc, gr)
+    check(got[:3] + (None,) + got[4:], ref, label=f"strong {gate}")
+    terms = to_np(x["q"]) * ref[0] - to_np(x["k"]) * ref[1]
+    if gate == "scalar":
+        terms = terms.sum(-1)
+    err = float(np.max(np.abs(to_np(got[3]) - ref[3])))
+    scale_x = float(np.sqrt(np.mean(terms * terms)))
+    print(f"strong {gate} dg: max err {err:.2e}, RMS(x) {scale_x:.2e}, "
+          f"RMS(dg) {float(np.sqrt(np.mean(ref[3] ** 2))):.2e}")
+    assert err <= 1e-4 * scale_x
+
+
+def test_empty_batch_and_zero_length():
+    gla = _gla()
+    x, gr = inputs(B=2, T=0, H=2)
+    res = gla.chunk_bwd(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]),
+                        cuda(gr["d_out"]), init_state=cuda(x["init_state"]),
+                        d_final_state=cuda(gr["d_final_state"]))
+    gla.status_sync()
+    assert torch.equal(res[4].cpu(), gr["d_final_state"])
+
+
+@pytest.mark.parametrize("gate", ["scalar", "vector"])
+def test_full_size_sampled_pairs(gate):
+    """The prefill workload at full size (B=4, H=16, T=2048) -- the launch
+    configuration the benchmark times -- checked on sampled (sequence, head)
+    pairs, each run through the oracle alone (pairs are independent)."""
+    over = {} if gate == "scalar" else dict(gate="vector", g_mu=2.0, g_div=4.0)
+    x, gr = inputs(**over)
+    got = run_gpu(x, gr, grad_dtype=torch.float32)
+    for b, h in [(0, 0), (3, 15), (2, 7)]:
+        sub = dict(x)
+        for key in ("q", "k", "v", "g"):
+            sub[key] = x[key][b:b + 1, :, h:h + 1]
+        sub["init_state"] = x["init_state"][b:b + 1, h:h + 1]
+        sgr = dict(d_out=gr["d_out"][b:b + 1, :, h:h + 1],
+                   d_final_state=gr["d_final_state"][b:b + 1, h:h + 1])
+        ref = run_ref(sub, sgr)
+        mine = [got[0][b:b + 1, :, h:h + 1], got[1][b:b + 1, :, h:h + 1],
+                got[2][b:b + 1, :, h:h + 1], got[3][b:b + 1, :, h:h + 1],
+                got[4][b:b + 1, h:h + 1]]
+        check(mine, ref, label=f"full {gate} ({b},{h})")
