@@ -54,7 +54,7 @@ constexpr int kBwdThreads = 256;
 constexpr int kC = 64;    // tokens per chunk
 constexpr int kIS = 32;   // key rows per CTA (dq and dk kernels)
 constexpr int kJS = 64;   // value columns per CTA (dv kernel)
-constexpr int kLDP = kC + 1;
+constexpr int kLDP = kC + 4;  // P and M rows: 16-byte aligned, 4 banks apart
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Store a gradient element as fp32 or (rounded to nearest-even) bf16.
@@ -65,35 +65,104 @@ __device__ __forceinline__ void store_grad(void* p, long long idx, float x, bool
     static_cast<__nv_bfloat16*>(p)[idx] = __float2bfloat16_rn(x);
 }
 
-// dst[t][c] (row stride ld) <- src rows base + t, columns c0 + c of a [rows, H, D]
-// tensor, for t < kC and c < W; rows past n are zero.
-template <int W, typename IO>
-__device__ __forceinline__ void load_tile(float* dst, int ld, const IO* __restrict__ src,
-                                          long long base, int n, int H, int h, int D, int c0) {
-  for (int idx = threadIdx.x; idx < kC * W; idx += kBwdThreads) {
-    const int t = idx / W, c = idx - t * W;
-    dst[t * ld + c] =
-        t < n ? to_f32(src[((base + t) * H + h) * (long long)D + c0 + c]) : 0.f;
+// Four consecutive floats into shared memory: one 128-bit store where the row
+// stride keeps them 16-byte aligned, else four scalar stores.
+__device__ __forceinline__ void store4(float* d, float4 x, int ld) {
+  if ((ld & 3) == 0) {
+    *reinterpret_cast<float4*>(d) = x;
+  } else {
+    d[0] = x.x;
+    d[1] = x.y;
+    d[2] = x.z;
+    d[3] = x.w;
   }
 }
 
-// G[t][c] <- log2(e) * sum_{s<=t} max(g_s, -clamp) for the chunk's tokens, per
-// key channel c0 + c (W columns, row stride ld) or per head (W = 1).  Rows past
-// n repeat the last sum.  Two barriers inside.
-template <int W, bool VEC>
-__device__ __forceinline__ void load_gate(float* G, int ld, const float* __restrict__ g,
-                                          long long base, int n, int H, int h, int DK, int c0) {
-  for (int idx = threadIdx.x; idx < kC * W; idx += kBwdThreads) {
-    const int t = idx / W, c = idx - t * W;
-    float x = 0.f;
-    if (t < n) {
-      const float raw = VEC ? g[((base + t) * H + h) * (long long)DK + c0 + c]
-                            : g[(base + t) * H + h];
-      x = fmaxf(raw, -kGateClamp) * kLog2e;
+// A chunk's tile of a [rows, H, D] tensor -- rows base .. base + kC - 1,
+// columns c0 .. c0 + W - 1 -- fetched as 16-byte vectors into registers, so
+// that the next chunk's loads are in flight while this chunk is computed, and
+// then put into shared memory as fp32 (row stride ld).  Rows past n are zero.
+// Every row and column offset is a multiple of 16 bytes (checked by the host:
+// 16-byte-aligned tensors, d a multiple of 32).
+template <typename IO, int W>
+struct TileFetch {
+  static constexpr int VE = 16 / (int)sizeof(IO);  // elements per vector
+  static constexpr int VPR = W / VE;               // vectors per row
+  static constexpr int NV = kC * VPR;
+  static constexpr int PER = (NV + kBwdThreads - 1) / kBwdThreads;
+  static_assert(W % VE == 0, "tile width must be whole vectors");
+  uint4 r[PER];
+
+  __device__ __forceinline__ void fetch(const IO* __restrict__ src, long long base, int n,
+                                        int H, int h, int D, int c0) {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int idx = threadIdx.x + p * kBwdThreads;
+      const int t = idx / VPR, cv = idx - t * VPR;
+      r[p] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < NV && t < n)
+        r[p] = __ldg(reinterpret_cast<const uint4*>(
+            src + ((base + t) * H + h) * (long long)D + c0 + cv * VE));
     }
-    G[t * ld + c] = x;
   }
-  __syncthreads();
+
+  __device__ __forceinline__ void put(float* dst, int ld) const {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int idx = threadIdx.x + p * kBwdThreads;
+      if (idx < NV) {
+        const int t = idx / VPR, cv = idx - t * VPR;
+        float* d = dst + t * ld + cv * VE;
+        if constexpr (sizeof(IO) == 4) {
+          store4(d, make_float4(__uint_as_float(r[p].x), __uint_as_float(r[p].y),
+                                __uint_as_float(r[p].z), __uint_as_float(r[p].w)), ld);
+        } else {
+          // bf16 -> fp32 is exact: the bf16 bits are the high half of the float
+          store4(d, make_float4(__uint_as_float(r[p].x << 16),
+                                __uint_as_float(r[p].x & 0xffff0000u),
+                                __uint_as_float(r[p].y << 16),
+                                __uint_as_float(r[p].y & 0xffff0000u)), ld);
+          store4(d + 4, make_float4(__uint_as_float(r[p].z << 16),
+                                    __uint_as_float(r[p].z & 0xffff0000u),
+                                    __uint_as_float(r[p].w << 16),
+                                    __uint_as_float(r[p].w & 0xffff0000u)), ld);
+        }
+      }
+    }
+  }
+};
+
+// The chunk's log-decays: per key channel (W columns from c0, fetched like a
+// tile) or per head (one value per token, strided by H).  put() stores them
+// raw; gate_scan() turns them into running sums.
+template <bool VEC, int W>
+struct GateFetch {
+  TileFetch<float, VEC ? W : 4> vec;
+  float one;
+
+  __device__ __forceinline__ void fetch(const float* __restrict__ g, long long base, int n,
+                                        int H, int h, int DK, int c0) {
+    if constexpr (VEC) {
+      vec.fetch(g, base, n, H, h, DK, c0);
+    } else {
+      one = 0.f;
+      if ((int)threadIdx.x < n) one = __ldg(g + (base + threadIdx.x) * H + h);
+    }
+  }
+
+  __device__ __forceinline__ void put(float* G, int ld) const {
+    if constexpr (VEC)
+      vec.put(G, ld);
+    else if (threadIdx.x < kC)
+      G[threadIdx.x] = one;
+  }
+};
+
+// G[t][c] <- log2(e) * sum_{s<=t} max(g_s, -clamp) down each of W columns
+// (row stride ld), in place over the raw values that put() stored.  Rows past
+// the chunk's end hold 0 and so repeat the last sum.
+template <int W>
+__device__ __forceinline__ void gate_scan(float* G, int ld) {
   if (threadIdx.x < W) {
     float v[kC];
 #pragma unroll
@@ -101,11 +170,10 @@ __device__ __forceinline__ void load_gate(float* G, int ld, const float* __restr
     float run = 0.f;
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
-      run += v[t];
+      run += fmaxf(v[t], -kGateClamp) * kLog2e;
       G[t * ld + threadIdx.x] = run;
     }
   }
-  __syncthreads();
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -121,27 +189,143 @@ __device__ __forceinline__ float row_sum16(float x) {
   return x;
 }
 
+// ---------------------------------------------------------------------------
+// Register-tile products over shared memory.  Thread (tx, ty) = (tid % 16,
+// tid / 16).  Row strides are multiples of 4 floats (16-byte rows) and, where
+// 16 lanes read 16 different rows, 4 modulo 32, so that those 128-bit reads
+// fall in distinct banks; the reads that all lanes of a half-warp share are
+// broadcasts.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float2 ld2(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+__device__ __forceinline__ float comp(const float4& x, int i) {
+  return i == 0 ? x.x : i == 1 ? x.y : i == 2 ? x.z : x.w;
+}
+
+// acc[m][n] += sum_k A[ty + 16 m][k] B[tx + 16 n][k]   (K a multiple of 4)
+template <int TM, int TN>
+__device__ __forceinline__ void gemm_nt(float (&acc)[TM][TN], const float* A, int lda,
+                                        const float* B, int ldb, int K) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float* pa = A + ty * lda;
+  const float* pb = B + tx * ldb;
+  float4 a[2][TM], b[2][TN];  // fragments of step k and k + 4, loaded one step ahead
+#pragma unroll
+  for (int m = 0; m < TM; ++m) a[0][m] = ld4(pa + 16 * m * lda);
+#pragma unroll
+  for (int n = 0; n < TN; ++n) b[0][n] = ld4(pb + 16 * n * ldb);
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    const int cur = (k >> 2) & 1;
+    if (k + 4 < K) {
+#pragma unroll
+      for (int m = 0; m < TM; ++m) a[cur ^ 1][m] = ld4(pa + 16 * m * lda + k + 4);
+#pragma unroll
+      for (int n = 0; n < TN; ++n) b[cur ^ 1][n] = ld4(pb + 16 * n * ldb + k + 4);
+    }
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+#pragma unroll
+      for (int n = 0; n < TN; ++n) {
+        acc[m][n] = fmaf(a[cur][m].x, b[cur][n].x, acc[m][n]);
+        acc[m][n] = fmaf(a[cur][m].y, b[cur][n].y, acc[m][n]);
+        acc[m][n] = fmaf(a[cur][m].z, b[cur][n].z, acc[m][n]);
+        acc[m][n] = fmaf(a[cur][m].w, b[cur][n].w, acc[m][n]);
+      }
+  }
+}
+
+// acc[m][n] += sum_k A[ty + 16 m][k] B[k][tx + 16 n]   (K a multiple of 4)
+template <int TM, int TN>
+__device__ __forceinline__ void gemm_nn(float (&acc)[TM][TN], const float* A, int lda,
+                                        const float* B, int ldb, int K) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[TM];
+#pragma unroll
+    for (int m = 0; m < TM; ++m) a[m] = ld4(A + (ty + 16 * m) * lda + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      float b[TN];
+#pragma unroll
+      for (int n = 0; n < TN; ++n) b[n] = B[(k + kk) * ldb + tx + 16 * n];
+#pragma unroll
+      for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int n = 0; n < TN; ++n) acc[m][n] = fmaf(comp(a[m], kk), b[n], acc[m][n]);
+    }
+  }
+}
+
+// Column of element n of a thread's row when every thread owns runs of four
+// adjacent columns, the runs of a half-warp side by side: 4 tx + 64 (n / 4) + n % 4.
+__device__ __forceinline__ int col4(int n) {
+  return 4 * (threadIdx.x & 15) + 64 * (n >> 2) + (n & 3);
+}
+
+// acc[m][n] += sum_k A[k][TM ty + m] B[k][col4(n)]   (TM even, TN a multiple of 4)
+template <int TM, int TN>
+__device__ __forceinline__ void gemm_tn(float (&acc)[TM][TN], const float* A, int lda,
+                                        const float* B, int ldb, int K) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    float a[TM];
+    float4 b[TN / 4];
+#pragma unroll
+    for (int m = 0; m < TM; m += 2) {
+      const float2 x = ld2(A + k * lda + TM * ty + m);
+      a[m] = x.x;
+      a[m + 1] = x.y;
+    }
+#pragma unroll
+    for (int n = 0; n < TN / 4; ++n) b[n] = ld4(B + k * ldb + 4 * tx + 64 * n);
+#pragma unroll
+    for (int m = 0; m < TM; ++m)
+#pragma unroll
+      for (int n = 0; n < TN; ++n) acc[m][n] = fmaf(a[m], comp(b[n >> 2], n & 3), acc[m][n]);
+  }
+}
+
+// acc[m][n] += sum_k A[TM ty + m][k] B[k][col4(n)]   (K a multiple of 4, TN of 4)
+template <int TM, int TN>
+__device__ __forceinline__ void gemm_nn4(float (&acc)[TM][TN], const float* A, int lda,
+                                         const float* B, int ldb, int K) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[TM];
+#pragma unroll
+    for (int m = 0; m < TM; ++m) a[m] = ld4(A + (TM * ty + m) * lda + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      float4 b[TN / 4];
+#pragma unroll
+      for (int n = 0; n < TN / 4; ++n) b[n] = ld4(B + (k + kk) * ldb + 4 * tx + 64 * n);
+#pragma unroll
+      for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int n = 0; n < TN; ++n)
+          acc[m][n] = fmaf(comp(a[m], kk), comp(b[n >> 2], n & 3), acc[m][n]);
+    }
+  }
+}
+
 // P[a][b] = dO_a . V_b for b <= a (the later token a, the earlier b), times
 // exp(G_a - G_b) for the per-head gate; zero above the diagonal.  The same
 // matrix serves dq (rows t, columns u <= t) and dk (rows u, columns t <= u).
 template <int DV, bool VEC>
 __device__ __forceinline__ void make_p(float* sP, const float* sDO, const float* sV,
                                        const float* sG) {
-  constexpr int LDV = DV + 1;
+  constexpr int LDV = DV + 4;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   float acc[4][4] = {};
-#pragma unroll 4
-  for (int j = 0; j < DV; ++j) {
-    float a[4], b[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) a[m] = sDO[(ty + 16 * m) * LDV + j];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) b[c] = sV[(tx + 16 * c) * LDV + j];
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(a[m], b[c], acc[m][c]);
-  }
+  gemm_nt<4, 4>(acc, sDO, LDV, sV, LDV, DV);
 #pragma unroll
   for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -158,7 +342,7 @@ __device__ __forceinline__ void make_p(float* sP, const float* sDO, const float*
 // ---------------------------------------------------------------------------
 template <int DK, int DV, bool VEC>
 struct DqSmem {
-  static constexpr int LDV = DV + 1;
+  static constexpr int LDV = DV + 4;  // 16-byte rows, 4 banks apart
   static constexpr int GW = VEC ? kIS : 1;
   static constexpr int kFloats =
       2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP + kIS * LDV;
@@ -198,15 +382,33 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     sS[i * LDV + j] = init_state ? init_state[st_off + (size_t)(i0 + i) * DV + j] : 0.f;
   }
 
+  TileFetch<IO, DV> fDO, fV;
+  TileFetch<IO, kIS> fK, fQ;
+  GateFetch<VEC, kIS> fG;
+  auto fetch = [&](int c) {
+    const int n = min(kC, len - c);
+    const long long base = start + c;
+    fDO.fetch(d_out, base, n, H, h, DV, 0);
+    fV.fetch(v, base, n, H, h, DV, 0);
+    fK.fetch(k, base, n, H, h, DK, i0);
+    if (dg) fQ.fetch(q, base, n, H, h, DK, i0);
+    fG.fetch(g, base, n, H, h, DK, i0);
+  };
+  if (len > 0) fetch(0);
+
   for (int c0 = 0; c0 < len; c0 += kC) {
     const int n = min(kC, len - c0);
     const long long base = start + c0;
     __syncthreads();  // the previous chunk is consumed
-    load_tile<DV>(sDO, LDV, d_out, base, n, H, h, DV, 0);
-    load_tile<DV>(sV, LDV, v, base, n, H, h, DV, 0);
-    load_tile<kIS>(sK, kIS, k, base, n, H, h, DK, i0);
-    if (dg) load_tile<kIS>(sQ, kIS, q, base, n, H, h, DK, i0);
-    load_gate<GW, VEC>(sG, GW, g, base, n, H, h, DK, i0);
+    fDO.put(sDO, LDV);
+    fV.put(sV, LDV);
+    fK.put(sK, kIS);
+    if (dg) fQ.put(sQ, kIS);
+    fG.put(sG, GW);
+    __syncthreads();
+    if (c0 + kC < len) fetch(c0 + kC);  // in flight during this chunk
+    gate_scan<GW>(sG, GW);
+    __syncthreads();
     make_p<DV, VEC>(sP, sDO, sV, sG);
     __syncthreads();
 
@@ -238,31 +440,9 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
             }
         }
       } else {
-#pragma unroll 4
-        for (int u = 0; u < kC; ++u) {
-          float a[4], b[2];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) a[m] = sP[(ty + 16 * m) * kLDP + u];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) b[c] = sK[u * kIS + tx + 16 * c];
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) intra[m][c] = fmaf(a[m], b[c], intra[m][c]);
-        }
+        gemm_nn<4, 2>(intra, sP, kLDP, sK, kIS, kC);
       }
-#pragma unroll 4
-      for (int j = 0; j < DV; ++j) {
-        float a[4], b[2];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) a[m] = sDO[(ty + 16 * m) * LDV + j];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) b[c] = sS[(tx + 16 * c) * LDV + j];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) inter[m][c] = fmaf(a[m], b[c], inter[m][c]);
-      }
+      gemm_nt<4, 2>(inter, sDO, LDV, sS, LDV, DV);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int t = ty + 16 * m;
@@ -297,26 +477,16 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     }
     __syncthreads();
     {
+      // rows i = 2 ty + r, columns col4(c)
       float acc[2][TN] = {};
-#pragma unroll 4
-      for (int u = 0; u < kC; ++u) {
-        float a[2], b[TN];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) a[r] = sK[u * kIS + ty + 16 * r];
-#pragma unroll
-        for (int c = 0; c < TN; ++c) b[c] = sV[u * LDV + tx + 16 * c];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-      }
+      gemm_tn<2, TN>(acc, sK, kIS, sV, LDV, kC);
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int i = ty + 16 * r;
+        const int i = 2 * ty + r;
         const float el = exp2f(VEC ? sG[(n - 1) * kIS + i] : sG[n - 1]);
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
-          float* p = sS + i * LDV + tx + 16 * c;
+          float* p = sS + i * LDV + col4(c);
           *p = fmaf(el, *p, acc[r][c]);
         }
       }
@@ -348,7 +518,7 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
 // ---------------------------------------------------------------------------
 template <int DK, int DV, bool VEC>
 struct DkSmem {
-  static constexpr int LDV = DV + 1;
+  static constexpr int LDV = DV + 4;  // 16-byte rows, 4 banks apart
   static constexpr int GW = VEC ? kIS : 1;
   static constexpr int kFloats =
       2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP + kIS * LDV + (VEC ? kC * kIS : 0);
@@ -390,15 +560,34 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   }
   float carry = 0.f;  // per-key-channel gate: thread i < kIS carries column i's suffix sum
 
-  for (int c0 = ((len - 1) / kC) * kC; c0 >= 0 && len > 0; c0 -= kC) {
+  TileFetch<IO, DV> fDO, fV;
+  TileFetch<IO, kIS> fQ, fK;
+  GateFetch<VEC, kIS> fG;
+  auto fetch = [&](int c) {
+    const int n = min(kC, len - c);
+    const long long base = start + c;
+    fDO.fetch(d_out, base, n, H, h, DV, 0);
+    fV.fetch(v, base, n, H, h, DV, 0);
+    fQ.fetch(q, base, n, H, h, DK, i0);
+    if (dg) fK.fetch(k, base, n, H, h, DK, i0);
+    fG.fetch(g, base, n, H, h, DK, i0);
+  };
+  const int last_c0 = len > 0 ? ((len - 1) / kC) * kC : -1;
+  if (len > 0) fetch(last_c0);
+
+  for (int c0 = last_c0; c0 >= 0; c0 -= kC) {
     const int n = min(kC, len - c0);
     const long long base = start + c0;
     __syncthreads();
-    load_tile<DV>(sDO, LDV, d_out, base, n, H, h, DV, 0);
-    load_tile<DV>(sV, LDV, v, base, n, H, h, DV, 0);
-    load_tile<kIS>(sQ, kIS, q, base, n, H, h, DK, i0);
-    if (dg) load_tile<kIS>(sK, kIS, k, base, n, H, h, DK, i0);
-    load_gate<GW, VEC>(sG, GW, g, base, n, H, h, DK, i0);
+    fDO.put(sDO, LDV);
+    fV.put(sV, LDV);
+    fQ.put(sQ, kIS);
+    if (dg) fK.put(sK, kIS);
+    fG.put(sG, GW);
+    __syncthreads();
+    if (c0 > 0) fetch(c0 - kC);  // in flight during this chunk
+    gate_scan<GW>(sG, GW);
+    __syncthreads();
     make_p<DV, VEC>(sP, sDO, sV, sG);
     __syncthreads();
 
@@ -443,18 +632,7 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
             for (int c = 0; c < 2; ++c) intra[m][c] = fmaf(a[m], b[c], intra[m][c]);
         }
       }
-#pragma unroll 4
-      for (int j = 0; j < DV; ++j) {
-        float a[4], b[2];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) a[m] = sV[(ty + 16 * m) * LDV + j];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) b[c] = sR[(tx + 16 * c) * LDV + j];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) inter[m][c] = fmaf(a[m], b[c], inter[m][c]);
-      }
+      gemm_nt<4, 2>(inter, sV, LDV, sR, LDV, DV);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int t = ty + 16 * m;
@@ -502,26 +680,16 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     }
     __syncthreads();
     {
+      // rows i = 2 ty + r, columns col4(c)
       float acc[2][TN] = {};
-#pragma unroll 4
-      for (int u = 0; u < kC; ++u) {
-        float a[2], b[TN];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) a[r] = sQ[u * kIS + ty + 16 * r];
-#pragma unroll
-        for (int c = 0; c < TN; ++c) b[c] = sDO[u * LDV + tx + 16 * c];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-      }
+      gemm_tn<2, TN>(acc, sQ, kIS, sDO, LDV, kC);
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int i = ty + 16 * r;
+        const int i = 2 * ty + r;
         const float el = exp2f(VEC ? sG[(n - 1) * kIS + i] : sG[n - 1]);
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
-          float* p = sR + i * LDV + tx + 16 * c;
+          float* p = sR + i * LDV + col4(c);
           *p = fmaf(el, *p, scale * acc[r][c]);
         }
       }
@@ -541,8 +709,8 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
 // ---------------------------------------------------------------------------
 template <int DK, int DV, bool VEC>
 struct DvSmem {
-  static constexpr int LDK = DK + 1;
-  static constexpr int GW = VEC ? LDK : 1;
+  static constexpr int LDK = DK + 4;              // 16-byte rows, 4 banks apart
+  static constexpr int GW = VEC ? DK + 1 : 1;     // gate rows (scalar reads only)
   static constexpr int kFloats = 2 * kC * LDK + kC * kJS + kC * GW + kC * kLDP + DK * kJS;
   static constexpr size_t kBytes = sizeof(float) * (size_t)kFloats;
 };
@@ -578,17 +746,32 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
     sR[idx] = d_final ? d_final[st_off + (size_t)i * DV + j0 + j] : 0.f;
   }
 
-  for (int c0 = ((len - 1) / kC) * kC; c0 >= 0 && len > 0; c0 -= kC) {
+  TileFetch<IO, DK> fQ, fK;
+  TileFetch<IO, kJS> fDO;
+  GateFetch<VEC, DK> fG;
+  auto fetch = [&](int c) {
+    const int n = min(kC, len - c);
+    const long long base = start + c;
+    fQ.fetch(q, base, n, H, h, DK, 0);
+    fK.fetch(k, base, n, H, h, DK, 0);
+    fDO.fetch(d_out, base, n, H, h, DV, j0);
+    fG.fetch(g, base, n, H, h, DK, 0);
+  };
+  const int last_c0 = len > 0 ? ((len - 1) / kC) * kC : -1;
+  if (len > 0) fetch(last_c0);
+
+  for (int c0 = last_c0; c0 >= 0; c0 -= kC) {
     const int n = min(kC, len - c0);
     const long long base = start + c0;
     __syncthreads();
-    load_tile<DK>(sQ, LDK, q, base, n, H, h, DK, 0);
-    load_tile<DK>(sK, LDK, k, base, n, H, h, DK, 0);
-    load_tile<kJS>(sDO, kJS, d_out, base, n, H, h, DV, j0);
-    if constexpr (VEC)
-      load_gate<DK, true>(sG, LDK, g, base, n, H, h, DK, 0);
-    else
-      load_gate<1, false>(sG, 1, g, base, n, H, h, DK, 0);
+    fQ.put(sQ, LDK);
+    fK.put(sK, LDK);
+    fDO.put(sDO, kJS);
+    fG.put(sG, GW);
+    __syncthreads();
+    if (c0 > 0) fetch(c0 - kC);  // in flight during this chunk
+    gate_scan<VEC ? DK : 1>(sG, GW);
+    __syncthreads();
 
     // M[u][t] = q_u . (k_t exp(G_u - G_t)) for t <= u: rows u = ty + 16 m, columns t = tx + 16 c
     {
@@ -600,12 +783,12 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             a[m] = sQ[(ty + 16 * m) * LDK + i];
-            gu[m] = sG[(ty + 16 * m) * LDK + i];
+            gu[m] = sG[(ty + 16 * m) * GW + i];
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             b[c] = sK[(tx + 16 * c) * LDK + i];
-            gt[c] = sG[(tx + 16 * c) * LDK + i];
+            gt[c] = sG[(tx + 16 * c) * GW + i];
           }
 #pragma unroll
           for (int m = 0; m < 4; ++m)
@@ -616,18 +799,7 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
             }
         }
       } else {
-#pragma unroll 4
-        for (int i = 0; i < DK; ++i) {
-          float a[4], b[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) a[m] = sQ[(ty + 16 * m) * LDK + i];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) b[c] = sK[(tx + 16 * c) * LDK + i];
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(a[m], b[c], acc[m][c]);
-        }
+        gemm_nt<4, 4>(acc, sQ, LDK, sK, LDK, DK);
       }
 #pragma unroll
       for (int m = 0; m < 4; ++m)
@@ -643,79 +815,47 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
     // K <- K exp(G_L - G), Q <- Q exp(G)
     for (int idx = tid; idx < kC * DK; idx += kBwdThreads) {
       const int u = idx / DK, i = idx - u * DK;
-      const float gl = VEC ? sG[(n - 1) * LDK + i] : sG[n - 1];
-      const float gu = VEC ? sG[u * LDK + i] : sG[u];
+      const float gl = VEC ? sG[(n - 1) * GW + i] : sG[n - 1];
+      const float gu = VEC ? sG[u * GW + i] : sG[u];
       sK[u * LDK + i] *= exp2f(gl - gu);
       sQ[u * LDK + i] *= exp2f(gu);
     }
     __syncthreads();
 
-    // dv[t][j] = scale sum_u M[u][t] dO[u][j] + sum_i Kd[t][i] R[i][j]
+    // dv[t][j] = scale sum_u M[u][t] dO[u][j] + sum_i Kd[t][i] R[i][j]:
+    // rows t = 4 ty + m, columns j = 4 tx + c
     {
       float acc[4][4] = {};
-#pragma unroll 4
-      for (int u = 0; u < kC; ++u) {
-        float a[4], b[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) a[m] = sM[u * kLDP + ty + 16 * m];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b[c] = sDO[u * kJS + tx + 16 * c];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(a[m], b[c], acc[m][c]);
-      }
+      gemm_tn<4, 4>(acc, sM, kLDP, sDO, kJS, kC);
 #pragma unroll
       for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[m][c] *= scale;
-#pragma unroll 4
-      for (int i = 0; i < DK; ++i) {
-        float a[4], b[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) a[m] = sK[(ty + 16 * m) * LDK + i];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b[c] = sR[i * kJS + tx + 16 * c];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(a[m], b[c], acc[m][c]);
-      }
+      gemm_nn4<4, 4>(acc, sK, LDK, sR, kJS, DK);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int t = ty + 16 * m;
+        const int t = 4 * ty + m;
         if (t < n) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            store_grad(dv_out, ((base + t) * H + h) * (long long)DV + j0 + tx + 16 * c,
+            store_grad(dv_out, ((base + t) * H + h) * (long long)DV + j0 + 4 * tx + c,
                        acc[m][c], out_f32);
         }
       }
     }
     __syncthreads();
 
-    // R <- diag(exp G_L) R + scale (Q exp(G))^T dO: rows i = ty + 16 r
+    // R <- diag(exp G_L) R + scale (Q exp(G))^T dO: rows i = TR ty + r, columns 4 tx + c
     {
       float acc[TR][4] = {};
-#pragma unroll 4
-      for (int u = 0; u < kC; ++u) {
-        float a[TR], b[4];
-#pragma unroll
-        for (int r = 0; r < TR; ++r) a[r] = sQ[u * LDK + ty + 16 * r];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b[c] = sDO[u * kJS + tx + 16 * c];
-#pragma unroll
-        for (int r = 0; r < TR; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-      }
+      gemm_tn<TR, 4>(acc, sQ, LDK, sDO, kJS, kC);
 #pragma unroll
       for (int r = 0; r < TR; ++r) {
-        const int i = ty + 16 * r;
-        const float el = exp2f(VEC ? sG[(n - 1) * LDK + i] : sG[n - 1]);
+        const int i = TR * ty + r;
+        const float el = exp2f(VEC ? sG[(n - 1) * GW + i] : sG[n - 1]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float* p = sR + i * kJS + tx + 16 * c;
+          float* p = sR + i * kJS + 4 * tx + c;
           *p = fmaf(el, *p, scale * acc[r][c]);
         }
       }
