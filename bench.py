@@ -17,6 +17,11 @@ rotated so no step reads its inputs from L2; the decode state alone is 1.34 GB.
 prefill call) achieved HBM bandwidth against the measured copy bandwidth;
 ``prefill.roofline`` is the prefill kernel's.
 
+After the step (outside its time), side measurements are added to the line:
+the other prefill workloads, decode-width graph buckets, the mixer epilogue,
+and ``backward`` -- the chunked backward (gla_chunk_bwd) on the prefill
+workload's sizes, with its roofline against the CUDA cores' fp32 FMA peak.
+
 ``--impl reference`` times the fp64 CPU oracle (the reference for parity, a
 deliberately plain program) on a bounded sample of the same workload.
 
@@ -70,6 +75,31 @@ def prefill_flops(w, B, T, rows=None) -> int:
     per token and head 2 * (C * (dk + dv) + 2 * dk * dv)."""
     rows = B * T if rows is None else rows
     return 2 * (w.chunk * (w.dk + w.dv) + 2 * w.dk * w.dv) * rows * w.H
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops per FMA at
+# the maximum SM clock (2070 MHz); the backward is bound by these units.
+FP32_LANES = 152 * 128
+SM_MAX_MHZ = 2070.0
+
+
+def fp32_peak_tflops(sm_mhz: float = SM_MAX_MHZ) -> float:
+    return FP32_LANES * 2 * sm_mhz * 1e6 / 1e12
+
+
+BWD_CHUNK = 64
+
+
+def backward_flops(w, B, T) -> int:
+    """Algorithmic flops of the chunked backward (chunks of 64, the causal
+    triangles counted as halves): per token and head, the five C x C x d
+    products dO V^T, P K, P^T Q, Q K^T, M^T dO at C/2 MACs per output column
+    each -- (C/2)(2 dv + 3 dk) -- plus the three inter-chunk readouts (dq, dk, dv)
+    and the two state steps (S forward, the carried gradient backward), dk dv
+    MACs each: 2 flops per MAC."""
+    c = BWD_CHUNK
+    macs = (c // 2) * (2 * w.dv + 3 * w.dk) + 5 * w.dk * w.dv
+    return 2 * macs * B * T * w.H
 
 
 def decode_bytes(w) -> int:
@@ -390,6 +420,47 @@ def time_mixer(gla, dev, hbm, reps=20, warmup=3):
     return res
 
 
+def time_backward(gla, dev, reps=5, warmup=3):
+    """The chunked backward (gla_chunk_bwd: dq, dk, dv, dg, d_init) on the
+    prefill workload's sizes, for the per-head gate and for the per-key-channel
+    gate; timed alone with CUDA events on the launching stream."""
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = []
+    w0 = gla_inputs.WORKLOADS["prefill"]
+    for gate, over in (("per-head", {}), ("per-key-channel",
+                                          dict(gate="vector", g_mu=2.0, g_div=4.0))):
+        w = gla_inputs.dataclasses.replace(w0, **over)
+        x = gla_inputs.prefill_inputs(w)
+        gr = gla_inputs.grad_inputs(x)
+        args = [x[n].to(dev) for n in ("q", "k", "v", "g")] + [gr["d_out"].to(dev)]
+        kw = dict(scale=x["scale"], init_state=x["init_state"].to(dev),
+                  d_final_state=gr["d_final_state"].to(dev))
+        for _ in range(warmup):
+            gla.chunk_bwd(*args, **kw)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            gla.chunk_bwd(*args, **kw)
+        b.record(stream)
+        torch.cuda.synchronize()
+        gla.status_sync()
+        ms = a.elapsed_time(b) / reps
+        flops = backward_flops(w, w.B, w.T)
+        peak = fp32_peak_tflops()
+        res.append({
+            "workload": f"chunked backward, {gate} gate, B={w.B} T={w.T} H={w.H} "
+                        f"dk=dv={w.dk}, bf16 q/k/v/d_out, bf16 gradients, fp32 dg and d_init",
+            "ms": ms, "tokens_per_s": w.B * w.T / (ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12,
+                         "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / (ms / 1e3) / 1e12 / peak,
+                         "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
+                         "algorithmic_flops": flops},
+            "launches": 4 if gate == "per-key-channel" else 5})
+    return res
+
+
 def run_gla(args, world, rank, local):
     import gated_linear_attention_gla_gb300 as gla
     from gated_linear_attention_gla_gb300 import build as glabuild
@@ -588,6 +659,7 @@ def run_gla(args, world, rank, local):
         line["prefill_workloads"] = time_side_workloads(gla, dev, hbm, peak_kind)
         line["decode_graphs"] = [time_decode_graphs(gla, dev, width=n) for n in (8, 64)]
         line["mixer"] = time_mixer(gla, dev, hbm)
+        line["backward"] = time_backward(gla, dev)
     if world == 1 and not args.no_cpu_baseline:
         pre_cpu, dec_cpu = cpu_baseline(args.cpu_budget)
         line["cpu_baseline"] = pre_cpu
@@ -604,7 +676,18 @@ def run_profile_case(args):
     glabuild.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.profile in ("prefill", "vector", "varlen"):
+    if args.profile == "backward":
+        w = gla_inputs.WORKLOADS["prefill"]
+        x = gla_inputs.prefill_inputs(w)
+        gr = gla_inputs.grad_inputs(x)
+        bargs = [x[n].to(dev) for n in ("q", "k", "v", "g")] + [gr["d_out"].to(dev)]
+        bkw = dict(scale=x["scale"], init_state=x["init_state"].to(dev),
+                   d_final_state=gr["d_final_state"].to(dev))
+
+        def call():
+            gla.chunk_bwd(*bargs, **bkw)
+        nbytes = 0
+    elif args.profile in ("prefill", "vector", "varlen"):
         w = gla_inputs.WORKLOADS[args.profile]
         x = gla_inputs.prefill_inputs(w)
         q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))
@@ -690,7 +773,8 @@ def main(argv=None):
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-side-workloads", action="store_true",
                     help="skip timing the vector-gate and varlen prefill workloads")
-    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode", "backward"],
+                    default=None,
                     help="run one kernel alone (for ncu captures) instead of the bench")
     ap.add_argument("--decode-n", type=int, default=1280,
                     help="sequences for --profile decode")

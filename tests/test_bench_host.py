@@ -129,3 +129,12 @@ def test_decode_bucket_choice():
         pick_bucket(b, 13)
     with pytest.raises(ValueError):
         default_buckets(0)
+
+
+def test_backward_flops_and_fp32_peak():
+    import bench
+    w = gla_inputs.WORKLOADS["prefill"]
+    # per token and head: 32 * (2 * 128 + 3 * 128) + 5 * 128 * 128 MACs
+    per = 32 * 640 + 5 * 16384
+    assert bench.backward_flops(w, w.B, w.T) == 2 * per * w.B * w.T * w.H
+    assert abs(bench.fp32_peak_tflops() - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
