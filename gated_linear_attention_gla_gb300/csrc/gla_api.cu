@@ -341,8 +341,8 @@ gla_status gla_mixer_epilogue(void* out, const void* q, const void* k, const voi
   const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
   const bool f32out = fp32 || (flags & GLA_FLAG_FP32_OUT) != 0;
   const size_t esz = fp32 ? 4 : 2, osz = f32out ? 4 : 2;
-  if (!aligned(out, osz) || !aligned(q, esz) || !aligned(k, esz) || !aligned(v, esz) ||
-      !aligned(z, esz) || !aligned(aug, 4) || !aligned(norm_w, 4))
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(z, 16) || !aligned(aug, 16) || !aligned(norm_w, 16))
     return GLA_ERR_MISALIGNED;
   const size_t out_b = (size_t)(units * dv) * osz;
   const size_t qk_b = aug ? (size_t)(units * dk) * esz : 0;

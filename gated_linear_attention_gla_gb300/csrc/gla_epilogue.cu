@@ -7,8 +7,10 @@
 //     o  = o / sqrt(mean_j o_j^2 + eps) * w[h]        (head RMSNorm)
 //     o *= silu(z)                                    (output gate)
 // each step optional.  One warp per (token, head): the two dot products are
-// warp reductions, every lane owns dv / 32 columns.  A pure stream over o, q,
-// k, v and z (HBM-bound); the decode kernel fuses the same steps instead.
+// warp reductions, every lane owns dv / 32 adjacent columns (and dk / 32 key
+// channels), so each tensor is read as one contiguous span per warp.  A pure
+// stream over o, q, k, v and z (HBM-bound); the decode kernel fuses the same
+// steps instead.
 #include "gla_internal.cuh"
 
 namespace gla {
@@ -22,48 +24,115 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// N consecutive elements as fp32: 16-, 8- or 4-byte loads for even N (the
+// caller's tensors are 16-byte aligned and every run starts on a multiple of
+// its own size), element loads for odd N.
+template <int N, typename T>
+__device__ __forceinline__ void load_run(const T* __restrict__ p, float (&x)[N]) {
+  if constexpr (N % 2 != 0) {  // odd runs (dk = 96: three channels a lane)
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = to_f32(__ldg(p + i));
+  } else if constexpr (sizeof(T) == 4) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < N; i += 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
+        x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; i += 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(p + i));
+        x[i] = v.x; x[i + 1] = v.y;
+      }
+    }
+  } else {  // bf16: pairs in 32-bit words
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < N; i += 4) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + i));
+        x[i] = __uint_as_float(v.x << 16);
+        x[i + 1] = __uint_as_float(v.x & 0xffff0000u);
+        x[i + 2] = __uint_as_float(v.y << 16);
+        x[i + 3] = __uint_as_float(v.y & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; i += 2) {
+        const unsigned v = __ldg(reinterpret_cast<const unsigned*>(p + i));
+        x[i] = __uint_as_float(v << 16);
+        x[i + 1] = __uint_as_float(v & 0xffff0000u);
+      }
+    }
+  }
+}
+
+template <int N, typename T>
+__device__ __forceinline__ void store_run(T* __restrict__ p, const float (&x)[N]) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2)
+      *reinterpret_cast<float2*>(p + i) = make_float2(x[i], x[i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(x[i], x[i + 1]);
+      *reinterpret_cast<__nv_bfloat162*>(p + i) = b;
+    }
+  }
+}
+
+// One warp per (row, head): lane l owns the dv / 32 adjacent columns from
+// l * dv / 32 and the dk / 32 adjacent key channels from l * dk / 32, read and
+// written as runs (every access of the warp is one contiguous span).
 template <typename IO, typename OUT, int DK, int DV>
 __global__ void __launch_bounds__(kEpiWarps * 32)
 epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __restrict__ k,
                 const IO* __restrict__ v, const float* __restrict__ aug,
                 const float* __restrict__ norm_w, float eps, const IO* __restrict__ z,
                 long long units, int H) {
-  constexpr int PER = DV / 32;  // columns per lane
+  constexpr int PER = DV / 32;   // columns per lane
+  constexpr int PK = DK / 32;    // key channels per lane
   const int lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * kEpiWarps + (threadIdx.x >> 5);  // row * H + h
   if (unit >= units) return;
   const int h = (int)(unit % H);
+  const long long ob = unit * DV + lane * PER;
   float o[PER];
-#pragma unroll
-  for (int c = 0; c < PER; ++c) o[c] = to_f32(out[unit * DV + lane + 32 * c]);
+  load_run<PER>(out + ob, o);
   if (aug != nullptr) {
+    const long long kb = unit * DK + lane * PK;
+    float qv[PK], kv[PK], av[PK], vv[PER];
+    load_run<PK>(q + kb, qv);
+    load_run<PK>(k + kb, kv);
+    load_run<PK>(aug + h * DK + lane * PK, av);
+    load_run<PER>(v + ob, vv);
     float s = 0.f;
 #pragma unroll
-    for (int i = lane; i < DK; i += 32)
-      s += to_f32(q[unit * DK + i]) * __ldg(aug + h * DK + i) * to_f32(k[unit * DK + i]);
+    for (int i = 0; i < PK; ++i) s = fmaf(qv[i] * av[i], kv[i], s);
     s = warp_sum(s);
     const float gate = 1.f / (1.f + expf(-s));
 #pragma unroll
-    for (int c = 0; c < PER; ++c) o[c] = fmaf(gate, to_f32(v[unit * DV + lane + 32 * c]), o[c]);
+    for (int c = 0; c < PER; ++c) o[c] = fmaf(gate, vv[c], o[c]);
   }
   if (norm_w != nullptr) {
     float ss = 0.f;
 #pragma unroll
-    for (int c = 0; c < PER; ++c) ss += o[c] * o[c];
+    for (int c = 0; c < PER; ++c) ss = fmaf(o[c], o[c], ss);
     ss = warp_sum(ss);
     const float r = rsqrtf(ss / DV + eps);
+    float w[PER];
+    load_run<PER>(norm_w + h * DV + lane * PER, w);
 #pragma unroll
-    for (int c = 0; c < PER; ++c) o[c] *= r * __ldg(norm_w + h * DV + lane + 32 * c);
+    for (int c = 0; c < PER; ++c) o[c] *= r * w[c];
   }
   if (z != nullptr) {
+    float zz[PER];
+    load_run<PER>(z + ob, zz);
 #pragma unroll
-    for (int c = 0; c < PER; ++c) {
-      const float zz = to_f32(z[unit * DV + lane + 32 * c]);
-      o[c] *= zz / (1.f + expf(-zz));
-    }
+    for (int c = 0; c < PER; ++c) o[c] *= zz[c] / (1.f + expf(-zz[c]));
   }
-#pragma unroll
-  for (int c = 0; c < PER; ++c) out[unit * DV + lane + 32 * c] = from_f32<OUT>(o[c]);
+  store_run<PER>(out + ob, o);
 }
 
 template <typename IO, typename OUT, int DK>

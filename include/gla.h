@@ -193,7 +193,7 @@ gla_status gla_decode_step_slots(const void *q, const void *k, const void *v, co
  *   z            [rows, H, dv], q's dtype, or NULL
  *   rows, H      token rows and heads (>= 0); dk, dv as gla_chunk_fwd
  *   flags        GLA_FLAG_FP32_IO, GLA_FLAG_FP32_OUT only
- * Alignment: element alignment.  out must not overlap any input.
+ * Alignment: every pointer 16-byte aligned.  out must not overlap any input.
  */
 gla_status gla_mixer_epilogue(void *out, const void *q, const void *k, const void *v,
                               const float *aug, const float *norm_w, float eps, const void *z,
