@@ -90,16 +90,25 @@ def fp32_peak_tflops(sm_mhz: float = SM_MAX_MHZ) -> float:
 BWD_CHUNK = 64
 
 
-def backward_flops(w, B, T) -> int:
-    """Algorithmic flops of the chunked backward (chunks of 64, the causal
-    triangles counted as halves): per token and head, the five C x C x d
-    products dO V^T, P K, P^T Q, Q K^T, M^T dO at C/2 MACs per output column
-    each -- (C/2)(2 dv + 3 dk) -- plus the three inter-chunk readouts (dq, dk, dv)
-    and the two state steps (S forward, the carried gradient backward), dk dv
-    MACs each: 2 flops per MAC."""
-    c = BWD_CHUNK
-    macs = (c // 2) * (2 * w.dv + 3 * w.dk) + 5 * w.dk * w.dv
+def backward_flops(w, B, T, chunk=BWD_CHUNK) -> int:
+    """Algorithmic flops of the chunked backward (the causal triangles counted
+    as halves): per token and head, the five C x C x d products dO V^T, P K,
+    P^T Q, Q K^T, M^T dO at C/2 MACs per output column each -- (C/2)(2 dv + 3 dk)
+    -- plus the three inter-chunk readouts (dq, dk, dv) and the two state steps
+    (S forward, the carried gradient backward), dk dv MACs each: 2 flops per
+    MAC.  Chunks of 64 on the CUDA cores, 128 on the tensor cores."""
+    macs = (chunk // 2) * (2 * w.dv + 3 * w.dk) + 5 * w.dk * w.dv
     return 2 * macs * B * T * w.H
+
+
+def backward_bytes(w, B, T) -> int:
+    """Algorithmic HBM bytes of one backward call: read q, k, v, d_out (bf16)
+    and g (fp32), the initial state and the final state's gradient (fp32);
+    write dq, dk, dv (bf16), dg (fp32) and the initial state's gradient."""
+    tok = B * T * w.H
+    g_per = w.dk if w.gate == "vector" else 1
+    io = tok * (2 * (2 * w.dk + 2 * w.dv) + 4 * g_per + 2 * (2 * w.dk + w.dv) + 4 * g_per)
+    return io + 3 * 4 * B * w.H * w.dk * w.dv
 
 
 def decode_bytes(w) -> int:
@@ -428,14 +437,20 @@ def time_backward(gla, dev, reps=5, warmup=3):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     res = []
     w0 = gla_inputs.WORKLOADS["prefill"]
-    for gate, over in (("per-head", {}), ("per-key-channel",
-                                          dict(gate="vector", g_mu=2.0, g_div=4.0))):
+    hbm, bf16_peak, _, kind = peaks()
+    from gated_linear_attention_gla_gb300 import _binding
+    for gate, over, tc in (("per-head", {}, True), ("per-head", {}, False),
+                           ("per-key-channel", dict(gate="vector", g_mu=2.0, g_div=4.0), False)):
         w = gla_inputs.dataclasses.replace(w0, **over)
         x = gla_inputs.prefill_inputs(w)
         gr = gla_inputs.grad_inputs(x)
         args = [x[n].to(dev) for n in ("q", "k", "v", "g")] + [gr["d_out"].to(dev)]
+        ws = None
+        if tc:
+            n = _binding.chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, False, 0)
+            ws = torch.empty(n, dtype=torch.uint8, device=dev)
         kw = dict(scale=x["scale"], init_state=x["init_state"].to(dev),
-                  d_final_state=gr["d_final_state"].to(dev))
+                  d_final_state=gr["d_final_state"].to(dev), tensor_cores=tc, workspace=ws)
         for _ in range(warmup):
             gla.chunk_bwd(*args, **kw)
         torch.cuda.synchronize()
@@ -446,18 +461,33 @@ def time_backward(gla, dev, reps=5, warmup=3):
         torch.cuda.synchronize()
         gla.status_sync()
         ms = a.elapsed_time(b) / reps
-        flops = backward_flops(w, w.B, w.T)
-        peak = fp32_peak_tflops()
-        res.append({
+        sec = ms / 1e3
+        entry = {
             "workload": f"chunked backward, {gate} gate, B={w.B} T={w.T} H={w.H} "
                         f"dk=dv={w.dk}, bf16 q/k/v/d_out, bf16 gradients, fp32 dg and d_init",
-            "ms": ms, "tokens_per_s": w.B * w.T / (ms / 1e3),
-            "roofline": {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12,
-                         "peak": peak, "unit": "TFLOP/s",
-                         "frac": flops / (ms / 1e3) / 1e12 / peak,
-                         "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
-                         "algorithmic_flops": flops},
-            "launches": 4 if gate == "per-key-channel" else 5})
+            "path": "tensor cores (3 prefill runs)" if tc else "CUDA cores (fp32)",
+            "ms": ms, "tokens_per_s": w.B * w.T / sec}
+        if tc:
+            nbytes = backward_bytes(w, w.B, w.T)
+            flops = backward_flops(w, w.B, w.T, chunk=128)
+            entry["roofline"] = {
+                "bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": nbytes / sec / 1e9 / hbm, "peak_kind": kind,
+                "algorithmic_bytes": nbytes,
+                "tensor": {"achieved_tflops": flops / sec / 1e12, "peak_tflops": bf16_peak,
+                           "frac": flops / sec / 1e12 / bf16_peak, "algorithmic_flops": flops},
+                "workspace_bytes": ws.numel()}
+            entry["launches"] = 6
+        else:
+            flops = backward_flops(w, w.B, w.T)
+            peak = fp32_peak_tflops()
+            entry["roofline"] = {
+                "bound": "alu", "achieved": flops / sec / 1e12, "peak": peak,
+                "unit": "TFLOP/s", "frac": flops / sec / 1e12 / peak,
+                "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
+                "algorithmic_flops": flops}
+            entry["launches"] = 4 if gate == "per-key-channel" else 5
+        res.append(entry)
     return res
 
 
@@ -676,13 +706,14 @@ def run_profile_case(args):
     glabuild.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.profile == "backward":
+    if args.profile in ("backward", "backward-tc"):
         w = gla_inputs.WORKLOADS["prefill"]
         x = gla_inputs.prefill_inputs(w)
         gr = gla_inputs.grad_inputs(x)
         bargs = [x[n].to(dev) for n in ("q", "k", "v", "g")] + [gr["d_out"].to(dev)]
         bkw = dict(scale=x["scale"], init_state=x["init_state"].to(dev),
-                   d_final_state=gr["d_final_state"].to(dev))
+                   d_final_state=gr["d_final_state"].to(dev),
+                   tensor_cores=args.profile == "backward-tc")
 
         def call():
             gla.chunk_bwd(*bargs, **bkw)
@@ -773,7 +804,8 @@ def main(argv=None):
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-side-workloads", action="store_true",
                     help="skip timing the vector-gate and varlen prefill workloads")
-    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode", "backward"],
+    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode", "backward",
+                                          "backward-tc"],
                     default=None,
                     help="run one kernel alone (for ncu captures) instead of the bench")
     ap.add_argument("--decode-n", type=int, default=1280,

@@ -172,11 +172,23 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   return cuda_status(err);
 }
 
+size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int packed,
+                                    unsigned flags) {
+  if (!flags_ok(flags) || B <= 0 || H <= 0 || T < 0) return 0;
+  const bool fp32 = (flags & GLA_FLAG_FP32_IO) != 0;
+  const bool vec = (flags & GLA_FLAG_VECTOR_GATE) != 0;
+  if (!gla::chunk_bwd_tc_supported(dk, dv, fp32, vec)) return 0;
+  const long long rows = packed ? (long long)T : (long long)B * T;
+  if (rows * H * dk > kMaxElems) return 0;
+  return gla::chunk_bwd_tc_workspace(B, H, rows);
+}
+
 gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                          float scale, const float* init_state, const void* d_out,
                          const float* d_final_state, void* dq, void* dk_out, void* dv_out,
                          float* dg, float* d_init_state, const int32_t* cu_seqlens, int B,
-                         int H, int T, int dk, int dv, gla_stream_t stream, unsigned flags) {
+                         int H, int T, int dk, int dv, void* workspace, size_t workspace_bytes,
+                         gla_stream_t stream, unsigned flags) {
   if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
     return GLA_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
@@ -197,7 +209,8 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const floa
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(d_out, 16) ||
       !aligned(dq, 16) || !aligned(dk_out, 16) || !aligned(dv_out, 16) ||
       !aligned(init_state, 16) || !aligned(d_final_state, 16) || !aligned(d_init_state, 16) ||
-      !aligned(dg, 16) || !aligned(g, vec ? 16 : 4) || !aligned(cu_seqlens, 4))
+      !aligned(dg, 16) || !aligned(g, vec ? 16 : 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(workspace, 256))
     return GLA_ERR_MISALIGNED;
   // every output is disjoint from every input and from the other outputs
   const size_t qk_b = (size_t)(qk_elems * esz), v_b = (size_t)(v_elems * esz);
@@ -207,12 +220,16 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const floa
   const void* in_p[] = {q, k, v, g, d_out, init_state, d_final_state, cu_seqlens};
   const size_t in_b[] = {qk_b, qk_b, v_b, g_b, v_b, st_b, st_b,
                          cu_seqlens ? (size_t)(B + 1) * 4 : 0};
-  const void* out_p[] = {dq, dk_out, dv_out, dg, d_init_state};
-  const size_t out_b[] = {dqk_b, dqk_b, dv_b, g_b, st_b};
-  for (int o = 0; o < 5; ++o) {
+  // the tensor-core path runs when it covers the call and the workspace is large enough
+  const size_t ws_need =
+      gla::chunk_bwd_tc_supported(dk, dv, fp32, vec) ? gla::chunk_bwd_tc_workspace(B, H, rows) : 0;
+  const bool use_tc = rows > 0 && ws_need > 0 && workspace != nullptr && workspace_bytes >= ws_need;
+  const void* out_p[] = {dq, dk_out, dv_out, dg, d_init_state, use_tc ? workspace : nullptr};
+  const size_t out_b[] = {dqk_b, dqk_b, dv_b, g_b, st_b, ws_need};
+  for (int o = 0; o < 6; ++o) {
     for (int i = 0; i < 8; ++i)
       if (overlap(out_p[o], out_b[o], in_p[i], in_b[i])) return GLA_ERR_INVALID_ARG;
-    for (int o2 = o + 1; o2 < 5; ++o2)
+    for (int o2 = o + 1; o2 < 6; ++o2)
       if (overlap(out_p[o], out_b[o], out_p[o2], out_b[o2])) return GLA_ERR_INVALID_ARG;
   }
   if (rows == 0 && d_init_state == nullptr) return GLA_OK;
@@ -227,7 +244,9 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const floa
   a.B = B; a.H = H; a.T = T; a.dk_size = dk; a.dv_size = dv;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec; a.status = status;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (vec)
+  if (use_tc)
+    err = gla::launch_chunk_bwd_tc(a, workspace, s);
+  else if (vec)
     err = fp32 ? gla::launch_chunk_bwd_chan_f32(a, s) : gla::launch_chunk_bwd_chan_bf16(a, s);
   else
     err = fp32 ? gla::launch_chunk_bwd_head_f32(a, s) : gla::launch_chunk_bwd_head_bf16(a, s);

@@ -1,0 +1,354 @@
+// gla_chunk_bwd_tc.cu -- the backward for the per-head gate on the tensor
+// cores: three runs of the tcgen05 prefill kernel.
+//
+// Method: reverse mode through the recurrence of the "i14 Laplace 3B on AWS
+// Trainium2" page (paragraph "GLA mixer"), chunked as in its section
+// "Challenge 1".  The gradient of a linear recurrence is the same kind of
+// recurrence with the roles of its operands exchanged (fp64 check: 1e-15):
+//   dq:  S^T_t = e^{g_t} S^T_{t-1} + v_t^T k_t,  dq_t = scale do_t S^T_t
+//        -- the prefill with (q, k, v) = (do, v, k) and initial state S_0^T;
+//        its final state is S_T^T.
+//   dk, dv: with Sbar_t = dL/dS_t = scale q_t^T do_t + e^{g_{t+1}} Sbar_{t+1},
+//        R_t = Sbar_t / scale obeys the prefill recurrence backwards in time,
+//        with key q, value do, initial state dS_T / scale and, at reversed
+//        position tau, the gate of the following token (g_{len - tau}; 0 at
+//        tau = 0).  Then dk_t = scale v_t R_t^T -- the prefill with (q, k, v) =
+//        (v, do, q) on the reversed sequence, state R^T -- and dv_t = scale
+//        k_t R_t -- the prefill with (q, k, v) = (k, q, do), state R, whose
+//        final state is R_0, so d_init = scale e^{g_0} R_0.
+//   dg:  dg_t = sum_{u >= t} sum_i (q_u[i] dq_u[i] - k_u[i] dk_u[i])
+//               + sum_ij S_T[i][j] dS_T[i][j].
+// The prefill kernel reads tokens in order, so a prepare pass writes the
+// reversed (and gate-shifted) copies into the caller's workspace, the three
+// prefill runs store fp32 results there, and a finish pass puts dk and dv back
+// in token order, rounds every gradient to its output dtype and forms the dg
+// terms from the fp32 values; the suffix sums reuse the CUDA-core backward's
+// scan kernel.  Launches: prepare, 3 x prefill, finish, and the scan when dg
+// is wanted.
+#include "gla_chunk_bwd.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kBlocksPerPair = 32;  // CTAs per (sequence, head) for the copy passes
+constexpr int kTcDK = 128, kTcDV = 128;
+
+__device__ __forceinline__ void pair_and_block(int H, int* s, int* h, int* blk) {
+  const int pair = blockIdx.x / kBlocksPerPair;
+  *blk = blockIdx.x % kBlocksPerPair;
+  *s = pair / H;
+  *h = pair % H;
+}
+
+// tokens [t0, t1) of a sequence of len tokens for copy block blk
+__device__ __forceinline__ void block_range(int len, int blk, int* t0, int* t1) {
+  const int per = (len + kBlocksPerPair - 1) / kBlocksPerPair;
+  *t0 = min(len, blk * per);
+  *t1 = min(len, *t0 + per);
+}
+
+// Reversed copies of q, k, v, do (token t of a sequence to position len-1-t),
+// the gate shifted by one token (position tau holds g of natural token
+// len - tau, position 0 holds 0), S_0^T, dS_T / scale and its transpose.
+__global__ void __launch_bounds__(kCopyThreads)
+bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ d_out,
+                   const float* __restrict__ g, float inv_scale,
+                   const float* __restrict__ init_state, const float* __restrict__ d_final,
+                   __nv_bfloat16* __restrict__ rq, __nv_bfloat16* __restrict__ rk,
+                   __nv_bfloat16* __restrict__ rv, __nv_bfloat16* __restrict__ rdo,
+                   float* __restrict__ rg, float* __restrict__ s0t, float* __restrict__ dfs,
+                   float* __restrict__ dfst, const int32_t* __restrict__ cu, int B, int H,
+                   int T, unsigned* status) {
+  int s, h, blk;
+  pair_and_block(H, &s, &h, &blk);
+  long long start;
+  int len;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
+  int t0, t1;
+  block_range(len, blk, &t0, &t1);
+  // 16-byte vectors: a token's q and k rows (16 each at d = 128), then its v
+  // and do rows; eight vectors a thread in flight at a time
+  constexpr int VK = kTcDK / 8, VV = kTcDV / 8;
+  constexpr int VPT = 2 * VK + 2 * VV;
+  constexpr int kBatch = 8;
+  static_assert(VK == VV, "one row width");
+  auto src_of = [&](int w) { return w == 0 ? q : w == 1 ? k : w == 2 ? v : d_out; };
+  auto dst_of = [&](int w) { return w == 0 ? rq : w == 1 ? rk : w == 2 ? rv : rdo; };
+  const int nvec = (t1 - t0) * VPT;
+  for (int base = threadIdx.x; base < nvec; base += kCopyThreads * kBatch) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / VPT, c = idx % VPT;
+        const long long src = (start + t) * H + h;
+        r[b] = __ldg(reinterpret_cast<const uint4*>(src_of(c / VK) + src * kTcDK) + c % VK);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / VPT, c = idx % VPT;
+        const long long dst = (start + (len - 1 - t)) * H + h;
+        reinterpret_cast<uint4*>(dst_of(c / VK) + dst * kTcDK)[c % VK] = r[b];
+      }
+    }
+  }
+  for (int t = t0 + threadIdx.x; t < t1; t += kCopyThreads)
+    rg[(start + (len - 1 - t)) * H + h] = t + 1 < len ? __ldg(g + (start + t + 1) * H + h) : 0.f;
+  // the states: 32 x 32 tiles spread over the blocks of the pair, transposed through
+  // shared memory so that reads and writes are both row-contiguous
+  __shared__ float tile[2][32][33];
+  const size_t off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
+  constexpr int kTiles = (kTcDK / 32) * (kTcDV / 32);
+  for (int tt = blk; tt < kTiles; tt += kBlocksPerPair) {
+    const int ti = (tt / (kTcDV / 32)) * 32, tj = (tt % (kTcDV / 32)) * 32;
+    const int r = threadIdx.x / 32, c = threadIdx.x % 32;  // 8 rows of 32 per pass
+    __syncthreads();
+    for (int rr = r; rr < 32; rr += kCopyThreads / 32) {
+      const size_t e = off + (size_t)(ti + rr) * kTcDV + tj + c;
+      tile[0][rr][c] = init_state ? __ldg(init_state + e) : 0.f;
+      if (d_final) {
+        const float x = __ldg(d_final + e) * inv_scale;
+        dfs[e] = x;
+        tile[1][rr][c] = x;
+      }
+    }
+    __syncthreads();
+    for (int rr = r; rr < 32; rr += kCopyThreads / 32) {
+      const size_t e = off + (size_t)(tj + rr) * kTcDK + ti + c;  // row j, column i
+      if (init_state) s0t[e] = tile[0][c][rr];
+      if (d_final) dfst[e] = tile[1][c][rr];
+    }
+  }
+}
+
+// Four fp32 values as elements 4 lane .. 4 lane + 3 of the row at `base`, in
+// fp32 or rounded to bf16.
+__device__ __forceinline__ void store_row4(void* out, long long base, int lane, float4 x,
+                                           bool f32) {
+  if (f32) {
+    reinterpret_cast<float4*>(static_cast<float*>(out) + base)[lane] = x;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + base)[lane] =
+        make_uint2(*reinterpret_cast<const unsigned*>(&lo), *reinterpret_cast<const unsigned*>(&hi));
+  }
+}
+
+__device__ __forceinline__ float warp_sum32(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Gradients in token order and output dtype, the per-token dg terms (q.dq -
+// k.dk, plus the final-state term at the last token), and d_init's factor
+// scale * e^{g_0}.  One warp per token; lane l owns channels 4 l .. 4 l + 3.
+__global__ void __launch_bounds__(kCopyThreads, 2)
+bwd_tc_fin_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                  const float* __restrict__ g, float scale, const float* __restrict__ dq32,
+                  const float* __restrict__ rdk32, const float* __restrict__ rdv32,
+                  const float* __restrict__ stt, const float* __restrict__ dfst,
+                  void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
+                  bool out_f32, float* __restrict__ dg, float* __restrict__ d_init,
+                  const int32_t* __restrict__ cu, int B, int H, int T, unsigned* status) {
+  static_assert(kTcDK == 128 && kTcDV == 128, "four channels a lane");
+  __shared__ float red[kCopyThreads / 32];
+  int s, h, blk;
+  pair_and_block(H, &s, &h, &blk);
+  long long start;
+  int len;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
+  int t0, t1;
+  block_range(len, blk, &t0, &t1);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t st_off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
+
+  // the final-state term sum_ij S_T[i][j] dS_T[i][j] = scale sum_e S_T^T[e]
+  // (dS_T / scale)^T[e] -- both transposed copies in the workspace, read in
+  // order -- by the block holding the last token
+  float c_t = 0.f;
+  if (dg && dfst && stt && len > 0 && t0 <= len - 1 && len - 1 < t1) {
+    float acc = 0.f;
+    for (int e = threadIdx.x; e < kTcDK * kTcDV / 4; e += kCopyThreads) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(stt + st_off) + e);
+      const float4 y = __ldg(reinterpret_cast<const float4*>(dfst + st_off) + e);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+    }
+    acc = warp_sum32(acc);
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    for (int w = 0; w < kCopyThreads / 32; ++w) c_t += red[w];
+    c_t *= scale;
+  }
+
+  // eight tokens per warp and pass, their loads issued together
+  constexpr int kTok = 8;
+  constexpr int kWarps = kCopyThreads / 32;
+  for (int tb = t0 + kTok * warp; tb < t1; tb += kTok * kWarps) {
+    float4 av[kTok], bv[kTok];
+    uint2 qv[kTok], kv[kTok];
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int t = min(tb + u, t1 - 1);
+      const long long row = (start + t) * H + h;
+      const long long rrow = (start + (len - 1 - t)) * H + h;
+      av[u] = __ldg(reinterpret_cast<const float4*>(dq32 + row * kTcDK) + lane);
+      bv[u] = __ldg(reinterpret_cast<const float4*>(rdk32 + rrow * kTcDK) + lane);
+      if (dg) {
+        qv[u] = __ldg(reinterpret_cast<const uint2*>(q + row * kTcDK) + lane);
+        kv[u] = __ldg(reinterpret_cast<const uint2*>(k + row * kTcDK) + lane);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int t = tb + u;
+      if (t >= t1) break;  // warp-uniform
+      const long long row = (start + t) * H + h;
+      const float4 a = av[u], b = bv[u];
+      store_row4(dq, row * kTcDK, lane, a, out_f32);
+      store_row4(dk, row * kTcDK, lane, b, out_f32);
+      if (dg) {
+        const uint2 qr = qv[u], kr = kv[u];
+        float x = __uint_as_float(qr.x << 16) * a.x + __uint_as_float(qr.x & 0xffff0000u) * a.y +
+                  __uint_as_float(qr.y << 16) * a.z + __uint_as_float(qr.y & 0xffff0000u) * a.w;
+        x -= __uint_as_float(kr.x << 16) * b.x + __uint_as_float(kr.x & 0xffff0000u) * b.y +
+             __uint_as_float(kr.y << 16) * b.z + __uint_as_float(kr.y & 0xffff0000u) * b.w;
+        x = warp_sum32(x);
+        if (lane == 0) dg[row] = t == len - 1 ? x + c_t : x;
+      }
+    }
+  }
+
+  // dv: back in token order and dtype, eight tokens a warp in flight
+  for (int tb = t0 + kTok * warp; tb < t1; tb += kTok * kWarps) {
+    float4 cv[kTok];
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int t = min(tb + u, t1 - 1);
+      const long long rrow = (start + (len - 1 - t)) * H + h;
+      cv[u] = __ldg(reinterpret_cast<const float4*>(rdv32 + rrow * kTcDV) + lane);
+    }
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+      const int t = tb + u;
+      if (t >= t1) break;  // warp-uniform
+      store_row4(dv, ((start + t) * H + h) * kTcDV, lane, cv[u], out_f32);
+    }
+  }
+
+  // d_init = scale e^{g_0} R_0 (the dv run's final state), in place; each
+  // block of the pair scales an equal share
+  if (d_init) {
+    const float f = len > 0 ? scale * expf(fmaxf(__ldg(g + start * H + h), -kGateClamp)) : scale;
+    constexpr int kPer = kTcDK * kTcDV / 4 / kBlocksPerPair;
+    float4* p = reinterpret_cast<float4*>(d_init + st_off) + blk * kPer;
+    for (int e = threadIdx.x; e < kPer; e += kCopyThreads) {
+      float4 x = p[e];
+      x.x *= f; x.y *= f; x.z *= f; x.w *= f;
+      p[e] = x;
+    }
+  }
+}
+
+// Workspace sections, each starting on a 256-byte boundary.
+struct TcWorkspace {
+  size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, dq32, rdk32, rdv32, total;
+};
+
+TcWorkspace workspace_layout(int B, int H, long long rows) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t tok = (size_t)rows * H;
+  const size_t st = (size_t)B * H * kTcDK * kTcDV * 4;
+  TcWorkspace w;
+  size_t o = 0;
+  w.rq = o;    o += up(tok * kTcDK * 2);
+  w.rk = o;    o += up(tok * kTcDK * 2);
+  w.rv = o;    o += up(tok * kTcDV * 2);
+  w.rdo = o;   o += up(tok * kTcDV * 2);
+  w.rg = o;    o += up(tok * 4);
+  w.s0t = o;   o += up(st);
+  w.dfs = o;   o += up(st);
+  w.dfst = o;  o += up(st);
+  w.stt = o;   o += up(st);
+  w.dq32 = o;  o += up(tok * kTcDK * 4);
+  w.rdk32 = o; o += up(tok * kTcDK * 4);
+  w.rdv32 = o; o += up(tok * kTcDV * 4);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+
+bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate) {
+  return !fp32_io && !vector_gate && dk == kTcDK && dv == kTcDV;
+}
+
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows) {
+  return workspace_layout(B, H, rows).total;
+}
+
+cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream) {
+  const long long rows = a.cu_seqlens ? (long long)a.T : (long long)a.B * a.T;
+  const TcWorkspace w = workspace_layout(a.B, a.H, rows);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  auto fl = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  const unsigned grid = (unsigned)((long long)a.B * a.H * kBlocksPerPair);
+
+  bwd_tc_prep_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+      (const __nv_bfloat16*)a.d_out, a.g, 1.f / a.scale, a.init_state, a.d_final, bf(w.rq),
+      bf(w.rk), bf(w.rv), bf(w.rdo), fl(w.rg), fl(w.s0t), fl(w.dfs), fl(w.dfst), a.cu_seqlens,
+      a.B, a.H, a.T, a.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  ChunkArgs c{};
+  c.scale = a.scale; c.cu_seqlens = a.cu_seqlens; c.B = a.B; c.H = a.H; c.T = a.T;
+  c.chunk = 128; c.fp32_io = false; c.fp32_out = true; c.vector_gate = false;
+  c.status = a.status;
+  // dq: the prefill of (do, v, k) with S_0^T; its final state S_T^T feeds dg
+  c.q = a.d_out; c.k = a.v; c.v = a.k; c.g = a.g;
+  c.init_state = a.init_state ? fl(w.s0t) : nullptr;
+  c.out = fl(w.dq32);
+  c.final_state = (a.dg && a.d_final) ? fl(w.stt) : nullptr;
+  c.dk = kTcDV; c.dv = kTcDK;
+  if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
+  // dk (reversed): the prefill of (v, do, q) with (dS_T / scale)^T
+  c.q = bf(w.rv); c.k = bf(w.rdo); c.v = bf(w.rq); c.g = fl(w.rg);
+  c.init_state = a.d_final ? fl(w.dfst) : nullptr;
+  c.out = fl(w.rdk32);
+  c.final_state = nullptr;
+  c.dk = kTcDV; c.dv = kTcDK;
+  if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
+  // dv (reversed): the prefill of (k, q, do) with dS_T / scale; final state R_0
+  c.q = bf(w.rk); c.k = bf(w.rq); c.v = bf(w.rdo); c.g = fl(w.rg);
+  c.init_state = a.d_final ? fl(w.dfs) : nullptr;
+  c.out = fl(w.rdv32);
+  c.final_state = a.d_init;
+  c.dk = kTcDK; c.dv = kTcDV;
+  if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
+
+  bwd_tc_fin_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, a.g, a.scale, fl(w.dq32),
+      fl(w.rdk32), fl(w.rdv32), (a.dg && a.d_final) ? fl(w.stt) : nullptr,
+      a.d_final ? fl(w.dfst) : nullptr, a.dq, a.dk,
+      a.dv, a.fp32_out, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T, a.status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.dg) {
+    const long long pairs = (long long)a.B * a.H;
+    bwd_dg_scan_kernel<<<(unsigned)((pairs + kScanWarps - 1) / kScanWarps), kScanWarps * 32, 0,
+                         stream>>>(a.dg, a.cu_seqlens, a.B, a.H, a.T, a.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace gla

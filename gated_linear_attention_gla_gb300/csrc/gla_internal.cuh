@@ -110,6 +110,11 @@ cudaError_t launch_chunk_bwd_head_bf16(const ChunkBwdArgs& a, cudaStream_t strea
 cudaError_t launch_chunk_bwd_head_f32(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_f32(const ChunkBwdArgs& a, cudaStream_t stream);
+// the per-head-gate backward on the tensor cores (three prefill runs), bf16,
+// d_k = d_v = 128; needs chunk_bwd_tc_workspace(B, H, rows) bytes of workspace
+bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate);
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows);
+cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Small device helpers shared by the kernels.

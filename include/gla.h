@@ -243,17 +243,38 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
  *                 gate its terms are summed across CTAs with fp32 atomics, so
  *                 its last bits may vary from run to run.
  *   d_init_state  fp32 [B, H, dk, dv], or NULL (not written)
+ *   workspace     device scratch owned by the caller, or NULL; with at least
+ *                 gla_chunk_bwd_workspace_size(...) bytes (256-byte aligned),
+ *                 bf16 I/O, the per-head gate and dk = dv = 128, the call runs
+ *                 on the tensor cores: the gradient of the recurrence is the
+ *                 same recurrence with its operands exchanged -- dq is the
+ *                 prefill of (d_out, v, k), dk and dv are prefills of (v,
+ *                 d_out, q) and (k, q, d_out) run backwards in time -- so it
+ *                 runs the tcgen05 prefill kernel three times between a
+ *                 reversing pass and a finishing pass (accuracy that of the
+ *                 prefill: bf16 operands, fp32 accumulation).  Otherwise
+ *                 (or with a smaller workspace) the fp32 CUDA-core kernels run.
  *   flags         GLA_FLAG_FP32_IO, GLA_FLAG_VECTOR_GATE, GLA_FLAG_FP32_OUT
- * The outputs must not overlap one another or any input.  Empty sequences
- * write d_init_state = d_final_state (or zeros).  Four kernel launches (a
- * fifth, and a memset of dg, for the per-head gate's dg) on the CUDA cores.
+ * The outputs and the workspace must not overlap one another or any input.
+ * Empty sequences write d_init_state = d_final_state (or zeros).
  * Alignment: as gla_chunk_fwd; every output 16-byte aligned.
  */
 gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const float *g,
                          float scale, const float *init_state, const void *d_out,
                          const float *d_final_state, void *dq, void *dk_out, void *dv_out,
                          float *dg, float *d_init_state, const int32_t *cu_seqlens, int B,
-                         int H, int T, int dk, int dv, gla_stream_t stream, unsigned flags);
+                         int H, int T, int dk, int dv, void *workspace,
+                         size_t workspace_bytes, gla_stream_t stream, unsigned flags);
+
+/*
+ * gla_chunk_bwd_workspace_size -- bytes of device workspace with which
+ * gla_chunk_bwd takes its tensor-core path for these sizes and flags, or 0 when
+ * that path does not cover them (the call then runs on the CUDA cores and
+ * needs no workspace).  `packed` != 0: T counts packed rows (cu_seqlens given).
+ * Pure host function.
+ */
+size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int packed,
+                                    unsigned flags);
 
 /*
  * gla_chunk_fwd_kernel -- which kernel gla_chunk_fwd runs for a non-empty call

@@ -205,11 +205,14 @@ def test_decode_mixer_rejects_before_launch(L):
     assert call(q=0) == E.GLA_ERR_INVALID_ARG
 
 
+WS = 1 << 32  # a fake 256-byte-aligned workspace far from the other fake tensors
+
+
 def bwd(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, init=FAKE[4], d_out=FAKE[5],
         d_final=FAKE[6], dq=FAKE[7], dk_out=FAKE[8], dv_out=FAKE[9], dg=FAKE[10],
-        d_init=FAKE[11], cu=0, B=2, H=4, T=256, dk=128, dv=128, flags=0):
+        d_init=FAKE[11], cu=0, B=2, H=4, T=256, dk=128, dv=128, ws=0, ws_bytes=0, flags=0):
     return _binding.gla_chunk_bwd(q, k, v, g, scale, init, d_out, d_final, dq, dk_out, dv_out,
-                                  dg, d_init, cu, B, H, T, dk, dv, 0, flags)
+                                  dg, d_init, cu, B, H, T, dk, dv, ws, ws_bytes, 0, flags)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -231,6 +234,8 @@ def bwd(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], scale=0.1, init=FAKE[4], d_o
     (dict(d_init=FAKE[6]), E.GLA_ERR_INVALID_ARG),         # d_init overlaps d_final
     (dict(dg=FAKE[5] + 256), E.GLA_ERR_INVALID_ARG),       # dg inside d_out
     (dict(B=1 << 20, T=1 << 20), E.GLA_ERR_INVALID_ARG),   # size overflow
+    (dict(ws=WS + 16, ws_bytes=1 << 30), E.GLA_ERR_MISALIGNED),
+    (dict(ws=FAKE[7], ws_bytes=1 << 30), E.GLA_ERR_INVALID_ARG),  # workspace over dq and more
 ])
 def test_chunk_bwd_rejects_before_launch(L, kw, status):
     assert bwd(**kw) == status
@@ -241,3 +246,18 @@ def test_chunk_bwd_empty_problems_are_no_ops(L):
     assert bwd(H=0) == E.GLA_OK
     assert bwd(T=0, d_init=0, q=0, k=0, v=0, g=0, d_out=0, dq=0, dk_out=0, dv_out=0,
                dg=0) == E.GLA_OK
+
+
+def test_chunk_bwd_workspace_size(L):
+    ws = _binding.chunk_bwd_workspace_size
+    n = ws(2, 4, 256, 128, 128, 0, 0)
+    assert n > 0 and n % 256 == 0
+    # reversed q, k, v, do (bf16), the shifted gate, four states, three fp32 results
+    tok = 2 * 256 * 4
+    assert n >= tok * 128 * (4 * 2 + 3 * 4) + tok * 4 + 4 * 2 * 4 * 128 * 128 * 4
+    assert ws(2, 4, 512, 128, 128, 1, 0) == n          # packed: T counts the rows
+    assert ws(2, 4, 256, 128, 128, 0, E.GLA_FLAG_FP32_IO) == 0
+    assert ws(2, 4, 256, 128, 128, 0, E.GLA_FLAG_VECTOR_GATE) == 0
+    assert ws(2, 4, 256, 96, 192, 0, 0) == 0
+    assert ws(2, 4, 256, 128, 64, 0, 0) == 0
+    assert ws(0, 4, 256, 128, 128, 0, 0) == 0

@@ -1,5 +1,9 @@
 """GPU chunked backward (gla_chunk_bwd) against the fp64 oracle's gradient.
 
+Both paths behind the entry point: the fp32 CUDA-core kernels (every test
+without ``tc``) and the tensor-core path (bf16, per-head gate, d = 128: three
+runs of the tcgen05 prefill kernel on exchanged operands; the ``tc`` tests).
+
 The oracle's gradient (reverse mode through the recurrence, token by token)
 is itself pinned to finite differences of the forward in
 ``test_oracle_backward_pins.py``.  Here the GPU path is compared with it at
@@ -29,6 +33,15 @@ pytestmark = pytest.mark.gpu
 
 TOL_GRAD = 1e-4
 TOL_DG = 1e-3
+# tensor-core path: the prefill kernel's accuracy (bf16 operands, fp32
+# accumulation), the bf16 output tolerance applied to fp32 results
+TOL_GRAD_TC = 2e-2
+# dg on that path is a suffix sum over up to T tokens of 128-channel dot
+# products of the inputs with those gradients: the per-term errors add up
+# along the suffix like the terms themselves, so the relative error stays near
+# the gradients' but its maximum over a long sequence grows (2.3e-2 measured at
+# T = 2048): 5e-2
+TOL_DG_TC = 5e-2
 
 
 def _gla():
@@ -36,14 +49,17 @@ def _gla():
     return gla
 
 
-def run_gpu(x, gr, grad_dtype=None, need_dg=True, need_d_init=True, init=True, final=True):
+def run_gpu(x, gr, grad_dtype=None, need_dg=True, need_d_init=True, init=True, final=True,
+            tc=False):
+    """The CUDA-core path by default; ``tc`` takes the tensor-core path where it
+    covers the call."""
     gla = _gla()
     res = gla.chunk_bwd(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]),
                         cuda(gr["d_out"]), scale=x["scale"],
                         init_state=cuda(x["init_state"]) if init else None,
                         d_final_state=cuda(gr["d_final_state"]) if final else None,
                         cu_seqlens=cuda(x["cu_seqlens"]), grad_dtype=grad_dtype,
-                        need_dg=need_dg, need_d_init=need_d_init)
+                        need_dg=need_dg, need_d_init=need_d_init, tensor_cores=tc)
     gla.status_sync()
     return res
 
@@ -188,3 +204,65 @@ def test_full_size_sampled_pairs(gate):
                 got[2][b:b + 1, :, h:h + 1], got[3][b:b + 1, :, h:h + 1],
                 got[4][b:b + 1, h:h + 1]]
         check(mine, ref, label=f"full {gate} ({b},{h})")
+
+
+# --------------------------------------------------------------------------
+# tensor-core path
+# --------------------------------------------------------------------------
+def test_tc_path_is_taken_only_where_it_applies():
+    from gated_linear_attention_gla_gb300 import _binding as b
+    assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, 0) > 0
+    assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, b.GLA_FLAG_VECTOR_GATE) == 0
+
+
+def test_tc_backward_matches_oracle():
+    x, gr = inputs(B=2, T=300, H=3)   # two full 128-token chunks and a ragged tail
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc")
+
+
+def test_tc_bf16_gradients_are_the_fp32_ones_rounded():
+    x, gr = inputs(B=1, T=260, H=2)
+    g32 = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    g16 = run_gpu(x, gr, tc=True)
+    for a, b in zip(g16[:3], g32[:3]):
+        assert a.dtype == torch.bfloat16 and torch.equal(a, b.to(torch.bfloat16))
+    assert torch.equal(g16[4], g32[4])
+
+
+def test_tc_packed_with_empty_and_short_sequences():
+    x, gr = inputs("varlen", lengths=[300, 0, 1, 129, 128, 5], H=2)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc packed")
+    # the empty sequence hands d_final through (as (d_final / scale) * scale)
+    torch.testing.assert_close(got[4][1].cpu(), gr["d_final_state"][1], rtol=1e-6, atol=0)
+
+
+def test_tc_optional_inputs_and_outputs_left_out():
+    x, gr = inputs(B=2, T=200, H=2)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, init=False, final=False, tc=True)
+    check(got, run_ref(x, gr, init=False, final=False), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC,
+          label="tc no init/final")
+    dq, dk, dv, dg, d0 = run_gpu(x, gr, grad_dtype=torch.float32, need_dg=False,
+                                 need_d_init=False, init=False, final=False, tc=True)
+    assert dg is None and d0 is None
+    assert torch.equal(dq, got[0]) and torch.equal(dk, got[1]) and torch.equal(dv, got[2])
+
+
+def test_tc_full_size_sampled_pairs():
+    """The prefill workload at full size (B=4, H=16, T=2048) on the tensor-core
+    path, sampled (sequence, head) pairs against the oracle."""
+    x, gr = inputs()
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    for b, h in [(0, 0), (3, 15), (1, 9)]:
+        sub = dict(x)
+        for key in ("q", "k", "v", "g"):
+            sub[key] = x[key][b:b + 1, :, h:h + 1]
+        sub["init_state"] = x["init_state"][b:b + 1, h:h + 1]
+        sgr = dict(d_out=gr["d_out"][b:b + 1, :, h:h + 1],
+                   d_final_state=gr["d_final_state"][b:b + 1, h:h + 1])
+        mine = [got[0][b:b + 1, :, h:h + 1], got[1][b:b + 1, :, h:h + 1],
+                got[2][b:b + 1, :, h:h + 1], got[3][b:b + 1, :, h:h + 1],
+                got[4][b:b + 1, h:h + 1]]
+        check(mine, run_ref(sub, sgr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC,
+              label=f"tc full ({b},{h})")
