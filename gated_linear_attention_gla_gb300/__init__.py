@@ -147,7 +147,7 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
 def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
               d_final_state=None, cu_seqlens=None, grad_dtype=None, need_dg: bool = True,
               need_d_init: bool = True, tensor_cores: bool = True, workspace=None,
-              stream=None):
+              fixed_workspace: bool = False, stream=None):
     """Gradient of ``chunk_fwd`` (gla_chunk_bwd); returns ``(dq, dk, dv, dg, d_init)``.
 
     ``q, k, v, g, scale, init_state, cu_seqlens`` as given to ``chunk_fwd``;
@@ -160,7 +160,9 @@ def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
     ``tensor_cores``: use the tensor-core path where it covers the call (bf16,
     per-head gate, dk = dv = 128), with ``workspace`` (a CUDA uint8 tensor of at
     least ``gla_chunk_bwd_workspace_size`` bytes) or a fresh allocation; False
-    runs the fp32 CUDA-core kernels.
+    runs the fp32 CUDA-core kernels.  ``fixed_workspace``: call
+    gla_chunk_bwd_fixed_workspace instead, whose workspace is the library's own
+    fixed device buffer (nothing is allocated; ``workspace`` is ignored).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("d_out", d_out)):
         _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
@@ -191,6 +193,14 @@ def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
     dv_ = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
     dg = torch.empty(g.shape, dtype=torch.float32, device=q.device) if need_dg else None
     d_init = torch.empty(st, dtype=torch.float32, device=q.device) if need_d_init else None
+    if fixed_workspace:
+        rc = _binding.gla_chunk_bwd_fixed_workspace(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state), _ptr(d_out),
+            _ptr(d_final_state), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(d_init),
+            _ptr(cu_seqlens), B, H, T, dk, dv, _stream(stream), flags)
+        if rc != 0:
+            raise GlaError(rc, "gla_chunk_bwd_fixed_workspace")
+        return dq, dk_, dv_, dg, d_init
     ws_bytes = 0
     if tensor_cores:
         ws_bytes = _binding.chunk_bwd_workspace_size(B, H, T, dk, dv, cu_seqlens is not None,

@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
                                         _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                                         ctypes.c_size_t, _vp, ctypes.c_uint]
             L.gla_chunk_bwd.restype = _i
+            L.gla_chunk_bwd_fixed_workspace.argtypes = [
+                _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                _i, _i, _i, _i, _i, _vp, ctypes.c_uint]
+            L.gla_chunk_bwd_fixed_workspace.restype = _i
             L.gla_chunk_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_uint]
             L.gla_chunk_bwd_workspace_size.restype = ctypes.c_size_t
             L.gla_status_string.argtypes = [_i]
@@ -146,6 +150,16 @@ def gla_chunk_bwd(q, k, v, g, scale, init_state, d_out, d_final, dq, dk_out, dv_
                                n(d_final), n(dq), n(dk_out), n(dv_out), n(dg), n(d_init),
                                n(cu_seqlens), B, H, T, dk, dv, n(workspace),
                                int(workspace_bytes), n(stream), flags)
+
+
+def gla_chunk_bwd_fixed_workspace(q, k, v, g, scale, init_state, d_out, d_final, dq, dk_out,
+                                  dv_out, dg, d_init, cu_seqlens, B, H, T, dk, dv, stream,
+                                  flags) -> int:
+    """Raw call: pointers are ints (0 = NULL), ``stream`` an int handle."""
+    n = lambda p: p or None  # noqa: E731
+    return lib().gla_chunk_bwd_fixed_workspace(
+        n(q), n(k), n(v), n(g), float(scale), n(init_state), n(d_out), n(d_final), n(dq),
+        n(dk_out), n(dv_out), n(dg), n(d_init), n(cu_seqlens), B, H, T, dk, dv, n(stream), flags)
 
 
 def chunk_bwd_workspace_size(B, H, T, dk, dv, packed, flags) -> int:

@@ -183,12 +183,20 @@ size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int pac
   return gla::chunk_bwd_tc_workspace(B, H, rows);
 }
 
-gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
-                         float scale, const float* init_state, const void* d_out,
-                         const float* d_final_state, void* dq, void* dk_out, void* dv_out,
-                         float* dg, float* d_init_state, const int32_t* cu_seqlens, int B,
-                         int H, int T, int dk, int dv, void* workspace, size_t workspace_bytes,
-                         gla_stream_t stream, unsigned flags) {
+static_assert(GLA_BWD_FIXED_WORKSPACE_BYTES == gla::kBwdFixedWorkspaceBytes,
+              "the header states the fixed workspace's size");
+
+}  // extern "C"
+
+namespace {
+
+// gla_chunk_bwd's checks and launches; with check_only, returns after the checks.
+gla_status chunk_bwd_impl(const void* q, const void* k, const void* v, const float* g,
+                          float scale, const float* init_state, const void* d_out,
+                          const float* d_final_state, void* dq, void* dk_out, void* dv_out,
+                          float* dg, float* d_init_state, const int32_t* cu_seqlens, int B,
+                          int H, int T, int dk, int dv, void* workspace, size_t workspace_bytes,
+                          gla_stream_t stream, unsigned flags, bool check_only) {
   if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
     return GLA_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
@@ -232,7 +240,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const floa
     for (int o2 = o + 1; o2 < 6; ++o2)
       if (overlap(out_p[o], out_b[o], out_p[o2], out_b[o2])) return GLA_ERR_INVALID_ARG;
   }
-  if (rows == 0 && d_init_state == nullptr) return GLA_OK;
+  if (check_only || (rows == 0 && d_init_state == nullptr)) return GLA_OK;
 
   cudaError_t err;
   unsigned* status = status_word(&err);
@@ -251,6 +259,51 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const floa
   else
     err = fp32 ? gla::launch_chunk_bwd_head_f32(a, s) : gla::launch_chunk_bwd_head_bf16(a, s);
   return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                         float scale, const float* init_state, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk_out, void* dv_out,
+                         float* dg, float* d_init_state, const int32_t* cu_seqlens, int B,
+                         int H, int T, int dk, int dv, void* workspace, size_t workspace_bytes,
+                         gla_stream_t stream, unsigned flags) {
+  return chunk_bwd_impl(q, k, v, g, scale, init_state, d_out, d_final_state, dq, dk_out, dv_out,
+                        dg, d_init_state, cu_seqlens, B, H, T, dk, dv, workspace,
+                        workspace_bytes, stream, flags, false);
+}
+
+gla_status gla_chunk_bwd_fixed_workspace(const void* q, const void* k, const void* v,
+                                         const float* g, float scale, const float* init_state,
+                                         const void* d_out, const float* d_final_state,
+                                         void* dq, void* dk_out, void* dv_out, float* dg,
+                                         float* d_init_state, const int32_t* cu_seqlens, int B,
+                                         int H, int T, int dk, int dv, gla_stream_t stream,
+                                         unsigned flags) {
+  // every argument check first, exactly as gla_chunk_bwd makes them
+  const gla_status st =
+      chunk_bwd_impl(q, k, v, g, scale, init_state, d_out, d_final_state, dq, dk_out, dv_out,
+                     dg, d_init_state, cu_seqlens, B, H, T, dk, dv, nullptr, 0, stream, flags,
+                     true);
+  if (st != GLA_OK) return st;
+  // the library's buffer is used (and its module loaded) only when the
+  // tensor-core path covers the call and its workspace fits
+  void* ws = nullptr;
+  if (B > 0 && H > 0 && T > 0) {
+    const size_t need = gla_chunk_bwd_workspace_size(B, H, T, dk, dv, cu_seqlens != nullptr,
+                                                     flags);
+    if (need > 0 && need <= gla::kBwdFixedWorkspaceBytes) {
+      cudaError_t err;
+      ws = gla::bwd_fixed_workspace(&err);
+      if (!ws) return cuda_status(err);
+    }
+  }
+  return gla_chunk_bwd(q, k, v, g, scale, init_state, d_out, d_final_state, dq, dk_out, dv_out,
+                       dg, d_init_state, cu_seqlens, B, H, T, dk, dv, ws,
+                       ws ? gla::kBwdFixedWorkspaceBytes : 0, stream, flags);
 }
 
 namespace {

@@ -115,6 +115,10 @@ cudaError_t launch_chunk_bwd_chan_f32(const ChunkBwdArgs& a, cudaStream_t stream
 bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate);
 size_t chunk_bwd_tc_workspace(int B, int H, long long rows);
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream);
+// the fixed device workspace of gla_chunk_bwd_fixed_workspace (a static array;
+// its address, or null with *err set)
+constexpr size_t kBwdFixedWorkspaceBytes = 384ull << 20;
+void* bwd_fixed_workspace(cudaError_t* err);
 
 // ---------------------------------------------------------------------------
 // Small device helpers shared by the kernels.

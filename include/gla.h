@@ -46,6 +46,7 @@
 #ifndef GLA_H_
 #define GLA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -265,6 +266,26 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
                          float *dg, float *d_init_state, const int32_t *cu_seqlens, int B,
                          int H, int T, int dk, int dv, void *workspace,
                          size_t workspace_bytes, gla_stream_t stream, unsigned flags);
+
+/*
+ * gla_chunk_bwd_fixed_workspace -- gla_chunk_bwd without a caller workspace:
+ * the tensor-core path takes its workspace from a fixed device buffer inside
+ * the library (GLA_BWD_FIXED_WORKSPACE_BYTES, a static device array placed on
+ * the GPU when this function first needs it), so the call allocates nothing.
+ * Calls whose workspace need (gla_chunk_bwd_workspace_size) exceeds the buffer,
+ * or that the tensor-core path does not cover, run on the CUDA cores.
+ * Arguments, results and errors as gla_chunk_bwd.  The buffer is one per GPU:
+ * calls that use it must not overlap in time (issue them on one stream, or
+ * synchronise between them).
+ */
+#define GLA_BWD_FIXED_WORKSPACE_BYTES ((size_t)384 << 20)
+gla_status gla_chunk_bwd_fixed_workspace(const void *q, const void *k, const void *v,
+                                         const float *g, float scale, const float *init_state,
+                                         const void *d_out, const float *d_final_state,
+                                         void *dq, void *dk_out, void *dv_out, float *dg,
+                                         float *d_init_state, const int32_t *cu_seqlens, int B,
+                                         int H, int T, int dk, int dv, gla_stream_t stream,
+                                         unsigned flags);
 
 /*
  * gla_chunk_bwd_workspace_size -- bytes of device workspace with which

@@ -157,7 +157,8 @@ def test_decode_step_empty_is_no_op(L):
 def test_ctypes_signatures_match_header(L):
     """The binding's argument counts equal the header's parameter counts."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    for name in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step", "gla_decode_step_slots",
+    for name in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_chunk_bwd_fixed_workspace",
+                 "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_slots",
                  "gla_decode_step_mixer", "gla_mixer_epilogue", "gla_status_sync",
                  "gla_status_string"):
         m = re.search(name + r"\s*\(([^)]*)\)", text)
@@ -261,3 +262,17 @@ def test_chunk_bwd_workspace_size(L):
     assert ws(2, 4, 256, 96, 192, 0, 0) == 0
     assert ws(2, 4, 256, 128, 64, 0, 0) == 0
     assert ws(0, 4, 256, 128, 128, 0, 0) == 0
+
+
+def test_chunk_bwd_fixed_workspace_rejects_before_launch(L):
+    call = lambda **kw: _binding.gla_chunk_bwd_fixed_workspace(  # noqa: E731
+        *[kw.get(n, d) for n, d in (("q", FAKE[0]), ("k", FAKE[1]), ("v", FAKE[2]),
+                                     ("g", FAKE[3]))], kw.get("scale", 0.1), FAKE[4], FAKE[5],
+        FAKE[6], kw.get("dq", FAKE[7]), FAKE[8], FAKE[9], FAKE[10], FAKE[11], 0, 2, 4,
+        kw.get("T", 256), kw.get("dk", 128), 128, 0, kw.get("flags", 0))
+    assert call(flags=1 << 5) == E.GLA_ERR_INVALID_ARG
+    assert call(dk=80) == E.GLA_ERR_UNSUPPORTED
+    assert call(dq=0) == E.GLA_ERR_INVALID_ARG
+    assert call(dq=FAKE[0]) == E.GLA_ERR_INVALID_ARG       # dq overlaps q
+    assert call(scale=float("nan")) == E.GLA_ERR_INVALID_ARG
+    assert call(T=-1) == E.GLA_ERR_INVALID_ARG
