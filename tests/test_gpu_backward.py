@@ -300,3 +300,49 @@ def test_fixed_workspace_falls_back_when_too_large():
         assert torch.equal(mine[i], ref[i])
     # the per-head gate's dg terms meet through atomics: equal up to their order
     torch.testing.assert_close(mine[3], ref[3], rtol=1e-5, atol=1e-5 * float(ref[3].abs().max()))
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 256])
+def test_tc_chunk_boundaries(T):
+    x, gr = inputs(B=2, T=T, H=2)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label=f"tc T={T}")
+
+
+def test_tc_zero_gate():
+    """g = 0 (no decay): the gradients are those of causal linear attention."""
+    x, gr = inputs(B=1, T=200, H=2)
+    x["g"] = torch.zeros_like(x["g"])
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc g=0")
+
+
+def test_tc_strong_decays_take_the_wide_path():
+    """Gates around -40 make every chunk "wide" (decay span past 2^96) in the
+    three prefill runs, forward and reversed.  As for the CUDA-core path, the
+    reference is the oracle at max(g, -30).  dg is then ~1e-4 of its per-token
+    terms x_t = sum_i (q dq - k dk), and its error is the suffix sum of those
+    terms' own errors (the gradients' bf16-level ~1e-2 at most, a few 1e-3
+    typically): a random walk over up to T tokens, held to
+    1e-2 sqrt(T) RMS(x) (measured 5.2e-2 RMS(x) at T = 300, bound 0.17)."""
+    T = 300
+    x, gr = inputs(B=1, T=T, H=2, g_mu=-2.0, g_div=0.05)
+    xc = dict(x, g=x["g"].clamp(min=-30.0))
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    ref = run_ref(xc, gr)
+    check(got[:3] + (None,) + got[4:], ref, tol=TOL_GRAD_TC, label="tc strong")
+    terms = (to_np(x["q"]) * ref[0] - to_np(x["k"]) * ref[1]).sum(-1)
+    err = float(np.max(np.abs(to_np(got[3]) - ref[3])))
+    scale_x = float(np.sqrt(np.mean(terms * terms)))
+    print(f"tc strong dg: max err {err / scale_x:.2e} RMS(x)")
+    assert err <= 1e-2 * np.sqrt(T) * scale_x
+
+
+def test_tc_minus_inf_gate_resets():
+    """A gate of -inf at one token erases the state there (clamped to -30 on the
+    GPU): the gradient reaching across it is below 1e-13."""
+    x, gr = inputs(B=1, T=260, H=2)
+    x["g"][0, 130, :] = float("-inf")
+    xc = dict(x, g=x["g"].clamp(min=-30.0))
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(xc, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc -inf")
