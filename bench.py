@@ -439,15 +439,17 @@ def time_backward(gla, dev, reps=5, warmup=3):
     w0 = gla_inputs.WORKLOADS["prefill"]
     hbm, bf16_peak, _, kind = peaks()
     from gated_linear_attention_gla_gb300 import _binding
+    vec = dict(gate="vector", g_mu=2.0, g_div=4.0)
     for gate, over, tc in (("per-head", {}, True), ("per-head", {}, False),
-                           ("per-key-channel", dict(gate="vector", g_mu=2.0, g_div=4.0), False)):
+                           ("per-key-channel", vec, True), ("per-key-channel", vec, False)):
         w = gla_inputs.dataclasses.replace(w0, **over)
         x = gla_inputs.prefill_inputs(w)
         gr = gla_inputs.grad_inputs(x)
         args = [x[n].to(dev) for n in ("q", "k", "v", "g")] + [gr["d_out"].to(dev)]
         ws = None
         if tc:
-            n = _binding.chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, False, 0)
+            flags = _binding.GLA_FLAG_VECTOR_GATE if w.gate == "vector" else 0
+            n = _binding.chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, False, flags)
             ws = torch.empty(n, dtype=torch.uint8, device=dev)
         kw = dict(scale=x["scale"], init_state=x["init_state"].to(dev),
                   d_final_state=gr["d_final_state"].to(dev), tensor_cores=tc, workspace=ws)
@@ -465,9 +467,11 @@ def time_backward(gla, dev, reps=5, warmup=3):
         entry = {
             "workload": f"chunked backward, {gate} gate, B={w.B} T={w.T} H={w.H} "
                         f"dk=dv={w.dk}, bf16 q/k/v/d_out, bf16 gradients, fp32 dg and d_init",
-            "path": "tensor cores (3 prefill runs)" if tc else "CUDA cores (fp32)",
+            "path": ("CUDA cores (fp32)" if not tc else
+                     "tensor cores (3 prefill runs)" if w.gate != "vector" else
+                     "dv on the tensor cores (reversed prefill), dq and dk on the CUDA cores"),
             "ms": ms, "tokens_per_s": w.B * w.T / sec}
-        if tc:
+        if tc and w.gate != "vector":
             nbytes = backward_bytes(w, w.B, w.T)
             flops = backward_flops(w, w.B, w.T, chunk=128)
             entry["roofline"] = {
@@ -478,6 +482,16 @@ def time_backward(gla, dev, reps=5, warmup=3):
                            "frac": flops / sec / 1e12 / bf16_peak, "algorithmic_flops": flops},
                 "workspace_bytes": ws.numel()}
             entry["launches"] = 6
+        elif tc:
+            # mostly the CUDA-core dq and dk kernels: their fp32 roofline
+            flops = backward_flops(w, w.B, w.T)
+            peak = fp32_peak_tflops()
+            entry["roofline"] = {
+                "bound": "alu", "achieved": flops / sec / 1e12, "peak": peak,
+                "unit": "TFLOP/s", "frac": flops / sec / 1e12 / peak,
+                "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
+                "algorithmic_flops": flops, "workspace_bytes": ws.numel()}
+            entry["launches"] = 5
         else:
             flops = backward_flops(w, w.B, w.T)
             peak = fp32_peak_tflops()

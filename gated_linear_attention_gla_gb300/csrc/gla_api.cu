@@ -180,7 +180,7 @@ size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int pac
   if (!gla::chunk_bwd_tc_supported(dk, dv, fp32, vec)) return 0;
   const long long rows = packed ? (long long)T : (long long)B * T;
   if (rows * H * dk > kMaxElems) return 0;
-  return gla::chunk_bwd_tc_workspace(B, H, rows);
+  return gla::chunk_bwd_tc_workspace(B, H, rows, vec);
 }
 
 static_assert(GLA_BWD_FIXED_WORKSPACE_BYTES == gla::kBwdFixedWorkspaceBytes,
@@ -229,8 +229,9 @@ gla_status chunk_bwd_impl(const void* q, const void* k, const void* v, const flo
   const size_t in_b[] = {qk_b, qk_b, v_b, g_b, v_b, st_b, st_b,
                          cu_seqlens ? (size_t)(B + 1) * 4 : 0};
   // the tensor-core path runs when it covers the call and the workspace is large enough
-  const size_t ws_need =
-      gla::chunk_bwd_tc_supported(dk, dv, fp32, vec) ? gla::chunk_bwd_tc_workspace(B, H, rows) : 0;
+  const size_t ws_need = gla::chunk_bwd_tc_supported(dk, dv, fp32, vec)
+                             ? gla::chunk_bwd_tc_workspace(B, H, rows, vec)
+                             : 0;
   const bool use_tc = rows > 0 && ws_need > 0 && workspace != nullptr && workspace_bytes >= ws_need;
   const void* out_p[] = {dq, dk_out, dv_out, dg, d_init_state, use_tc ? workspace : nullptr};
   const size_t out_b[] = {dqk_b, dqk_b, dv_b, g_b, st_b, ws_need};
@@ -251,10 +252,16 @@ gla_status chunk_bwd_impl(const void* q, const void* k, const void* v, const flo
   a.dg = rows > 0 ? dg : nullptr; a.d_init = d_init_state; a.cu_seqlens = cu_seqlens;
   a.B = B; a.H = H; a.T = T; a.dk_size = dk; a.dv_size = dv;
   a.fp32_io = fp32; a.fp32_out = f32out; a.vector_gate = vec; a.status = status;
+  a.skip_dv = false;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (use_tc)
+  if (use_tc && !vec) {
     err = gla::launch_chunk_bwd_tc(a, workspace, s);
-  else if (vec)
+  } else if (use_tc) {
+    // per-key-channel gate: dq, dk (and dg, d_init) on the CUDA cores, dv on the tensor cores
+    a.skip_dv = true;
+    err = gla::launch_chunk_bwd_chan_bf16(a, s);
+    if (err == cudaSuccess) err = gla::launch_chunk_bwd_tc_vec_dv(a, workspace, s);
+  } else if (vec)
     err = fp32 ? gla::launch_chunk_bwd_chan_f32(a, s) : gla::launch_chunk_bwd_chan_bf16(a, s);
   else
     err = fp32 ? gla::launch_chunk_bwd_head_f32(a, s) : gla::launch_chunk_bwd_head_bf16(a, s);

@@ -946,7 +946,7 @@ cudaError_t launch_shape(const ChunkBwdArgs& a, cudaStream_t stream) {
         a.d_final, a.dk, a.fp32_out, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
+  if (!a.skip_dv) {
     using L = DvSmem<DK, DV, VEC>;
     auto kern = bwd_dv_kernel<IO, DK, DV, VEC>;
     if ((e = set_smem(kern, L::kBytes)) != cudaSuccess) return e;

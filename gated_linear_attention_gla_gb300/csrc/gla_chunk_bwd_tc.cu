@@ -257,6 +257,117 @@ bwd_tc_fin_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   }
 }
 
+// Per-key-channel gate (dv only): reversed copies of q, k and do, the gate
+// rows (one value per key channel) shifted by one token, and dS_T / scale.
+__global__ void __launch_bounds__(kCopyThreads)
+bwd_tc_prep_vec_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                       const __nv_bfloat16* __restrict__ d_out, const float* __restrict__ g,
+                       float inv_scale, const float* __restrict__ d_final,
+                       __nv_bfloat16* __restrict__ rq, __nv_bfloat16* __restrict__ rk,
+                       __nv_bfloat16* __restrict__ rdo, float* __restrict__ rg,
+                       float* __restrict__ dfs, const int32_t* __restrict__ cu, int B, int H,
+                       int T, unsigned* status) {
+  int s, h, blk;
+  pair_and_block(H, &s, &h, &blk);
+  long long start;
+  int len;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
+  int t0, t1;
+  block_range(len, blk, &t0, &t1);
+  // 16-byte vectors of a token: q, k, do rows (bf16, 16 each) and its gate row
+  // (fp32, 32); eight vectors a thread in flight at a time
+  constexpr int VB = kTcDK / 8, VG = kTcDK / 4;
+  constexpr int VPT = 3 * VB + VG;
+  constexpr int kBatch = 8;
+  static_assert(kTcDK == kTcDV, "one row width");
+  auto src_of = [&](int c, long long row) -> const uint4* {
+    if (c < 3 * VB) {
+      const __nv_bfloat16* b = c < VB ? q : c < 2 * VB ? k : d_out;
+      return reinterpret_cast<const uint4*>(b + row * kTcDK) + c % VB;
+    }
+    // the gate of the following token (none for the last one)
+    return reinterpret_cast<const uint4*>(g + (row + H) * kTcDK) + (c - 3 * VB);
+  };
+  auto dst_of = [&](int c, long long row) -> uint4* {
+    if (c < 3 * VB) {
+      __nv_bfloat16* b = c < VB ? rq : c < 2 * VB ? rk : rdo;
+      return reinterpret_cast<uint4*>(b + row * kTcDK) + c % VB;
+    }
+    return reinterpret_cast<uint4*>(rg + row * kTcDK) + (c - 3 * VB);
+  };
+  const int nvec = (t1 - t0) * VPT;
+  for (int base = threadIdx.x; base < nvec; base += kCopyThreads * kBatch) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / VPT, c = idx % VPT;
+        const bool last_gate = c >= 3 * VB && t + 1 >= len;
+        r[b] = last_gate ? make_uint4(0u, 0u, 0u, 0u) : __ldg(src_of(c, (start + t) * H + h));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / VPT, c = idx % VPT;
+        *dst_of(c, (start + (len - 1 - t)) * H + h) = r[b];
+      }
+    }
+  }
+  if (d_final) {
+    const size_t off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
+    constexpr int kPer = kTcDK * kTcDV / 4 / kBlocksPerPair;
+    const float4* src = reinterpret_cast<const float4*>(d_final + off) + blk * kPer;
+    float4* dst = reinterpret_cast<float4*>(dfs + off) + blk * kPer;
+    for (int e = threadIdx.x; e < kPer; e += kCopyThreads) {
+      float4 x = __ldg(src + e);
+      x.x *= inv_scale; x.y *= inv_scale; x.z *= inv_scale; x.w *= inv_scale;
+      dst[e] = x;
+    }
+  }
+}
+
+// dv back in token order: row t of the output is row len - 1 - t of the
+// reversed run's output (same dtype), 16-byte vectors, eight in flight.
+__global__ void __launch_bounds__(kCopyThreads)
+bwd_tc_unreverse_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                        int row_bytes, const int32_t* __restrict__ cu, int B, int H, int T,
+                        unsigned* status) {
+  int s, h, blk;
+  pair_and_block(H, &s, &h, &blk);
+  long long start;
+  int len;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
+  int t0, t1;
+  block_range(len, blk, &t0, &t1);
+  const int vpr = row_bytes / 16;
+  const int nvec = (t1 - t0) * vpr;
+  constexpr int kBatch = 8;
+  for (int base = threadIdx.x; base < nvec; base += kCopyThreads * kBatch) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / vpr, c = idx % vpr;
+        const long long row = (start + (len - 1 - t)) * H + h;
+        r[b] = __ldg(reinterpret_cast<const uint4*>(src + row * row_bytes) + c);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + b * kCopyThreads;
+      if (idx < nvec) {
+        const int t = t0 + idx / vpr, c = idx % vpr;
+        const long long row = (start + t) * H + h;
+        reinterpret_cast<uint4*>(dst + row * row_bytes)[c] = r[b];
+      }
+    }
+  }
+}
+
 // Workspace sections, each starting on a 256-byte boundary.
 struct TcWorkspace {
   size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, dq32, rdk32, rdv32, total;
@@ -284,14 +395,64 @@ TcWorkspace workspace_layout(int B, int H, long long rows) {
   return w;
 }
 
+// Per-key-channel gate: the workspace of the dv run.
+struct TcVecWorkspace {
+  size_t rq, rk, rdo, rg, dfs, rdv, total;
+};
+
+TcVecWorkspace vec_workspace_layout(int B, int H, long long rows) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t tok = (size_t)rows * H;
+  TcVecWorkspace w;
+  size_t o = 0;
+  w.rq = o;   o += up(tok * kTcDK * 2);
+  w.rk = o;   o += up(tok * kTcDK * 2);
+  w.rdo = o;  o += up(tok * kTcDV * 2);
+  w.rg = o;   o += up(tok * kTcDK * 4);
+  w.dfs = o;  o += up((size_t)B * H * kTcDK * kTcDV * 4);
+  w.rdv = o;  o += up(tok * kTcDV * 4);
+  w.total = o;
+  return w;
+}
+
 }  // namespace
 
 bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate) {
-  return !fp32_io && !vector_gate && dk == kTcDK && dv == kTcDV;
+  (void)vector_gate;  // the per-key-channel gate takes the tensor-core path for dv
+  return !fp32_io && dk == kTcDK && dv == kTcDV;
 }
 
-size_t chunk_bwd_tc_workspace(int B, int H, long long rows) {
-  return workspace_layout(B, H, rows).total;
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows, bool vector_gate) {
+  return vector_gate ? vec_workspace_layout(B, H, rows).total
+                     : workspace_layout(B, H, rows).total;
+}
+
+cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
+                                       cudaStream_t stream) {
+  const long long rows = a.cu_seqlens ? (long long)a.T : (long long)a.B * a.T;
+  const TcVecWorkspace w = vec_workspace_layout(a.B, a.H, rows);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  auto fl = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  const unsigned grid = (unsigned)((long long)a.B * a.H * kBlocksPerPair);
+  bwd_tc_prep_vec_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.d_out, a.g,
+      1.f / a.scale, a.d_final, bf(w.rq), bf(w.rk), bf(w.rdo), fl(w.rg), fl(w.dfs),
+      a.cu_seqlens, a.B, a.H, a.T, a.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // dv (reversed): the per-key-channel prefill of (k, q, do) with dS_T / scale
+  ChunkArgs c{};
+  c.q = bf(w.rk); c.k = bf(w.rq); c.v = bf(w.rdo); c.g = fl(w.rg);
+  c.scale = a.scale; c.init_state = a.d_final ? fl(w.dfs) : nullptr;
+  c.out = ws + w.rdv; c.final_state = nullptr; c.cu_seqlens = a.cu_seqlens;
+  c.B = a.B; c.H = a.H; c.T = a.T; c.dk = kTcDK; c.dv = kTcDV; c.chunk = 128;
+  c.fp32_io = false; c.fp32_out = a.fp32_out; c.vector_gate = true; c.status = a.status;
+  if ((e = launch_chunk_tc_vec(c, stream)) != cudaSuccess) return e;
+  bwd_tc_unreverse_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      ws + w.rdv, static_cast<uint8_t*>(a.dv), kTcDV * (a.fp32_out ? 4 : 2), a.cu_seqlens, a.B,
+      a.H, a.T, a.status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream) {

@@ -93,6 +93,7 @@ struct ChunkBwdArgs {
   bool fp32_io;
   bool fp32_out;
   bool vector_gate;
+  bool skip_dv;             // the CUDA-core kernels leave dv to another path
   unsigned* status;
 };
 
@@ -110,11 +111,15 @@ cudaError_t launch_chunk_bwd_head_bf16(const ChunkBwdArgs& a, cudaStream_t strea
 cudaError_t launch_chunk_bwd_head_f32(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_f32(const ChunkBwdArgs& a, cudaStream_t stream);
-// the per-head-gate backward on the tensor cores (three prefill runs), bf16,
-// d_k = d_v = 128; needs chunk_bwd_tc_workspace(B, H, rows) bytes of workspace
+// the backward on the tensor cores, bf16, d_k = d_v = 128, with
+// chunk_bwd_tc_workspace(B, H, rows, vector_gate) bytes of workspace: per-head
+// gate, every gradient from three prefill runs; per-key-channel gate, dv from
+// one run of the per-key-channel prefill (dq, dk on the CUDA cores)
 bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate);
-size_t chunk_bwd_tc_workspace(int B, int H, long long rows);
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows, bool vector_gate);
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream);
+cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
+                                       cudaStream_t stream);
 // the fixed device workspace of gla_chunk_bwd_fixed_workspace (a static array;
 // its address, or null with *err set)
 constexpr size_t kBwdFixedWorkspaceBytes = 384ull << 20;

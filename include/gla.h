@@ -246,15 +246,19 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
  *   d_init_state  fp32 [B, H, dk, dv], or NULL (not written)
  *   workspace     device scratch owned by the caller, or NULL; with at least
  *                 gla_chunk_bwd_workspace_size(...) bytes (256-byte aligned),
- *                 bf16 I/O, the per-head gate and dk = dv = 128, the call runs
- *                 on the tensor cores: the gradient of the recurrence is the
- *                 same recurrence with its operands exchanged -- dq is the
- *                 prefill of (d_out, v, k), dk and dv are prefills of (v,
- *                 d_out, q) and (k, q, d_out) run backwards in time -- so it
- *                 runs the tcgen05 prefill kernel three times between a
- *                 reversing pass and a finishing pass (accuracy that of the
- *                 prefill: bf16 operands, fp32 accumulation).  Otherwise
- *                 (or with a smaller workspace) the fp32 CUDA-core kernels run.
+ *                 bf16 I/O and dk = dv = 128, the call uses the tensor cores:
+ *                 the gradient of the recurrence is the same recurrence with
+ *                 its operands exchanged -- dq is the prefill of (d_out, v, k),
+ *                 dk and dv are prefills of (v, d_out, q) and (k, q, d_out) run
+ *                 backwards in time.  Per-head gate: the tcgen05 prefill kernel
+ *                 runs three times between a reversing pass and a finishing
+ *                 pass.  Per-key-channel gate: dv is one reversed run of the
+ *                 per-key-channel tcgen05 prefill (whose decay falls on the
+ *                 state's rows, as dv's does); dq and dk, whose decays fall on
+ *                 the value side, stay on the CUDA cores.  Tensor-core results
+ *                 have the prefill's accuracy (bf16 operands, fp32
+ *                 accumulation).  Otherwise (or with a smaller workspace) the
+ *                 fp32 CUDA-core kernels run.
  *   flags         GLA_FLAG_FP32_IO, GLA_FLAG_VECTOR_GATE, GLA_FLAG_FP32_OUT
  * The outputs and the workspace must not overlap one another or any input.
  * Empty sequences write d_init_state = d_final_state (or zeros).

@@ -212,7 +212,41 @@ def test_full_size_sampled_pairs(gate):
 def test_tc_path_is_taken_only_where_it_applies():
     from gated_linear_attention_gla_gb300 import _binding as b
     assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, 0) > 0
-    assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, b.GLA_FLAG_VECTOR_GATE) == 0
+    assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, b.GLA_FLAG_VECTOR_GATE) > 0
+    assert b.chunk_bwd_workspace_size(2, 3, 200, 96, 192, 0, 0) == 0
+    assert b.chunk_bwd_workspace_size(2, 3, 200, 128, 128, 0, b.GLA_FLAG_FP32_IO) == 0
+
+
+@pytest.mark.parametrize("T", [200, 300])
+def test_tc_per_key_channel_gate(T):
+    """Per-key-channel gate with a workspace: dq, dk, dg and d_init from the
+    CUDA-core kernels (their tolerances), dv from the reversed run of the
+    per-key-channel tensor-core prefill (the prefill's tolerance)."""
+    x, gr = inputs(B=2, T=T, H=2, gate="vector", g_mu=2.0, g_div=4.0)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    ref = run_ref(x, gr)
+    check((got[0], got[1], None, got[3], got[4]), ref, label="tc vec (cuda-core part)")
+    check((None, None, got[2], None, None), ref, tol=TOL_GRAD_TC, label="tc vec dv")
+    g16 = run_gpu(x, gr, tc=True)
+    assert torch.equal(g16[2], got[2].to(torch.bfloat16))
+
+
+def test_tc_per_key_channel_gate_packed_and_full_size():
+    x, gr = inputs("varlen", lengths=[300, 0, 1, 129], H=2, gate="vector", g_mu=2.0, g_div=4.0)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check((None, None, got[2], None, None), run_ref(x, gr), tol=TOL_GRAD_TC,
+          label="tc vec packed dv")
+    x, gr = inputs(gate="vector", g_mu=2.0, g_div=4.0)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    for b, h in [(0, 0), (3, 15)]:
+        sub = dict(x)
+        for key in ("q", "k", "v", "g"):
+            sub[key] = x[key][b:b + 1, :, h:h + 1]
+        sub["init_state"] = x["init_state"][b:b + 1, h:h + 1]
+        sgr = dict(d_out=gr["d_out"][b:b + 1, :, h:h + 1],
+                   d_final_state=gr["d_final_state"][b:b + 1, h:h + 1])
+        check((None, None, got[2][b:b + 1, :, h:h + 1], None, None), run_ref(sub, sgr),
+              tol=TOL_GRAD_TC, label=f"tc vec full dv ({b},{h})")
 
 
 def test_tc_backward_matches_oracle():
