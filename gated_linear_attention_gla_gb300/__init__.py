@@ -205,6 +205,11 @@ def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
     if tensor_cores:
         ws_bytes = _binding.chunk_bwd_workspace_size(B, H, T, dk, dv, cu_seqlens is not None,
                                                      flags)
+        if workspace is not None:
+            _check(workspace.is_cuda and workspace.device == q.device and
+                   workspace.dtype == torch.uint8 and workspace.is_contiguous() and
+                   workspace.data_ptr() % 256 == 0,
+                   "workspace must be a contiguous, 256-byte aligned uint8 tensor on q's GPU")
         if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
             workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     else:
