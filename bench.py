@@ -412,6 +412,25 @@ def time_mixer(gla, dev, hbm, reps=20, warmup=3):
                       "ms_plain": plain, "ms_with_epilogue": fused,
                       "epilogue_ms": fused - plain, "epilogue_bytes": epi_bytes,
                       "epilogue_frac_of_hbm": epi_bytes / ((fused - plain) / 1e3) / 1e9 / hbm}
+    # the per-key-channel workload: the prefill, then the pass over its output
+    wv = gla_inputs.WORKLOADS["vector"]
+    xv = gla_inputs.prefill_inputs(wv)
+    qv, kv, vv, gv = (xv[n].to(dev) for n in ("q", "k", "v", "g"))
+    mv = gla_inputs.mixer_inputs(wv, qv.shape[:-2])
+    mixv = {n: (t.to(dev) if torch.is_tensor(t) else t) for n, t in mv.items()}
+    outv = torch.empty(vv.shape, dtype=torch.bfloat16, device=dev)
+    kwv = dict(scale=xv["scale"], chunk=wv.chunk, out=outv, output_final_state=False)
+    plain_v = timed(lambda: gla.chunk_fwd(qv, kv, vv, gv, **kwv))
+    fused_v = timed(lambda: gla.chunk_fwd(qv, kv, vv, gv, mixer=mixv, **kwv))
+    units_v = wv.B * wv.T * wv.H
+    epi_v = units_v * 2 * (wv.dv + 2 * wv.dk + wv.dv + wv.dv + wv.dv)
+    res["prefill_vector"] = {
+        "workload": f"per-key-channel prefill B={wv.B} T={wv.T} H={wv.H} d={wv.dk}, epilogue "
+                    f"pass over the bf16 output",
+        "ms_plain": plain_v, "ms_with_epilogue": fused_v, "epilogue_ms": fused_v - plain_v,
+        "epilogue_bytes": epi_v,
+        "epilogue_frac_of_hbm": epi_v / ((fused_v - plain_v) / 1e3) / 1e9 / hbm}
+    del qv, kv, vv, gv, outv
     wd = gla_inputs.WORKLOADS["decode"]
     d = gla_inputs.decode_inputs(wd, steps=1)
     dq, dk_, dv_, dg = (d[n][0].to(dev) for n in ("q", "k", "v", "g"))

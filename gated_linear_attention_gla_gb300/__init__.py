@@ -94,8 +94,8 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
     returned ``final_state`` are fp32 ``[B, H, dk, dv]``.  ``out`` has q's dtype,
     or fp32 (``out_dtype=torch.float32``) for bf16 inputs.
 
-    ``mixer`` (optional dict): the steps after the readout, applied to out in
-    place by gla_mixer_epilogue -- ``aug`` fp32 [H, dk] (self-augmentation),
+    ``mixer`` (optional dict): the steps after the readout (gla_chunk_fwd_mixer:
+    the prefill, then a pass over out) -- ``aug`` fp32 [H, dk] (self-augmentation),
     ``norm_w`` fp32 [H, dv] and ``eps`` (head RMSNorm), ``z`` [.., H, dv] in
     q's dtype (SiLU output gate); absent keys skip their step.
     """
@@ -128,19 +128,19 @@ def chunk_fwd(q, k, v, g, scale: Optional[float] = None, init_state=None, cu_seq
     if final_state is None and output_final_state:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
     aug, norm_w, eps, z = _mixer_args(mixer, q, H, dk, dv, q.shape[:-2])
-    rc = _binding.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state),
-                                _ptr(out), _ptr(final_state), _ptr(cu_seqlens), B, H, T, dk,
-                                dv, chunk, _stream(stream), flags)
+    if mixer is None:
+        rc = _binding.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale, _ptr(init_state),
+                                    _ptr(out), _ptr(final_state), _ptr(cu_seqlens), B, H, T,
+                                    dk, dv, chunk, _stream(stream), flags)
+        name = "gla_chunk_fwd"
+    else:
+        rc = _binding.gla_chunk_fwd_mixer(_ptr(q), _ptr(k), _ptr(v), _ptr(g), scale,
+                                          _ptr(init_state), _ptr(out), _ptr(final_state),
+                                          _ptr(cu_seqlens), B, H, T, dk, dv, chunk, _ptr(aug),
+                                          _ptr(norm_w), eps, _ptr(z), _stream(stream), flags)
+        name = "gla_chunk_fwd_mixer"
     if rc != 0:
-        raise GlaError(rc, "gla_chunk_fwd")
-    if mixer is not None:
-        rows = q.numel() // (H * dk)
-        eflags = flags & (GLA_FLAG_FP32_IO | GLA_FLAG_FP32_OUT)
-        rc = _binding.gla_mixer_epilogue(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(aug),
-                                         _ptr(norm_w), eps, _ptr(z), rows, H, dk, dv,
-                                         _stream(stream), eflags)
-        if rc != 0:
-            raise GlaError(rc, "gla_mixer_epilogue")
+        raise GlaError(rc, name)
     return out, final_state
 
 

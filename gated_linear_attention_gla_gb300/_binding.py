@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
             L.gla_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp,
                                         _i, _i, _i, _i, _i, _i, _vp, ctypes.c_uint]
             L.gla_chunk_fwd.restype = _i
+            L.gla_chunk_fwd_mixer.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
+                                              _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                              ctypes.c_float, _vp, _vp, ctypes.c_uint]
+            L.gla_chunk_fwd_mixer.restype = _i
             L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                           _i, _i, _i, _i, _vp, ctypes.c_uint]
             L.gla_decode_step.restype = _i
@@ -108,6 +112,16 @@ def gla_chunk_fwd(q, k, v, g, scale, init_state, out, final_state, cu_seqlens, B
                                init_state or None, out or None, final_state or None,
                                cu_seqlens or None, B, H, T, dk, dv, chunk, stream or None,
                                flags)
+
+
+def gla_chunk_fwd_mixer(q, k, v, g, scale, init_state, out, final_state, cu_seqlens, B, H, T,
+                        dk, dv, chunk, aug, norm_w, eps, z, stream, flags) -> int:
+    """Raw call: pointers are ints (0 = NULL), ``stream`` an int handle."""
+    n = lambda p: p or None  # noqa: E731
+    return lib().gla_chunk_fwd_mixer(n(q), n(k), n(v), n(g), float(scale), n(init_state),
+                                     n(out), n(final_state), n(cu_seqlens), B, H, T, dk, dv,
+                                     chunk, n(aug), n(norm_w), float(eps), n(z), n(stream),
+                                     flags)
 
 
 def gla_decode_step(q, k, v, g, scale, state_inout, out, N, H, dk, dv, stream, flags) -> int:

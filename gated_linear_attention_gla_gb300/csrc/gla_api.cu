@@ -105,10 +105,18 @@ const char* gla_status_string(gla_status status) {
   return "unknown status";
 }
 
-gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                         float scale, const float* init_state, void* out,
-                         float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
-                         int dk, int dv, int chunk, gla_stream_t stream, unsigned flags) {
+}  // extern "C"
+
+namespace {
+
+// gla_chunk_fwd, and with `mixer` (its aug / norm_w / eps / z; q, k, v, out and
+// the sizes are taken from the call) the mixer's steps after the readout as a
+// second launch over out.
+gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, const float* g,
+                          float scale, const float* init_state, void* out,
+                          float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                          int dk, int dv, int chunk, gla_stream_t stream, unsigned flags,
+                          const gla::EpilogueArgs* mixer) {
   if (!flags_ok(flags) || B < 0 || H < 0 || T < 0 || !std::isfinite(scale))
     return GLA_ERR_INVALID_ARG;
   if (!dk_ok(dk) || !dv_ok(dv)) return GLA_ERR_UNSUPPORTED;
@@ -148,6 +156,20 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if (overlap(final_state, st_b, q, qk_b) || overlap(final_state, st_b, k, qk_b) ||
       overlap(final_state, st_b, v, v_b) || overlap(final_state, st_b, g, g_b))
     return GLA_ERR_INVALID_ARG;
+  if (mixer) {
+    if (!std::isfinite(mixer->eps) || mixer->eps < 0.f) return GLA_ERR_INVALID_ARG;
+    if (!aligned(mixer->aug, 16) || !aligned(mixer->norm_w, 16) || !aligned(mixer->z, 16))
+      return GLA_ERR_MISALIGNED;
+    const size_t aug_b = mixer->aug ? (size_t)H * dk * 4 : 0;
+    const size_t w_b = mixer->norm_w ? (size_t)H * dv * 4 : 0;
+    const size_t z_b = mixer->z ? v_b : 0;
+    if (overlap(out, out_b, mixer->aug, aug_b) || overlap(out, out_b, mixer->norm_w, w_b) ||
+        overlap(out, out_b, mixer->z, z_b) || overlap(final_state, st_b, mixer->z, z_b) ||
+        overlap(final_state, st_b, mixer->aug, aug_b) ||
+        overlap(final_state, st_b, mixer->norm_w, w_b))
+      return GLA_ERR_INVALID_ARG;
+    if (!mixer->aug && !mixer->norm_w && !mixer->z) mixer = nullptr;  // nothing to apply
+  }
 
   cudaError_t err;
   unsigned* status = status_word(&err);
@@ -169,7 +191,37 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const floa
     err = gla::launch_chunk_tc_vec(a, s);
   else
     err = gla::launch_chunk_simt(a, s);
+  if (err == cudaSuccess && mixer && rows > 0) {
+    gla::EpilogueArgs e = *mixer;
+    e.out = out; e.q = q; e.k = k; e.v = v; e.rows = rows; e.H = H; e.dk = dk; e.dv = dv;
+    e.fp32_io = fp32; e.fp32_out = f32out;
+    err = gla::launch_epilogue(e, s);
+  }
   return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         float scale, const float* init_state, void* out,
+                         float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                         int dk, int dv, int chunk, gla_stream_t stream, unsigned flags) {
+  return chunk_fwd_impl(q, k, v, g, scale, init_state, out, final_state, cu_seqlens, B, H, T,
+                        dk, dv, chunk, stream, flags, nullptr);
+}
+
+gla_status gla_chunk_fwd_mixer(const void* q, const void* k, const void* v, const float* g,
+                               float scale, const float* init_state, void* out,
+                               float* final_state, const int32_t* cu_seqlens, int B, int H,
+                               int T, int dk, int dv, int chunk, const float* aug,
+                               const float* norm_w, float eps, const void* z,
+                               gla_stream_t stream, unsigned flags) {
+  gla::EpilogueArgs m{};
+  m.aug = aug; m.norm_w = norm_w; m.eps = eps; m.z = z;
+  return chunk_fwd_impl(q, k, v, g, scale, init_state, out, final_state, cu_seqlens, B, H, T,
+                        dk, dv, chunk, stream, flags, &m);
 }
 
 size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int packed,

@@ -202,6 +202,22 @@ gla_status gla_mixer_epilogue(void *out, const void *q, const void *k, const voi
                               unsigned flags);
 
 /*
+ * gla_chunk_fwd_mixer -- gla_chunk_fwd followed by the mixer's steps after the
+ * readout (as gla_mixer_epilogue) on its output, in one call: the prefill, then
+ * a second launch over `out` (a pass at ~70 % of HBM bandwidth).  Arguments:
+ * those of gla_chunk_fwd, plus aug, norm_w, eps and z as for
+ * gla_mixer_epilogue (z shaped like out, in q's dtype); each step is skipped
+ * when its pointer is NULL.  Alignment: as gla_chunk_fwd, and aug, norm_w, z
+ * 16-byte aligned.
+ */
+gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, const float *g,
+                               float scale, const float *init_state, void *out,
+                               float *final_state, const int32_t *cu_seqlens, int B, int H,
+                               int T, int dk, int dv, int chunk, const float *aug,
+                               const float *norm_w, float eps, const void *z,
+                               gla_stream_t stream, unsigned flags);
+
+/*
  * gla_decode_step_mixer -- the decode step with the mixer's steps after the
  * readout fused into it (one CTA owns a head's whole output row).
  *

@@ -157,7 +157,8 @@ def test_decode_step_empty_is_no_op(L):
 def test_ctypes_signatures_match_header(L):
     """The binding's argument counts equal the header's parameter counts."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    for name in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_chunk_bwd_fixed_workspace",
+    for name in ("gla_chunk_fwd", "gla_chunk_fwd_mixer", "gla_chunk_bwd",
+                 "gla_chunk_bwd_fixed_workspace",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_slots",
                  "gla_decode_step_mixer", "gla_mixer_epilogue", "gla_status_sync",
                  "gla_status_string"):
@@ -278,3 +279,21 @@ def test_chunk_bwd_fixed_workspace_rejects_before_launch(L):
     assert call(dq=FAKE[0]) == E.GLA_ERR_INVALID_ARG       # dq overlaps q
     assert call(scale=float("nan")) == E.GLA_ERR_INVALID_ARG
     assert call(T=-1) == E.GLA_ERR_INVALID_ARG
+
+
+def test_chunk_fwd_mixer_rejects_before_launch(L):
+    def call(**kw):
+        a = dict(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], init=FAKE[4], out=FAKE[5],
+                 final=FAKE[6], aug=FAKE[7], norm_w=FAKE[8], eps=1e-6, z=FAKE[9], flags=0)
+        a.update(kw)
+        return _binding.gla_chunk_fwd_mixer(a["q"], a["k"], a["v"], a["g"], 0.1, a["init"],
+                                            a["out"], a["final"], 0, 2, 4, 256, 128, 128, 128,
+                                            a["aug"], a["norm_w"], a["eps"], a["z"], 0,
+                                            a["flags"])
+    assert call(eps=-1.0) == E.GLA_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == E.GLA_ERR_INVALID_ARG
+    assert call(aug=FAKE[7] + 4) == E.GLA_ERR_MISALIGNED
+    assert call(z=FAKE[5] + 64) == E.GLA_ERR_INVALID_ARG     # z inside out
+    assert call(aug=FAKE[5]) == E.GLA_ERR_INVALID_ARG        # aug inside out
+    assert call(q=FAKE[0] + 8) == E.GLA_ERR_MISALIGNED       # the prefill's own checks
+    assert call(out=FAKE[0]) == E.GLA_ERR_INVALID_ARG

@@ -1,6 +1,7 @@
 """The mixer's steps after the readout (self-augmentation, head RMSNorm, SiLU
 output gate) on the GPU, against the fp64 oracle: after every prefill kernel
-(gla_mixer_epilogue over its output) and fused into the decode step.
+(gla_chunk_fwd_mixer: the prefill, then a pass over its output) and fused into
+the decode step.
 
 The check is split in two.  The readout o itself must match the oracle within
 the output tolerance (as everywhere); the epilogue, applied by the GPU to that
@@ -148,3 +149,45 @@ def test_decode_mixer_on_slot_pages(cuda_ok):
                                   z=m["z"][live])
     assert rel_max(to_np(out[live]), y_ref) <= 1e-5
     assert (out[1] == 0).all()
+
+
+def _vector_case(seed=41, **over):
+    w = gla_inputs.WORKLOADS["vector"]
+    kw = dict(B=2, T=300, H=4, init_std=0.02)
+    kw.update(over)
+    x = gla_inputs.prefill_inputs(w, seed=seed, **kw)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=seed, H=kw.get("H", 4))
+    return x, m
+
+
+def _run_vector(x, m, out_dtype):
+    gla = _gla()
+    mix = {k: cuda(v) if torch.is_tensor(v) else v for k, v in m.items()}
+    args = (cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]))
+    kw = dict(scale=x["scale"], init_state=cuda(x["init_state"]),
+              cu_seqlens=cuda(x["cu_seqlens"]), chunk=128, out_dtype=out_dtype)
+    o, _ = gla.chunk_fwd(*args, **kw)
+    y, _ = gla.chunk_fwd(*args, mixer=mix, **kw)
+    gla.status_sync()
+    return o, y
+
+
+def test_vector_mixer_on_wide_chunks(cuda_ok):
+    """Strong per-channel decays make every chunk "wide" (processed token by
+    token by the per-key-channel kernel); the steps follow as for any output."""
+    x, m = _vector_case(g_mu=-1.0, g_div=1.0)
+    o, y = _run_vector(x, m, torch.float32)
+    o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                init_state=x["init_state"])
+    assert rel_max(to_np(o), o_ref) <= out_tol(torch.bfloat16)
+    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, "all"))
+    assert e <= 1e-5, f"epilogue error {e:.3e}"
+
+
+def test_vector_mixer_packed(cuda_ok):
+    w = gla_inputs.WORKLOADS["vector"]
+    x = gla_inputs.prefill_inputs(w, seed=43, lengths=[300, 0, 1, 129], H=2, init_std=0.02)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=43, H=2)
+    o, y = _run_vector(x, m, torch.float32)
+    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, "all"))
+    assert e <= 1e-5, f"epilogue error {e:.3e}"
