@@ -98,15 +98,19 @@ epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __res
   if (unit >= units) return;
   const int h = (int)(unit % H);
   const long long ob = unit * DV + lane * PER;
-  float o[PER];
+  const long long kb = unit * DK + lane * PK;
+  // every load of the row first, so that they are all in flight together
+  float o[PER], vv[PER], zz[PER], w[PER], qv[PK], kv[PK], av[PK];
   load_run<PER>(out + ob, o);
   if (aug != nullptr) {
-    const long long kb = unit * DK + lane * PK;
-    float qv[PK], kv[PK], av[PK], vv[PER];
     load_run<PK>(q + kb, qv);
     load_run<PK>(k + kb, kv);
     load_run<PK>(aug + h * DK + lane * PK, av);
     load_run<PER>(v + ob, vv);
+  }
+  if (norm_w != nullptr) load_run<PER>(norm_w + h * DV + lane * PER, w);
+  if (z != nullptr) load_run<PER>(z + ob, zz);
+  if (aug != nullptr) {
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < PK; ++i) s = fmaf(qv[i] * av[i], kv[i], s);
@@ -121,14 +125,10 @@ epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __res
     for (int c = 0; c < PER; ++c) ss = fmaf(o[c], o[c], ss);
     ss = warp_sum(ss);
     const float r = rsqrtf(ss / DV + eps);
-    float w[PER];
-    load_run<PER>(norm_w + h * DV + lane * PER, w);
 #pragma unroll
     for (int c = 0; c < PER; ++c) o[c] *= r * w[c];
   }
   if (z != nullptr) {
-    float zz[PER];
-    load_run<PER>(z + ob, zz);
 #pragma unroll
     for (int c = 0; c < PER; ++c) o[c] *= zz[c] / (1.f + expf(-zz[c]));
   }
