@@ -345,9 +345,17 @@ struct DqSmem {
   static constexpr int LDV = DV + 4;  // 16-byte rows, 4 banks apart
   static constexpr int GW = VEC ? kIS : 1;
   static constexpr int kFloats =
-      2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP + kIS * LDV;
+      2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP + kIS * LDV + (VEC ? kC * kIS : 0);
   static constexpr size_t kBytes = sizeof(float) * (size_t)kFloats;
 };
+
+// Per-key-channel gate: the in-chunk decays e^{G_t[i] - G_u[i]} of pairs in
+// different 16-token sub-blocks are split at a sub-block boundary b between
+// them, e^{G_t - G_b} e^{G_b - G_u} (both factors <= 1), so that one factor
+// folds into the operand rows and the other into the result, one exp per
+// (row, channel, sub-block); only pairs inside one sub-block take an exp each.
+// Thread rows t = ty + 16 m lie in sub-block m.
+constexpr int kSub = 16;
 
 template <typename IO, int DK, int DV, bool VEC>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -366,6 +374,7 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   float* sG = sQ + kC * kIS;     // [kC][GW]
   float* sP = sG + kC * GW;      // [kC][kLDP]
   float* sS = sP + kC * kLDP;    // [kIS][LDV]: the state's rows i0 .. i0 + 31
+  float* sKh = sS + kIS * LDV;   // [kC][kIS]: k e^{G_b - G} to its sub-block's end b (VEC)
 
   const int slice = blockIdx.x % NS;
   const int h = (blockIdx.x / NS) % H;
@@ -416,28 +425,45 @@ bwd_dq_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     {
       float intra[4][2] = {}, inter[4][2] = {};
       if constexpr (VEC) {
-        float gt[4][2];
+        // u in an earlier sub-block: through that sub-block's last token b
+        for (int idx = tid; idx < kC * kIS; idx += kBwdThreads) {
+          const int u = idx / kIS, i = idx - u * kIS;
+          sKh[idx] = sK[idx] * exp2f(sG[(u | (kSub - 1)) * kIS + i] - sG[u * kIS + i]);
+        }
+        __syncthreads();
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 4; ++m) {
+          const int t = ty + 16 * m;
+          float gt[2];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) gt[m][c] = sG[(ty + 16 * m) * kIS + tx + 16 * c];
-#pragma unroll 2
-        for (int u = 0; u < kC; ++u) {
-          float a[4], b[2], gu[2];
+          for (int c = 0; c < 2; ++c) gt[c] = sG[t * kIS + tx + 16 * c];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) a[m] = sP[(ty + 16 * m) * kLDP + u];
+          for (int bu = 0; bu < m; ++bu) {
+            float part[2] = {0.f, 0.f};
+#pragma unroll 4
+            for (int uu = 0; uu < kSub; ++uu) {
+              const int u = kSub * bu + uu;
+              const float a = sP[t * kLDP + u];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            b[c] = sK[u * kIS + tx + 16 * c];
-            gu[c] = sG[u * kIS + tx + 16 * c];
+              for (int c = 0; c < 2; ++c) part[c] = fmaf(a, sKh[u * kIS + tx + 16 * c], part[c]);
+            }
+            const int b = kSub * bu + kSub - 1;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              intra[m][c] =
+                  fmaf(part[c], exp2f(gt[c] - sG[b * kIS + tx + 16 * c]), intra[m][c]);
           }
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
+          // u in t's own sub-block, u <= t: one exp each (P is zero past t)
+#pragma unroll 4
+          for (int uu = 0; uu < kSub; ++uu) {
+            const int u = kSub * m + uu;
+            const float a = sP[t * kLDP + u];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const float e = (u <= ty + 16 * m) ? exp2f(gt[m][c] - gu[c]) : 0.f;
-              intra[m][c] = fmaf(a[m] * b[c], e, intra[m][c]);
+              const float e = u <= t ? exp2f(gt[c] - sG[u * kIS + tx + 16 * c]) : 0.f;
+              intra[m][c] = fmaf(a * sK[u * kIS + tx + 16 * c], e, intra[m][c]);
             }
+          }
         }
       } else {
         gemm_nn<4, 2>(intra, sP, kLDP, sK, kIS, kC);
@@ -520,8 +546,8 @@ template <int DK, int DV, bool VEC>
 struct DkSmem {
   static constexpr int LDV = DV + 4;  // 16-byte rows, 4 banks apart
   static constexpr int GW = VEC ? kIS : 1;
-  static constexpr int kFloats =
-      2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP + kIS * LDV + (VEC ? kC * kIS : 0);
+  static constexpr int kFloats = 2 * kC * LDV + 2 * kC * kIS + kC * GW + kC * kLDP +
+                                kIS * LDV + (VEC ? 2 * kC * kIS : 0);
   static constexpr size_t kBytes = sizeof(float) * (size_t)kFloats;
 };
 
@@ -543,6 +569,7 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
   float* sP = sG + kC * GW;      // [kC][kLDP]
   float* sR = sP + kC * kLDP;    // [kIS][LDV]: rows i0 .. i0 + 31 of the carried gradient
   float* sX = sR + kIS * LDV;    // [kC][kIS]: dg terms (per-key-channel gate)
+  float* sQh = sX + kC * kIS;    // [kC][kIS]: q e^{G - G_b} from the boundary b before its sub-block
 
   const int slice = blockIdx.x % NS;
   const int h = (blockIdx.x / NS) % H;
@@ -595,28 +622,45 @@ bwd_dk_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const IO* __re
     {
       float intra[4][2] = {}, inter[4][2] = {};
       if constexpr (VEC) {
-        float gt[4][2];
+        // u in a later sub-block: through the token b just before that sub-block
+        for (int idx = kSub * kIS + tid; idx < kC * kIS; idx += kBwdThreads) {
+          const int u = idx / kIS, i = idx - u * kIS;
+          sQh[idx] = sQ[idx] * exp2f(sG[u * kIS + i] - sG[((u & ~(kSub - 1)) - 1) * kIS + i]);
+        }
+        __syncthreads();
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 4; ++m) {
+          const int t = ty + 16 * m;
+          float gt[2];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) gt[m][c] = sG[(ty + 16 * m) * kIS + tx + 16 * c];
-#pragma unroll 2
-        for (int u = 0; u < kC; ++u) {
-          float a[4], b[2], gu[2];
+          for (int c = 0; c < 2; ++c) gt[c] = sG[t * kIS + tx + 16 * c];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) a[m] = sP[u * kLDP + ty + 16 * m];
+          for (int bu = m + 1; bu < 4; ++bu) {
+            float part[2] = {0.f, 0.f};
+#pragma unroll 4
+            for (int uu = 0; uu < kSub; ++uu) {
+              const int u = kSub * bu + uu;
+              const float a = sP[u * kLDP + t];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            b[c] = sQ[u * kIS + tx + 16 * c];
-            gu[c] = sG[u * kIS + tx + 16 * c];
+              for (int c = 0; c < 2; ++c) part[c] = fmaf(a, sQh[u * kIS + tx + 16 * c], part[c]);
+            }
+            const int b = kSub * bu - 1;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              intra[m][c] =
+                  fmaf(part[c], exp2f(sG[b * kIS + tx + 16 * c] - gt[c]), intra[m][c]);
           }
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
+          // u in t's own sub-block, u >= t: one exp each (P[u][t] is zero for u < t)
+#pragma unroll 4
+          for (int uu = 0; uu < kSub; ++uu) {
+            const int u = kSub * m + uu;
+            const float a = sP[u * kLDP + t];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const float e = (u >= ty + 16 * m) ? exp2f(gu[c] - gt[m][c]) : 0.f;
-              intra[m][c] = fmaf(a[m] * b[c], e, intra[m][c]);
+              const float e = u >= t ? exp2f(sG[u * kIS + tx + 16 * c] - gt[c]) : 0.f;
+              intra[m][c] = fmaf(a * sQ[u * kIS + tx + 16 * c], e, intra[m][c]);
             }
+          }
         }
       } else {
 #pragma unroll 4
