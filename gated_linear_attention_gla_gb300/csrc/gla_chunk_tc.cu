@@ -299,13 +299,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // ------------------------------------------- producer: gate sums and TMA
     // All lanes: prefix sums of g for chunk c (lane l owns tokens 4l .. 4l+3)
     // into the gate ring; lane 0: the TMA loads of chunk c.
+    // raw values: the clamp is applied where they are used, an iteration or more
+    // later, so that nothing waits for these loads in the iteration that issues them
     auto load4 = [&](int c, float (&gv)[4]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = c * kC + 4 * lane + i;
-        gv[i] = (c < nch && t < len) ? fmaxf(__ldg(p.g + (start + t) * p.H + h), -kGateClamp)
-                                     : 0.f;
+        gv[i] = (c < nch && t < len) ? __ldg(p.g + (start + t) * p.H + h) : 0.f;
       }
+    };
+    auto clamp4 = [](const float (&x)[4]) {
+      return fmaxf(x[0], -kGateClamp) + fmaxf(x[1], -kGateClamp) + fmaxf(x[2], -kGateClamp) +
+             fmaxf(x[3], -kGateClamp);
     };
     // sum over the warp of a per-lane value
     auto warp_sum = [&](float x) {
@@ -314,12 +319,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       return x;
     };
     const int bidx = packed ? 0 : s;
-    // g of chunks c + 1 and c + 2 are loaded one and two iterations ahead: their
-    // totals decide whether MMA4(c) needs the lo half of W V (the final state
-    // sees chunk c's rounding scaled by the decay still to come)
-    float gnext[4], gnext2[4];
+    // The totals of g over chunks c + 1 and c + 2 decide whether MMA4(c) needs the
+    // lo half of W V (the final state sees chunk c's rounding scaled by the decay
+    // still to come).  g is loaded three chunks ahead, so that those sums never
+    // wait for a load issued in the same iteration (this warp's gate sums and TMA
+    // issues pace every other role).
+    float gnext[4], gnext2[4], gnext3[4];
     load4(0, gnext);
     load4(1, gnext2);
+    load4(2, gnext3);
     for (int c = 0; c < nch; ++c) {
       bool ok = true;
       float gv[4];
@@ -327,13 +335,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int i = 0; i < 4; ++i) {
         gv[i] = gnext[i];
         gnext[i] = gnext2[i];
+        gnext2[i] = gnext3[i];
       }
-      load4(c + 2, gnext2);
-      const float rest = warp_sum(gnext[0] + gnext[1] + gnext[2] + gnext[3]) +
-                         warp_sum(gnext2[0] + gnext2[1] + gnext2[2] + gnext2[3]);
+      load4(c + 3, gnext3);
+      const float rest = warp_sum(clamp4(gnext)) + warp_sum(clamp4(gnext2));
       if (c >= kSlots && !wait(kGFree0 + c % kSlots, ph(c / kSlots - 1))) ok = false;
       if (__any_sync(0xffffffffu, !ok)) break;
       float* slot = slot_of(c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gv[i] = fmaxf(gv[i], -kGateClamp);
       float run[4];
       run[0] = gv[0];
 #pragma unroll
