@@ -14,7 +14,7 @@
  * "Simple GLA" with a per-head decay -- or one value per (token, head, key
  * channel), where row i of S decays by exp(g_t[i]).
  *
- * Two serving forms are exported:
+ * Entry points:
  *   gla_chunk_fwd    prefill: the chunked form of the same page's section
  *                    "Challenge 1" (Figure 3) -- per chunk a causal Q K^T
  *                    weighted by the decays, times V, plus the carried-in
@@ -23,14 +23,26 @@
  *   gla_decode_step  one token for each of N concurrent sequences, each with a
  *                    fixed-size state page updated in place (section
  *                    "Inference optimization on Trainium2": one fixed page per
- *                    sequence).
+ *                    sequence); gla_decode_step_slots takes the pages from a
+ *                    pool by slot index (for padded, graph-replayed batches).
+ *   gla_mixer_epilogue, gla_chunk_fwd_mixer, gla_decode_step_mixer
+ *                    the mixer's steps after the readout (self-augmentation,
+ *                    head RMSNorm, SiLU output gate): over a finished output,
+ *                    after a prefill in one call, fused into the decode step.
  *   gla_chunk_bwd    the gradient of the prefill (dq, dk, dv, dg and the
- *                    initial state's gradient) for training.
+ *                    initial state's gradient) for training;
+ *                    gla_chunk_bwd_workspace_size sizes its tensor-core path's
+ *                    workspace, gla_chunk_bwd_fixed_workspace runs it on a
+ *                    buffer of the library's own.
+ *   gla_status_sync, gla_status_string, gla_last_error_string, gla_version,
+ *   gla_chunk_fwd_kernel
+ *                    diagnostics.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates or frees them; it keeps only one device status word per
- *     GPU (a static __device__ variable) and no other state.
+ *     never allocates or frees device memory; it keeps one device status word
+ *     per GPU and the fixed backward workspace (static __device__ variables)
+ *     and no other state.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Host-side
  *     argument checks happen before anything is enqueued: a call that returns
  *     an error has launched nothing and written nothing.
