@@ -261,6 +261,19 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn)
           tma_load_4d(smem + kOffV + pn * kPanel, &tmV, &bars[kVFull], pn * 64, h, row, bidx);
+        // every tile is single-buffered, so chunk c + 1's loads can only be issued
+        // once chunk c has released them: fetch its tiles into L2 now, so that
+        // those loads then wait for L2 rather than HBM
+        if (c + 1 < nch) {
+          const int nrow = row + kC;
+          tma_prefetch_l2_4d(&tmG, 0, h, nrow, bidx);
+#pragma unroll
+          for (int pn = 0; pn < 2; ++pn) {
+            tma_prefetch_l2_4d(&tmQ, pn * 64, h, nrow, bidx);
+            tma_prefetch_l2_4d(&tmK, pn * 64, h, nrow, bidx);
+            tma_prefetch_l2_4d(&tmV, pn * 64, h, nrow, bidx);
+          }
+        }
       }
     }
   } else if (warp == 1) {

@@ -85,6 +85,18 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Prefetch a 4-D tile into L2 (no shared memory, no barrier): the later
+// tma_load_4d of the same box then reads from L2.  Boxes reaching past the
+// tensor's bounds fetch only what exists.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1,
+                                                   int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
