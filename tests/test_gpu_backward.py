@@ -380,3 +380,14 @@ def test_tc_minus_inf_gate_resets():
     xc = dict(x, g=x["g"].clamp(min=-30.0))
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
     check(got, run_ref(xc, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc -inf")
+
+
+def test_tc_per_key_channel_strong_decays():
+    """Per-key-channel gates around -1.3 make every chunk "wide" in the reversed
+    per-key-channel prefill run that gives dv (token by token there); the
+    reference is the oracle's gradient at max(g, -30)."""
+    x, gr = inputs(B=1, T=300, H=2, gate="vector", g_mu=-1.0, g_div=1.0)
+    xc = dict(x, g=x["g"].clamp(min=-30.0))
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check((None, None, got[2], None, None), run_ref(xc, gr), tol=TOL_GRAD_TC,
+          label="tc vec strong dv")
