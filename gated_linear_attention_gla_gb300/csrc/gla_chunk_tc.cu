@@ -18,9 +18,10 @@
 //     o_t = scale * exp(G_t - G_L) * ( Q S' + causal(A) (W V) )_t,  S' = exp(G_L) S
 // and the two contractions share one accumulator.
 //
-// Head sizes: d_k = 128, or 96 run as 128 (the TMA fills channels 96..127
-// with zeros, so those state rows stay zero and are never stored); d_v = 64,
-// 128 or 192 (one CTA per 64-wide slice).
+// Head sizes: d_k = 128, or 64 and 96 run as 128 (the TMA fills the channels
+// past d_k with zeros -- for d_k = 64 the whole second 64-channel panel lies
+// outside the tensor -- so those state rows stay zero and are never stored);
+// d_v = 64, 128 or 192 (one CTA per 64-wide slice).
 //
 // One CTA owns one (sequence, head, 64-wide slice of dv) and walks the chunks
 // in order.  The state slice S (dk x 64, fp32) lives in tensor memory (TMEM)
@@ -86,7 +87,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = 128;        // chunk (tokens)
-constexpr int kDK = 128;       // key head size of the tiles (d_k = 96 runs zero-padded)
+constexpr int kDK = 128;       // key head size of the tiles (d_k = 64, 96 run zero-padded)
 constexpr int kDVS = 64;       // value columns per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kMaskWarps = 4;
@@ -144,7 +145,7 @@ struct TcParams {
   void* out;
   float* final_state;
   const int32_t* cu_seqlens;
-  int B, H, T, DK, DV, nslices;  // DK = 96 runs as 128 with zero channels 96..127
+  int B, H, T, DK, DV, nslices;  // DK = 64, 96 run as 128 with zero channels DK..127
   int out_v8;  // out is 32-byte aligned: 256-bit stores
   unsigned* status;
 };
@@ -600,8 +601,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int half = (warp - 8) >> 2;     // which 32 of the 64 state / V columns
     const int r = 32 * q4 + lane;         // state row i (key channel), token row for W V
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    // state rows past the key head size (d_k = 96) stay zero: their K channels
-    // are the zero columns the TMA fills in
+    // state rows past the key head size (d_k = 64, 96) stay zero: their K
+    // channels are the zero columns the TMA fills in
     const bool row_ok = r < p.DK;
     const size_t st_off = ((size_t)s * p.H + h) * (size_t)p.DK * p.DV +
                           (size_t)(row_ok ? r : 0) * p.DV + (size_t)sl * kDVS + 32 * half;
@@ -778,7 +779,8 @@ bool make_map(CUtensorMap* map, const void* base, int d, int H, long long rows, 
 }  // namespace
 
 bool chunk_tc_supported(const ChunkArgs& a) {
-  return !a.fp32_io && !a.vector_gate && a.chunk == kC && (a.dk == 96 || a.dk == kDK) &&
+  return !a.fp32_io && !a.vector_gate && a.chunk == kC &&
+         (a.dk == 64 || a.dk == 96 || a.dk == kDK) &&
          (a.dv == 64 || a.dv == 128 || a.dv == 192);
 }
 

@@ -116,10 +116,11 @@ typedef enum gla_status {
  *               sequence (or packed rows).  B, H, T >= 0; with T = 0 (or empty
  *               sequences) final_state receives init_state (or zeros).
  *   dk, dv      head sizes: dk 64, 96 or 128; dv 64, 128 or 192
- *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O with
- *               dk = 128: the per-head gate with dv = 64 or 128, the
- *               per-key-channel gate with dv = 128), or 16, 32, 64 (fp32 SIMT
- *               path); fp32 I/O and the other head sizes take the SIMT path
+ *   chunk       tokens per chunk: 128 (tensor-core path for bf16 I/O: the
+ *               per-head gate with every head size above -- dk = 64 and 96
+ *               run zero-padded to 128 --, the per-key-channel gate with
+ *               dk = dv = 128), or 16, 32, 64 (fp32 SIMT path); fp32 I/O and
+ *               the other head sizes take the SIMT path
  *   stream      CUDA stream
  *   flags       GLA_FLAG_* bits; 0 = bf16 I/O, per-head gate
  *

@@ -122,6 +122,22 @@ def test_laplace_head_with_the_fixed_decay_schedule(cuda_ok):
     check(x, out, fin, *run_ref(x))
 
 
+@pytest.mark.parametrize("mu", [-3.0, 8.0, None])
+def test_tensor_core_key_head_64(cuda_ok, mu):
+    """d_k = 64 on the tensor-core kernel: the second 64-channel panel of Q and K
+    lies wholly outside the tensor and is zero-filled, so state rows 64..127
+    stay zero.  Packed sequences (an empty one, a length-1 one, one longer than
+    several chunks) with very strong (mu = -3), very weak (mu = 8) and the
+    workload's own decays."""
+    x = small(B=0, lengths=[300, 1, 0, 129, 520], H=3, dk=64, dv=128, init_std=0.05)
+    if mu is not None:
+        gen = torch.Generator().manual_seed(6)
+        x["g"] = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
+    out, fin = run_gpu(x)
+    check(x, out, fin, *run_ref(x))
+    assert torch.equal(fin[2].cpu(), x["init_state"][2])
+
+
 @pytest.mark.parametrize("gate", ["scalar", "vector"])
 def test_bf16_no_initial_state_no_final_state(cuda_ok, gate):
     x = small(B=2, T=300, H=2, gate=gate)

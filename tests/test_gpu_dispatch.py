@@ -1,9 +1,9 @@
 """Which kernel serves which call.
 
 The dispatch rule is a pure host function of the C ABI (checked on the CPU):
-bf16 I/O with chunk 128 and dk = 128 runs a tcgen05 tensor-core kernel (the
-per-head gate with dv = 64 or 128, the per-key-channel gate with dv = 128),
-everything else the fp32 CUDA-core kernel.  On a GPU, where the CUDA profiler
+bf16 I/O with chunk 128 runs a tcgen05 tensor-core kernel (the per-head gate
+with dk = 64, 96 or 128 and dv = 64, 128 or 192; the per-key-channel gate with
+dk = dv = 128), everything else the fp32 CUDA-core kernel.  On a GPU, where the CUDA profiler
 can trace kernels, the launched kernel names are checked as well."""
 import pytest
 import torch
@@ -29,7 +29,11 @@ def L():
     (128, 128, 128, F32OUT, "tensor_core"),
     (128, 128, 64, 0, "cuda_core"),
     (128, 128, 128, F32, "cuda_core"),
-    (64, 64, 128, 0, "cuda_core"),
+    (64, 64, 128, 0, "tensor_core"),
+    (64, 128, 128, 0, "tensor_core"),
+    (64, 192, 128, 0, "tensor_core"),
+    (64, 128, 128, VEC, "cuda_core"),
+    (64, 128, 128, F32, "cuda_core"),
     (128, 128, 128, VEC, "tensor_core"),
     (128, 128, 128, VEC | F32OUT, "tensor_core"),
     (128, 64, 128, VEC, "cuda_core"),
