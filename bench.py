@@ -500,7 +500,7 @@ def time_backward(gla, dev, reps=5, warmup=3):
                 "tensor": {"achieved_tflops": flops / sec / 1e12, "peak_tflops": bf16_peak,
                            "frac": flops / sec / 1e12 / bf16_peak, "algorithmic_flops": flops},
                 "workspace_bytes": ws.numel()}
-            entry["launches"] = 6
+            entry["launches"] = 6  # prepare, 3 x prefill, finish, dg scan
         elif tc:
             # mostly the CUDA-core dq and dk kernels: their fp32 roofline
             flops = backward_flops(w, w.B, w.T)
@@ -510,7 +510,7 @@ def time_backward(gla, dev, reps=5, warmup=3):
                 "unit": "TFLOP/s", "frac": flops / sec / 1e12 / peak,
                 "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
                 "algorithmic_flops": flops, "workspace_bytes": ws.numel()}
-            entry["launches"] = 5
+            entry["launches"] = 4  # prepare, per-key-channel prefill, dq, dk
         else:
             flops = backward_flops(w, w.B, w.T)
             peak = fp32_peak_tflops()
@@ -519,7 +519,9 @@ def time_backward(gla, dev, reps=5, warmup=3):
                 "unit": "TFLOP/s", "frac": flops / sec / 1e12 / peak,
                 "peak_source": "fp32 FMA lanes x 2 x max SM clock (derived)",
                 "algorithmic_flops": flops}
-            entry["launches"] = 4 if gate == "per-key-channel" else 5
+            # dq, dk, dv (+ the dg scan for the per-head gate, after a driver memset
+            # of dg that is not counted)
+            entry["launches"] = 3 if gate == "per-key-channel" else 4
         res.append(entry)
     return res
 

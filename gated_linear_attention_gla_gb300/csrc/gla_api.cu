@@ -175,7 +175,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
   unsigned* status = status_word(&err);
   if (!status) return cuda_status(err);
 
-  gla::ChunkArgs a;
+  gla::ChunkArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.scale = scale;
   a.init_state = init_state; a.out = out; a.final_state = final_state;
   a.cu_seqlens = cu_seqlens;

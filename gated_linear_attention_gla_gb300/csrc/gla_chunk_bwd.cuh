@@ -32,7 +32,7 @@
 //                  also the suffix sums (the CTA owns its columns of dg)
 //   bwd_dv_kernel  reverse sweep, one CTA per (sequence, head, 64 value
 //                  columns): dv
-//   bwd_dg_scan_kernel  per-head gate only: suffix sums of dg, one warp per
+//   bwd_dg_scan_kernel  per-head gate only: suffix sums of dg, one CTA per
 //                  (sequence, head)
 // The key-row and value-column splits keep every output owned by one CTA;
 // only the per-head gate's dg terms are summed across CTAs (fp32 atomics, so
@@ -910,28 +910,35 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
 // ---------------------------------------------------------------------------
 // per-head gate: dg_t <- sum_{u >= t} dg_u within each sequence (in place)
 // ---------------------------------------------------------------------------
-constexpr int kScanWarps = 8;
-constexpr int kScanPer = 8;  // tokens per lane per pass
+constexpr int kScanThreads = 256;
+constexpr int kScanPer = 8;  // tokens per thread per pass
 
-__global__ void __launch_bounds__(kScanWarps * 32)
+// One CTA per (sequence, head).  A pass covers the last kScanThreads *
+// kScanPer tokens not yet summed: thread i holds kScanPer consecutive tokens
+// (later tokens in higher threads), sums them from the back, and adds the
+// totals of every later thread (warp shuffles, then the warps' totals through
+// shared memory) and of every later pass (the carry).
+__global__ void __launch_bounds__(kScanThreads)
 bwd_dg_scan_kernel(float* __restrict__ dg, const int32_t* __restrict__ cu, int B, int H, int T,
                    unsigned* status) {
-  const int lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * kScanWarps + (threadIdx.x >> 5);
-  if (unit >= (long long)B * H) return;
+  constexpr int kWarps = kScanThreads / 32;
+  __shared__ float warp_total[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long unit = blockIdx.x;
+  if (unit >= (long long)B * H) return;  // whole CTA
   const int s = (int)(unit / H), h = (int)(unit % H);
   long long start;
   int len;
-  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
-  constexpr int kSpan = 32 * kScanPer;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;  // whole CTA
+  constexpr int kSpan = kScanThreads * kScanPer;
   float carry = 0.f;
   for (int end = len; end > 0; end -= kSpan) {
     const int lo = end - kSpan;  // may be negative: those tokens do not exist
     float x[kScanPer];
 #pragma unroll
     for (int r = 0; r < kScanPer; ++r) {
-      const int t = lo + kScanPer * lane + r;
-      x[r] = (t >= 0 && t < end) ? dg[(start + t) * H + h] : 0.f;
+      const int t = lo + kScanPer * (int)threadIdx.x + r;
+      x[r] = (t >= 0) ? dg[(start + t) * H + h] : 0.f;
     }
     float suf = 0.f;
 #pragma unroll
@@ -939,19 +946,29 @@ bwd_dg_scan_kernel(float* __restrict__ dg, const int32_t* __restrict__ cu, int B
       suf += x[r];
       x[r] = suf;
     }
-    float incl = suf;  // sum over this lane and every later lane
+    float incl = suf;  // sum over this thread and the later lanes of its warp
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float y = __shfl_down_sync(0xffffffffu, incl, off);
       if (lane + off < 32) incl += y;
     }
-    const float later = incl - suf + carry;
+    if (lane == 0) warp_total[warp] = incl;
+    __syncthreads();
+    float later_warps = 0.f, pass_total = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float v = warp_total[w];
+      pass_total += v;
+      if (w > warp) later_warps += v;
+    }
+    const float later = incl - suf + later_warps + carry;
 #pragma unroll
     for (int r = 0; r < kScanPer; ++r) {
-      const int t = lo + kScanPer * lane + r;
-      if (t >= 0 && t < end) dg[(start + t) * H + h] = x[r] + later;
+      const int t = lo + kScanPer * (int)threadIdx.x + r;
+      if (t >= 0) dg[(start + t) * H + h] = x[r] + later;
     }
-    carry += __shfl_sync(0xffffffffu, incl, 0);
+    carry += pass_total;
+    __syncthreads();  // warp_total is rewritten by the next pass
   }
 }
 
@@ -1000,9 +1017,8 @@ cudaError_t launch_shape(const ChunkBwdArgs& a, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.dg && !VEC) {
-    const unsigned grid = (unsigned)((pairs + kScanWarps - 1) / kScanWarps);
-    bwd_dg_scan_kernel<<<grid, kScanWarps * 32, 0, stream>>>(a.dg, a.cu_seqlens, a.B, a.H, a.T,
-                                                              a.status);
+    bwd_dg_scan_kernel<<<(unsigned)pairs, kScanThreads, 0, stream>>>(a.dg, a.cu_seqlens, a.B,
+                                                                      a.H, a.T, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -19,12 +19,13 @@
 //   dg:  dg_t = sum_{u >= t} sum_i (q_u[i] dq_u[i] - k_u[i] dk_u[i])
 //               + sum_ij S_T[i][j] dS_T[i][j].
 // The prefill kernel reads tokens in order, so a prepare pass writes the
-// reversed (and gate-shifted) copies into the caller's workspace, the three
-// prefill runs store fp32 results there, and a finish pass puts dk and dv back
-// in token order, rounds every gradient to its output dtype and forms the dg
-// terms from the fp32 values; the suffix sums reuse the CUDA-core backward's
-// scan kernel.  Launches: prepare, 3 x prefill, finish, and the scan when dg
-// is wanted.
+// reversed (and gate-shifted) copies into the caller's workspace.  The dv run
+// stores its rows back in token order (row len - 1 - tau for reversed position
+// tau), directly in the gradients' dtype; the dq and dk runs store fp32 results
+// in the workspace, and a finish pass puts dk back in token order, rounds both
+// to the output dtype and forms the dg terms from the fp32 values; the suffix
+// sums reuse the CUDA-core backward's scan kernel.  Launches: prepare,
+// 3 x prefill, finish, and the scan when dg is wanted.
 #include "gla_chunk_bwd.cuh"
 
 namespace gla {
@@ -147,15 +148,14 @@ __device__ __forceinline__ float warp_sum32(float x) {
   return x;
 }
 
-// Gradients in token order and output dtype, the per-token dg terms (q.dq -
+// dq and dk in token order and output dtype, the per-token dg terms (q.dq -
 // k.dk, plus the final-state term at the last token), and d_init's factor
 // scale * e^{g_0}.  One warp per token; lane l owns channels 4 l .. 4 l + 3.
 __global__ void __launch_bounds__(kCopyThreads, 2)
 bwd_tc_fin_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                   const float* __restrict__ g, float scale, const float* __restrict__ dq32,
-                  const float* __restrict__ rdk32, const float* __restrict__ rdv32,
-                  const float* __restrict__ stt, const float* __restrict__ dfst,
-                  void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
+                  const float* __restrict__ rdk32, const float* __restrict__ stt,
+                  const float* __restrict__ dfst, void* __restrict__ dq, void* __restrict__ dk,
                   bool out_f32, float* __restrict__ dg, float* __restrict__ d_init,
                   const int32_t* __restrict__ cu, int B, int H, int T, unsigned* status) {
   static_assert(kTcDK == 128 && kTcDV == 128, "four channels a lane");
@@ -223,23 +223,6 @@ bwd_tc_fin_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         x = warp_sum32(x);
         if (lane == 0) dg[row] = t == len - 1 ? x + c_t : x;
       }
-    }
-  }
-
-  // dv: back in token order and dtype, eight tokens a warp in flight
-  for (int tb = t0 + kTok * warp; tb < t1; tb += kTok * kWarps) {
-    float4 cv[kTok];
-#pragma unroll
-    for (int u = 0; u < kTok; ++u) {
-      const int t = min(tb + u, t1 - 1);
-      const long long rrow = (start + (len - 1 - t)) * H + h;
-      cv[u] = __ldg(reinterpret_cast<const float4*>(rdv32 + rrow * kTcDV) + lane);
-    }
-#pragma unroll
-    for (int u = 0; u < kTok; ++u) {
-      const int t = tb + u;
-      if (t >= t1) break;  // warp-uniform
-      store_row4(dv, ((start + t) * H + h) * kTcDV, lane, cv[u], out_f32);
     }
   }
 
@@ -329,48 +312,9 @@ bwd_tc_prep_vec_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
   }
 }
 
-// dv back in token order: row t of the output is row len - 1 - t of the
-// reversed run's output (same dtype), 16-byte vectors, eight in flight.
-__global__ void __launch_bounds__(kCopyThreads)
-bwd_tc_unreverse_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                        int row_bytes, const int32_t* __restrict__ cu, int B, int H, int T,
-                        unsigned* status) {
-  int s, h, blk;
-  pair_and_block(H, &s, &h, &blk);
-  long long start;
-  int len;
-  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
-  int t0, t1;
-  block_range(len, blk, &t0, &t1);
-  const int vpr = row_bytes / 16;
-  const int nvec = (t1 - t0) * vpr;
-  constexpr int kBatch = 8;
-  for (int base = threadIdx.x; base < nvec; base += kCopyThreads * kBatch) {
-    uint4 r[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int idx = base + b * kCopyThreads;
-      if (idx < nvec) {
-        const int t = t0 + idx / vpr, c = idx % vpr;
-        const long long row = (start + (len - 1 - t)) * H + h;
-        r[b] = __ldg(reinterpret_cast<const uint4*>(src + row * row_bytes) + c);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int idx = base + b * kCopyThreads;
-      if (idx < nvec) {
-        const int t = t0 + idx / vpr, c = idx % vpr;
-        const long long row = (start + t) * H + h;
-        reinterpret_cast<uint4*>(dst + row * row_bytes)[c] = r[b];
-      }
-    }
-  }
-}
-
 // Workspace sections, each starting on a 256-byte boundary.
 struct TcWorkspace {
-  size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, dq32, rdk32, rdv32, total;
+  size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, dq32, rdk32, total;
 };
 
 TcWorkspace workspace_layout(int B, int H, long long rows) {
@@ -390,14 +334,13 @@ TcWorkspace workspace_layout(int B, int H, long long rows) {
   w.stt = o;   o += up(st);
   w.dq32 = o;  o += up(tok * kTcDK * 4);
   w.rdk32 = o; o += up(tok * kTcDK * 4);
-  w.rdv32 = o; o += up(tok * kTcDV * 4);
   w.total = o;
   return w;
 }
 
 // Per-key-channel gate: the workspace of the dv run.
 struct TcVecWorkspace {
-  size_t rq, rk, rdo, rg, dfs, rdv, total;
+  size_t rq, rk, rdo, rg, dfs, total;
 };
 
 TcVecWorkspace vec_workspace_layout(int B, int H, long long rows) {
@@ -410,7 +353,6 @@ TcVecWorkspace vec_workspace_layout(int B, int H, long long rows) {
   w.rdo = o;  o += up(tok * kTcDV * 2);
   w.rg = o;   o += up(tok * kTcDK * 4);
   w.dfs = o;  o += up((size_t)B * H * kTcDK * kTcDV * 4);
-  w.rdv = o;  o += up(tok * kTcDV * 4);
   w.total = o;
   return w;
 }
@@ -441,18 +383,16 @@ cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
       a.cu_seqlens, a.B, a.H, a.T, a.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // dv (reversed): the per-key-channel prefill of (k, q, do) with dS_T / scale
+  // dv (reversed): the per-key-channel prefill of (k, q, do) with dS_T / scale,
+  // stored back in token order and in the gradients' dtype
   ChunkArgs c{};
   c.q = bf(w.rk); c.k = bf(w.rq); c.v = bf(w.rdo); c.g = fl(w.rg);
   c.scale = a.scale; c.init_state = a.d_final ? fl(w.dfs) : nullptr;
-  c.out = ws + w.rdv; c.final_state = nullptr; c.cu_seqlens = a.cu_seqlens;
+  c.out = a.dv; c.out_reversed = true;
+  c.final_state = nullptr; c.cu_seqlens = a.cu_seqlens;
   c.B = a.B; c.H = a.H; c.T = a.T; c.dk = kTcDK; c.dv = kTcDV; c.chunk = 128;
   c.fp32_io = false; c.fp32_out = a.fp32_out; c.vector_gate = true; c.status = a.status;
-  if ((e = launch_chunk_tc_vec(c, stream)) != cudaSuccess) return e;
-  bwd_tc_unreverse_kernel<<<grid, kCopyThreads, 0, stream>>>(
-      ws + w.rdv, static_cast<uint8_t*>(a.dv), kTcDV * (a.fp32_out ? 4 : 2), a.cu_seqlens, a.B,
-      a.H, a.T, a.status);
-  return cudaGetLastError();
+  return launch_chunk_tc_vec(c, stream);
 }
 
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream) {
@@ -489,24 +429,25 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   c.final_state = nullptr;
   c.dk = kTcDV; c.dv = kTcDK;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
-  // dv (reversed): the prefill of (k, q, do) with dS_T / scale; final state R_0
+  // dv (reversed): the prefill of (k, q, do) with dS_T / scale, stored back in
+  // token order and in the gradients' dtype; final state R_0
   c.q = bf(w.rk); c.k = bf(w.rq); c.v = bf(w.rdo); c.g = fl(w.rg);
   c.init_state = a.d_final ? fl(w.dfs) : nullptr;
-  c.out = fl(w.rdv32);
+  c.out = a.dv; c.fp32_out = a.fp32_out; c.out_reversed = true;
   c.final_state = a.d_init;
   c.dk = kTcDK; c.dv = kTcDV;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
 
   bwd_tc_fin_kernel<<<grid, kCopyThreads, 0, stream>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, a.g, a.scale, fl(w.dq32),
-      fl(w.rdk32), fl(w.rdv32), (a.dg && a.d_final) ? fl(w.stt) : nullptr,
-      a.d_final ? fl(w.dfst) : nullptr, a.dq, a.dk,
-      a.dv, a.fp32_out, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T, a.status);
+      fl(w.rdk32), (a.dg && a.d_final) ? fl(w.stt) : nullptr,
+      a.d_final ? fl(w.dfst) : nullptr, a.dq, a.dk, a.fp32_out, a.dg, a.d_init, a.cu_seqlens,
+      a.B, a.H, a.T, a.status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.dg) {
     const long long pairs = (long long)a.B * a.H;
-    bwd_dg_scan_kernel<<<(unsigned)((pairs + kScanWarps - 1) / kScanWarps), kScanWarps * 32, 0,
-                         stream>>>(a.dg, a.cu_seqlens, a.B, a.H, a.T, a.status);
+    bwd_dg_scan_kernel<<<(unsigned)pairs, kScanThreads, 0, stream>>>(a.dg, a.cu_seqlens, a.B,
+                                                                      a.H, a.T, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

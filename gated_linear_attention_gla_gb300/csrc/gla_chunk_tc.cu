@@ -146,7 +146,8 @@ struct TcParams {
   float* final_state;
   const int32_t* cu_seqlens;
   int B, H, T, DK, DV, nslices;  // DK = 64, 96 run as 128 with zero channels DK..127
-  int out_v8;  // out is 32-byte aligned: 256-bit stores
+  int out_v8;        // out is 32-byte aligned: 256-bit stores
+  int out_reversed;  // token t of a sequence stored at row len - 1 - t
   unsigned* status;
 };
 
@@ -505,8 +506,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       const int n = min(kC, len - c * kC);
       const float s1 = scale * f;
-      const long long rowbase = start + (long long)c * kC;
-      const size_t off = ((size_t)(rowbase + r) * p.H + h) * p.DV + (size_t)sl * kDVS;
+      const long long tok = (long long)c * kC + r;  // stored only while r < n
+      const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+      const size_t off = ((size_t)orow * p.H + h) * p.DV + (size_t)sl * kDVS;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {
         uint32_t v[16];
@@ -799,6 +801,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
   p.B = a.B; p.H = a.H; p.T = a.T; p.DK = a.dk; p.DV = a.dv; p.nslices = a.dv / kDVS;
   p.status = a.status;
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+  p.out_reversed = a.out_reversed;
   const long long ctas = (long long)a.B * a.H * p.nslices;
   if (a.fp32_out) {
     auto kern = chunk_tc_kernel<true>;

@@ -107,7 +107,8 @@ struct VecParams {
   float* final_state;
   const int32_t* cu_seqlens;
   int B, H, T;
-  int out_v8;  // out is 32-byte aligned: 256-bit stores
+  int out_v8;        // out is 32-byte aligned: 256-bit stores
+  int out_reversed;  // token t of a sequence stored at row len - 1 - t
   unsigned* status;
 };
 
@@ -349,7 +350,9 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (!wait_w(kOFull0 + ob, ph(n >> 1))) return false;
       tc_fence_after();
       const int nrows = min(kC, len - c * kC);
-      const size_t off = ((size_t)(start + (long long)c * kC + r) * p.H + h) * kD;
+      const long long tok = (long long)c * kC + r;  // stored only while r < nrows
+      const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+      const size_t off = ((size_t)orow * p.H + h) * kD;
 #pragma unroll 1
       for (int part = 0; part < kD / 16; ++part) {
         uint32_t v[16];
@@ -539,7 +542,9 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int w = 0; w < 4; ++w) o += rb[w * kD + col];
             o *= p.scale;
-            const size_t off = ((size_t)(start + (long long)c * kC + t) * p.H + h) * kD + col;
+            const long long tok = (long long)c * kC + t;
+            const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+            const size_t off = ((size_t)orow * p.H + h) * kD + col;
             if constexpr (OUTF32)
               static_cast<float*>(p.out)[off] = o;
             else
@@ -745,6 +750,7 @@ cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream) {
   p.final_state = a.final_state; p.cu_seqlens = a.cu_seqlens;
   p.B = a.B; p.H = a.H; p.T = a.T; p.status = a.status;
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+  p.out_reversed = a.out_reversed;
   const long long ctas = (long long)a.B * a.H;
   if (a.fp32_out) {
     auto kern = chunk_tc_vec_kernel<true>;

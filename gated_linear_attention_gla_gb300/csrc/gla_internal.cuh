@@ -32,7 +32,9 @@ struct ChunkArgs {
   bool fp32_io;      // q, k, v (and out) fp32
   bool fp32_out;     // out fp32 with bf16 q, k, v
   bool vector_gate;
-  unsigned* status;  // device status word
+  bool out_reversed;  // token t of a sequence of len tokens stored at row len - 1 - t
+                      // (tensor-core kernels only; the backward's reversed runs)
+  unsigned* status;   // device status word
 };
 
 struct DecodeArgs {

@@ -316,7 +316,7 @@ def _run_fixed(x, gr, **kw):
 
 
 def test_fixed_workspace_equals_caller_workspace():
-    """At the prefill workload's size (353 MB of workspace, inside the 384 MiB
+    """At the prefill workload's size (286 MB of workspace, inside the 384 MiB
     buffer) the results equal those of the same path on a caller workspace."""
     x, gr = inputs()
     mine = _run_fixed(x, gr, fixed_workspace=True)
@@ -326,7 +326,7 @@ def test_fixed_workspace_equals_caller_workspace():
 
 
 def test_fixed_workspace_falls_back_when_too_large():
-    """B = 8 needs 705 MB of workspace: the call runs on the CUDA cores."""
+    """B = 8 needs 571 MB of workspace: the call runs on the CUDA cores."""
     x, gr = inputs(B=8, H=16, T=2048)
     mine = _run_fixed(x, gr, fixed_workspace=True)
     ref = _run_fixed(x, gr, tensor_cores=False)
