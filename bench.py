@@ -500,7 +500,7 @@ def time_backward(gla, dev, reps=5, warmup=3):
                 "tensor": {"achieved_tflops": flops / sec / 1e12, "peak_tflops": bf16_peak,
                            "frac": flops / sec / 1e12 / bf16_peak, "algorithmic_flops": flops},
                 "workspace_bytes": ws.numel()}
-            entry["launches"] = 6  # prepare, 3 x prefill, finish, dg scan
+            entry["launches"] = 5  # prepare, 3 x prefill, tail (after a driver memset of dg)
         elif tc:
             # mostly the CUDA-core dq and dk kernels: their fp32 roofline
             flops = backward_flops(w, w.B, w.T)

@@ -913,23 +913,17 @@ bwd_dv_kernel(const IO* __restrict__ q, const IO* __restrict__ k, const float* _
 constexpr int kScanThreads = 256;
 constexpr int kScanPer = 8;  // tokens per thread per pass
 
-// One CTA per (sequence, head).  A pass covers the last kScanThreads *
-// kScanPer tokens not yet summed: thread i holds kScanPer consecutive tokens
-// (later tokens in higher threads), sums them from the back, and adds the
-// totals of every later thread (warp shuffles, then the warps' totals through
-// shared memory) and of every later pass (the carry).
-__global__ void __launch_bounds__(kScanThreads)
-bwd_dg_scan_kernel(float* __restrict__ dg, const int32_t* __restrict__ cu, int B, int H, int T,
-                   unsigned* status) {
+// Suffix sums of dg over the len tokens of one (sequence, head), in place, by
+// one CTA of kScanThreads threads (warp_total: kScanThreads / 32 floats of
+// shared memory).  A pass covers the last kScanThreads * kScanPer tokens not
+// yet summed: thread i holds kScanPer consecutive tokens (later tokens in
+// higher threads), sums them from the back, and adds the totals of every later
+// thread (warp shuffles, then the warps' totals through shared memory) and of
+// every later pass (the carry).
+__device__ __forceinline__ void dg_suffix_scan_cta(float* __restrict__ dg, long long start,
+                                                   int len, int H, int h, float* warp_total) {
   constexpr int kWarps = kScanThreads / 32;
-  __shared__ float warp_total[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long unit = blockIdx.x;
-  if (unit >= (long long)B * H) return;  // whole CTA
-  const int s = (int)(unit / H), h = (int)(unit % H);
-  long long start;
-  int len;
-  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;  // whole CTA
   constexpr int kSpan = kScanThreads * kScanPer;
   float carry = 0.f;
   for (int end = len; end > 0; end -= kSpan) {
@@ -970,6 +964,20 @@ bwd_dg_scan_kernel(float* __restrict__ dg, const int32_t* __restrict__ cu, int B
     carry += pass_total;
     __syncthreads();  // warp_total is rewritten by the next pass
   }
+}
+
+// One CTA per (sequence, head).
+__global__ void __launch_bounds__(kScanThreads)
+bwd_dg_scan_kernel(float* __restrict__ dg, const int32_t* __restrict__ cu, int B, int H, int T,
+                   unsigned* status) {
+  __shared__ float warp_total[kScanThreads / 32];
+  const long long unit = blockIdx.x;
+  if (unit >= (long long)B * H) return;  // whole CTA
+  const int s = (int)(unit / H), h = (int)(unit % H);
+  long long start;
+  int len;
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;  // whole CTA
+  dg_suffix_scan_cta(dg, start, len, H, h, warp_total);
 }
 
 // ---------------------------------------------------------------------------

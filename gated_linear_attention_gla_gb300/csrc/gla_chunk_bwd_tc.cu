@@ -19,13 +19,14 @@
 //   dg:  dg_t = sum_{u >= t} sum_i (q_u[i] dq_u[i] - k_u[i] dk_u[i])
 //               + sum_ij S_T[i][j] dS_T[i][j].
 // The prefill kernel reads tokens in order, so a prepare pass writes the
-// reversed (and gate-shifted) copies into the caller's workspace.  The dv run
-// stores its rows back in token order (row len - 1 - tau for reversed position
-// tau), directly in the gradients' dtype; the dq and dk runs store fp32 results
-// in the workspace, and a finish pass puts dk back in token order, rounds both
-// to the output dtype and forms the dg terms from the fp32 values; the suffix
-// sums reuse the CUDA-core backward's scan kernel.  Launches: prepare,
-// 3 x prefill, finish, and the scan when dg is wanted.
+// reversed (and gate-shifted) copies into the caller's workspace.  Each run
+// stores its gradient straight into the caller's buffer in the gradients'
+// dtype (the dk and dv runs back in token order: row len - 1 - tau for
+// reversed position tau), and the dq and dk runs add dg's per-token terms
+// q . dq and -k . dk, formed from their fp32 outputs, to dg (zeroed first).  A
+// tail pass adds the final-state term, takes the suffix sums and scales
+// d_init.  Launches: prepare, 3 x prefill, and the tail when dg or d_init is
+// wanted (plus a memset of dg).
 #include "gla_chunk_bwd.cuh"
 
 namespace gla {
@@ -128,114 +129,76 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   }
 }
 
-// Four fp32 values as elements 4 lane .. 4 lane + 3 of the row at `base`, in
-// fp32 or rounded to bf16.
-__device__ __forceinline__ void store_row4(void* out, long long base, int lane, float4 x,
-                                           bool f32) {
-  if (f32) {
-    reinterpret_cast<float4*>(static_cast<float*>(out) + base)[lane] = x;
-  } else {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
-    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + base)[lane] =
-        make_uint2(*reinterpret_cast<const unsigned*>(&lo), *reinterpret_cast<const unsigned*>(&hi));
-  }
-}
-
 __device__ __forceinline__ float warp_sum32(float x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
   return x;
 }
 
-// dq and dk in token order and output dtype, the per-token dg terms (q.dq -
-// k.dk, plus the final-state term at the last token), and d_init's factor
-// scale * e^{g_0}.  One warp per token; lane l owns channels 4 l .. 4 l + 3.
-__global__ void __launch_bounds__(kCopyThreads, 2)
-bwd_tc_fin_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const float* __restrict__ g, float scale, const float* __restrict__ dq32,
-                  const float* __restrict__ rdk32, const float* __restrict__ stt,
-                  const float* __restrict__ dfst, void* __restrict__ dq, void* __restrict__ dk,
-                  bool out_f32, float* __restrict__ dg, float* __restrict__ d_init,
-                  const int32_t* __restrict__ cu, int B, int H, int T, unsigned* status) {
-  static_assert(kTcDK == 128 && kTcDV == 128, "four channels a lane");
-  __shared__ float red[kCopyThreads / 32];
-  int s, h, blk;
-  pair_and_block(H, &s, &h, &blk);
+// The per-(sequence, head) tail of the backward, one CTA each: the final-state
+// term of dg, sum_ij S_T[i][j] dS_T[i][j] = scale sum_e S_T^T[e] (dS_T /
+// scale)^T[e] (both transposed copies in the workspace, read in order), added
+// at the last token; the suffix sums of dg (whose per-token terms q.dq - k.dk
+// the dq and dk runs have added); and d_init = scale e^{g_0} R_0 from the dv
+// run's final state, in place.
+__global__ void __launch_bounds__(kScanThreads)
+bwd_tc_tail_kernel(const float* __restrict__ g, float scale, const float* __restrict__ stt,
+                   const float* __restrict__ dfst, float* __restrict__ dg,
+                   float* __restrict__ d_init, const int32_t* __restrict__ cu, int B, int H,
+                   int T, unsigned* status) {
+  __shared__ float red[kScanThreads / 32];
+  __shared__ float warp_total[kScanThreads / 32];
+  const long long unit = blockIdx.x;
+  if (unit >= (long long)B * H) return;  // whole CTA
+  const int s = (int)(unit / H), h = (int)(unit % H);
   long long start;
   int len;
-  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
-  int t0, t1;
-  block_range(len, blk, &t0, &t1);
+  if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;  // whole CTA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t st_off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
-
-  // the final-state term sum_ij S_T[i][j] dS_T[i][j] = scale sum_e S_T^T[e]
-  // (dS_T / scale)^T[e] -- both transposed copies in the workspace, read in
-  // order -- by the block holding the last token
-  float c_t = 0.f;
-  if (dg && dfst && stt && len > 0 && t0 <= len - 1 && len - 1 < t1) {
+  constexpr int kPer = kTcDK * kTcDV / 4 / kScanThreads;  // float4 a thread
+  constexpr int kBatch = 8;                                // loads in flight
+  static_assert(kPer % kBatch == 0, "whole batches");
+  if (dg && stt && dfst && len > 0) {
     float acc = 0.f;
-    for (int e = threadIdx.x; e < kTcDK * kTcDV / 4; e += kCopyThreads) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(stt + st_off) + e);
-      const float4 y = __ldg(reinterpret_cast<const float4*>(dfst + st_off) + e);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+#pragma unroll 1
+    for (int b = 0; b < kPer; b += kBatch) {
+      float4 x[kBatch], y[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = (b + u) * kScanThreads + threadIdx.x;
+        x[u] = __ldg(reinterpret_cast<const float4*>(stt + st_off) + e);
+        y[u] = __ldg(reinterpret_cast<const float4*>(dfst + st_off) + e);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        acc = fmaf(x[u].x, y[u].x, fmaf(x[u].y, y[u].y, fmaf(x[u].z, y[u].z,
+                                                               fmaf(x[u].w, y[u].w, acc))));
     }
     acc = warp_sum32(acc);
     if (lane == 0) red[warp] = acc;
     __syncthreads();
-    for (int w = 0; w < kCopyThreads / 32; ++w) c_t += red[w];
-    c_t *= scale;
-  }
-
-  // eight tokens per warp and pass, their loads issued together
-  constexpr int kTok = 8;
-  constexpr int kWarps = kCopyThreads / 32;
-  for (int tb = t0 + kTok * warp; tb < t1; tb += kTok * kWarps) {
-    float4 av[kTok], bv[kTok];
-    uint2 qv[kTok], kv[kTok];
-#pragma unroll
-    for (int u = 0; u < kTok; ++u) {
-      const int t = min(tb + u, t1 - 1);
-      const long long row = (start + t) * H + h;
-      const long long rrow = (start + (len - 1 - t)) * H + h;
-      av[u] = __ldg(reinterpret_cast<const float4*>(dq32 + row * kTcDK) + lane);
-      bv[u] = __ldg(reinterpret_cast<const float4*>(rdk32 + rrow * kTcDK) + lane);
-      if (dg) {
-        qv[u] = __ldg(reinterpret_cast<const uint2*>(q + row * kTcDK) + lane);
-        kv[u] = __ldg(reinterpret_cast<const uint2*>(k + row * kTcDK) + lane);
-      }
+    if (threadIdx.x == 0) {
+      float c_t = 0.f;
+      for (int w = 0; w < kScanThreads / 32; ++w) c_t += red[w];
+      dg[(start + len - 1) * H + h] += scale * c_t;
     }
-#pragma unroll
-    for (int u = 0; u < kTok; ++u) {
-      const int t = tb + u;
-      if (t >= t1) break;  // warp-uniform
-      const long long row = (start + t) * H + h;
-      const float4 a = av[u], b = bv[u];
-      store_row4(dq, row * kTcDK, lane, a, out_f32);
-      store_row4(dk, row * kTcDK, lane, b, out_f32);
-      if (dg) {
-        const uint2 qr = qv[u], kr = kv[u];
-        float x = __uint_as_float(qr.x << 16) * a.x + __uint_as_float(qr.x & 0xffff0000u) * a.y +
-                  __uint_as_float(qr.y << 16) * a.z + __uint_as_float(qr.y & 0xffff0000u) * a.w;
-        x -= __uint_as_float(kr.x << 16) * b.x + __uint_as_float(kr.x & 0xffff0000u) * b.y +
-             __uint_as_float(kr.y << 16) * b.z + __uint_as_float(kr.y & 0xffff0000u) * b.w;
-        x = warp_sum32(x);
-        if (lane == 0) dg[row] = t == len - 1 ? x + c_t : x;
-      }
-    }
+    __syncthreads();  // the scan reads that token
   }
-
-  // d_init = scale e^{g_0} R_0 (the dv run's final state), in place; each
-  // block of the pair scales an equal share
+  if (dg) dg_suffix_scan_cta(dg, start, len, H, h, warp_total);
   if (d_init) {
     const float f = len > 0 ? scale * expf(fmaxf(__ldg(g + start * H + h), -kGateClamp)) : scale;
-    constexpr int kPer = kTcDK * kTcDV / 4 / kBlocksPerPair;
-    float4* p = reinterpret_cast<float4*>(d_init + st_off) + blk * kPer;
-    for (int e = threadIdx.x; e < kPer; e += kCopyThreads) {
-      float4 x = p[e];
-      x.x *= f; x.y *= f; x.z *= f; x.w *= f;
-      p[e] = x;
+    float4* p = reinterpret_cast<float4*>(d_init + st_off);
+#pragma unroll 1
+    for (int b = 0; b < kPer; b += kBatch) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) x[u] = p[(b + u) * kScanThreads + threadIdx.x];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        x[u].x *= f; x[u].y *= f; x[u].z *= f; x[u].w *= f;
+        p[(b + u) * kScanThreads + threadIdx.x] = x[u];
+      }
     }
   }
 }
@@ -314,7 +277,7 @@ bwd_tc_prep_vec_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 
 // Workspace sections, each starting on a 256-byte boundary.
 struct TcWorkspace {
-  size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, dq32, rdk32, total;
+  size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, total;
 };
 
 TcWorkspace workspace_layout(int B, int H, long long rows) {
@@ -332,8 +295,6 @@ TcWorkspace workspace_layout(int B, int H, long long rows) {
   w.dfs = o;   o += up(st);
   w.dfst = o;  o += up(st);
   w.stt = o;   o += up(st);
-  w.dq32 = o;  o += up(tok * kTcDK * 4);
-  w.rdk32 = o; o += up(tok * kTcDK * 4);
   w.total = o;
   return w;
 }
@@ -411,43 +372,50 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
+  // dg's per-token terms arrive from four CTAs each (two value slices of the dq
+  // and of the dk run) as fp32 atomics
+  if (a.dg) {
+    if ((e = cudaMemsetAsync(a.dg, 0, sizeof(float) * (size_t)(rows * a.H), stream)) !=
+        cudaSuccess)
+      return e;
+  }
   ChunkArgs c{};
   c.scale = a.scale; c.cu_seqlens = a.cu_seqlens; c.B = a.B; c.H = a.H; c.T = a.T;
-  c.chunk = 128; c.fp32_io = false; c.fp32_out = true; c.vector_gate = false;
+  c.chunk = 128; c.fp32_io = false; c.fp32_out = a.fp32_out; c.vector_gate = false;
   c.status = a.status;
-  // dq: the prefill of (do, v, k) with S_0^T; its final state S_T^T feeds dg
+  // dq: the prefill of (do, v, k) with S_0^T, stored in dq's dtype, adding
+  // q . dq to dg; its final state S_T^T feeds dg's final-state term
   c.q = a.d_out; c.k = a.v; c.v = a.k; c.g = a.g;
   c.init_state = a.init_state ? fl(w.s0t) : nullptr;
-  c.out = fl(w.dq32);
+  c.out = a.dq;
   c.final_state = (a.dg && a.d_final) ? fl(w.stt) : nullptr;
+  c.dot_rows = a.dg ? a.q : nullptr; c.dot_out = a.dg; c.dot_sign = 1.f;
   c.dk = kTcDV; c.dv = kTcDK;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
-  // dk (reversed): the prefill of (v, do, q) with (dS_T / scale)^T
+  // dk (reversed): the prefill of (v, do, q) with (dS_T / scale)^T, stored back
+  // in token order, adding -k . dk to dg
   c.q = bf(w.rv); c.k = bf(w.rdo); c.v = bf(w.rq); c.g = fl(w.rg);
   c.init_state = a.d_final ? fl(w.dfst) : nullptr;
-  c.out = fl(w.rdk32);
+  c.out = a.dk; c.out_reversed = true;
   c.final_state = nullptr;
+  c.dot_rows = a.dg ? a.k : nullptr; c.dot_out = a.dg; c.dot_sign = -1.f;
   c.dk = kTcDV; c.dv = kTcDK;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
   // dv (reversed): the prefill of (k, q, do) with dS_T / scale, stored back in
-  // token order and in the gradients' dtype; final state R_0
+  // token order; final state R_0
   c.q = bf(w.rk); c.k = bf(w.rq); c.v = bf(w.rdo); c.g = fl(w.rg);
   c.init_state = a.d_final ? fl(w.dfs) : nullptr;
-  c.out = a.dv; c.fp32_out = a.fp32_out; c.out_reversed = true;
+  c.out = a.dv; c.out_reversed = true;
   c.final_state = a.d_init;
+  c.dot_rows = nullptr; c.dot_out = nullptr;
   c.dk = kTcDK; c.dv = kTcDV;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
 
-  bwd_tc_fin_kernel<<<grid, kCopyThreads, 0, stream>>>(
-      (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, a.g, a.scale, fl(w.dq32),
-      fl(w.rdk32), (a.dg && a.d_final) ? fl(w.stt) : nullptr,
-      a.d_final ? fl(w.dfst) : nullptr, a.dq, a.dk, a.fp32_out, a.dg, a.d_init, a.cu_seqlens,
-      a.B, a.H, a.T, a.status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.dg) {
-    const long long pairs = (long long)a.B * a.H;
-    bwd_dg_scan_kernel<<<(unsigned)pairs, kScanThreads, 0, stream>>>(a.dg, a.cu_seqlens, a.B,
-                                                                      a.H, a.T, a.status);
+  if (a.dg || a.d_init) {
+    bwd_tc_tail_kernel<<<(unsigned)((long long)a.B * a.H), kScanThreads, 0, stream>>>(
+        a.g, a.scale, (a.dg && a.d_final) ? fl(w.stt) : nullptr,
+        a.d_final ? fl(w.dfst) : nullptr, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T,
+        a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

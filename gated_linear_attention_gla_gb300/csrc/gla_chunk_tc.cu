@@ -148,6 +148,11 @@ struct TcParams {
   int B, H, T, DK, DV, nslices;  // DK = 64, 96 run as 128 with zero channels DK..127
   int out_v8;        // out is 32-byte aligned: 256-bit stores
   int out_reversed;  // token t of a sequence stored at row len - 1 - t
+  // DOT kernels: dot_out[row, h] += dot_sign * (out row . dot_rows row), the
+  // fp32 output against a bf16 tensor of the output's layout
+  const __nv_bfloat16* dot_rows;
+  float* dot_out;
+  float dot_sign;
   unsigned* status;
 };
 
@@ -223,7 +228,7 @@ __device__ __noinline__ void build_p_wide(uint32_t a_row, int q4, int r, float G
   build_p_body<true>(a_row, q4, r, G2, G2s);
 }
 
-template <bool OUTF32>
+template <bool OUTF32, bool DOT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const TcParams p) {
@@ -501,14 +506,88 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     // output of chunk c: o = scale f_t O[c & 1], f_t = exp(G_t - G_L) (1 on wide
     // chunks, whose O carries the decay already)
+    // one 16-column part of an output row: to the output's dtype and stored
+    auto store_part = [&](size_t off, int part, const float* o) {
+      if constexpr (OUTF32) {
+        float* dst = static_cast<float*>(p.out) + off + 16 * part;
+        if (p.out_v8) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            st_global_v8(dst + 8 * j, __float_as_uint(o[8 * j]), __float_as_uint(o[8 * j + 1]),
+                         __float_as_uint(o[8 * j + 2]), __float_as_uint(o[8 * j + 3]),
+                         __float_as_uint(o[8 * j + 4]), __float_as_uint(o[8 * j + 5]),
+                         __float_as_uint(o[8 * j + 6]), __float_as_uint(o[8 * j + 7]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<float4*>(dst)[j] =
+                make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+      } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + off + 16 * part;
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
+        if (p.out_v8) {
+          st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    };
+
+    // this thread's output row of chunk c (valid while r < n)
+    auto out_row = [&](int c) -> long long {
+      const long long tok = (long long)c * kC + r;
+      return start + (p.out_reversed ? len - 1 - tok : tok);
+    };
+
+    // output of chunk c: o = scale f_t O[c & 1], f_t = exp(G_t - G_L) (1 on wide
+    // chunks, whose O carries the decay already)
     auto output = [&](int c, float f) -> bool {
+      const int n = min(kC, len - c * kC);
+      const long long orow = out_row(c);
+      const size_t off = ((size_t)orow * p.H + h) * p.DV + (size_t)sl * kDVS;
+      const float s1 = scale * f;
+      if constexpr (DOT) {
+        // the row's 64 partner values, loaded before MMA2 is waited for
+        uint4 pr[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          pr[j] = r < n ? __ldg(reinterpret_cast<const uint4*>(p.dot_rows + off) + j)
+                        : make_uint4(0u, 0u, 0u, 0u);
+        if (!wait_w(kOFull0 + (c & 1), ph(c >> 1))) return false;  // MMA2(c)
+        tc_fence_after();
+        float dot = 0.f;
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + lane_off + kColO + (c & 1) * kDVS + 16 * part, v);
+          tmem_ld_wait();
+          if (part == 3) {
+            tc_fence_before();
+            warp_arrive(kOFree0 + (c & 1));
+          }
+          float o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) o[j] = s1 * __uint_as_float(v[j]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint4 b = pr[2 * part + j];
+            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dot = fmaf(o[8 * j + 2 * e], bf16lo(bw[e]),
+                         fmaf(o[8 * j + 2 * e + 1], bf16hi(bw[e]), dot));
+          }
+          if (r < n) store_part(off, part, o);
+        }
+        if (r < n) atomicAdd(p.dot_out + (size_t)orow * p.H + h, p.dot_sign * dot);
+        return true;
+      }
       if (!wait_w(kOFull0 + (c & 1), ph(c >> 1))) return false;  // MMA2(c)
       tc_fence_after();
-      const int n = min(kC, len - c * kC);
-      const float s1 = scale * f;
-      const long long tok = (long long)c * kC + r;  // stored only while r < n
-      const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
-      const size_t off = ((size_t)orow * p.H + h) * p.DV + (size_t)sl * kDVS;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {
         uint32_t v[16];
@@ -521,35 +600,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         float o[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) o[j] = s1 * __uint_as_float(v[j]);
-        if (r < n) {
-          if constexpr (OUTF32) {
-            float* dst = static_cast<float*>(p.out) + off + 16 * part;
-            if (p.out_v8) {
-#pragma unroll
-              for (int j = 0; j < 2; ++j)
-                st_global_v8(dst + 8 * j, __float_as_uint(o[8 * j]), __float_as_uint(o[8 * j + 1]),
-                             __float_as_uint(o[8 * j + 2]), __float_as_uint(o[8 * j + 3]),
-                             __float_as_uint(o[8 * j + 4]), __float_as_uint(o[8 * j + 5]),
-                             __float_as_uint(o[8 * j + 6]), __float_as_uint(o[8 * j + 7]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                reinterpret_cast<float4*>(dst)[j] =
-                    make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            }
-          } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + off + 16 * part;
-            uint32_t w[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
-            if (p.out_v8) {
-              st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-            } else {
-              reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          }
-        }
+        if (r < n) store_part(off, part, o);
       }
       return true;
     };
@@ -560,6 +611,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int c = 0; c <= nch; ++c) {
       float f = 1.f;
       if (c < nch) {
+        if constexpr (DOT) {
+          // chunk c's partner rows into L2, an iteration before output(c) reads them
+          if (r < len - c * kC) {
+            const __nv_bfloat16* row =
+                p.dot_rows + ((size_t)out_row(c) * p.H + h) * p.DV + (size_t)sl * kDVS;
+            prefetch_l2(row);
+            prefetch_l2(row + kDVS - 8);
+          }
+        }
         const int st = c & 1;
         const float* slot = slot_of(c);
         if (!wait_w(kGReady0 + c % kSlots, ph(c / kSlots))) break;
@@ -802,21 +862,20 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   p.out_reversed = a.out_reversed;
+  p.dot_rows = static_cast<const __nv_bfloat16*>(a.dot_rows);
+  p.dot_out = a.dot_out;
+  p.dot_sign = a.dot_sign;
   const long long ctas = (long long)a.B * a.H * p.nslices;
-  if (a.fp32_out) {
-    auto kern = chunk_tc_kernel<true>;
+  auto run = [&](auto kern) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  } else {
-    auto kern = chunk_tc_kernel<false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  }
-  return cudaGetLastError();
+    return cudaGetLastError();
+  };
+  if (a.dot_out)
+    return a.fp32_out ? run(chunk_tc_kernel<true, true>) : run(chunk_tc_kernel<false, true>);
+  return a.fp32_out ? run(chunk_tc_kernel<true, false>) : run(chunk_tc_kernel<false, false>);
 }
 
 }  // namespace gla

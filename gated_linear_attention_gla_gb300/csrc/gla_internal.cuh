@@ -34,6 +34,12 @@ struct ChunkArgs {
   bool vector_gate;
   bool out_reversed;  // token t of a sequence of len tokens stored at row len - 1 - t
                       // (tensor-core kernels only; the backward's reversed runs)
+  // per-head tensor-core kernel only (the backward's dg terms): when dot_out is
+  // set, dot_out[row, h] += dot_sign * sum_j out[row, h, j] * dot_rows[row, h, j]
+  // (fp32 output values; dot_rows bf16 with the output's layout)
+  const void* dot_rows;
+  float* dot_out;
+  float dot_sign;
   unsigned* status;   // device status word
 };
 

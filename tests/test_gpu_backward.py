@@ -315,25 +315,30 @@ def _run_fixed(x, gr, **kw):
     return res
 
 
+def _dg_close(a, b):
+    # the per-head gate's dg terms meet through fp32 atomics: equal up to their order
+    torch.testing.assert_close(a, b, rtol=1e-5, atol=1e-5 * float(b.abs().max()))
+
+
 def test_fixed_workspace_equals_caller_workspace():
-    """At the prefill workload's size (286 MB of workspace, inside the 384 MiB
+    """At the prefill workload's size (152 MB of workspace, inside the 384 MiB
     buffer) the results equal those of the same path on a caller workspace."""
     x, gr = inputs()
     mine = _run_fixed(x, gr, fixed_workspace=True)
     ref = _run_fixed(x, gr)
-    for a, b in zip(mine, ref):
-        assert torch.equal(a, b)
+    for i in (0, 1, 2, 4):
+        assert torch.equal(mine[i], ref[i])
+    _dg_close(mine[3], ref[3])
 
 
 def test_fixed_workspace_falls_back_when_too_large():
-    """B = 8 needs 571 MB of workspace: the call runs on the CUDA cores."""
-    x, gr = inputs(B=8, H=16, T=2048)
+    """B = 16 needs 606 MB of workspace: the call runs on the CUDA cores."""
+    x, gr = inputs(B=16, H=16, T=2048)
     mine = _run_fixed(x, gr, fixed_workspace=True)
     ref = _run_fixed(x, gr, tensor_cores=False)
     for i in (0, 1, 2, 4):
         assert torch.equal(mine[i], ref[i])
-    # the per-head gate's dg terms meet through atomics: equal up to their order
-    torch.testing.assert_close(mine[3], ref[3], rtol=1e-5, atol=1e-5 * float(ref[3].abs().max()))
+    _dg_close(mine[3], ref[3])
 
 
 @pytest.mark.parametrize("T", [1, 127, 128, 129, 256])
