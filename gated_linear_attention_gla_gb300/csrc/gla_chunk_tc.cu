@@ -504,8 +504,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const float scale = p.scale;
 
-    // output of chunk c: o = scale f_t O[c & 1], f_t = exp(G_t - G_L) (1 on wide
-    // chunks, whose O carries the decay already)
     // one 16-column part of an output row: to the output's dtype and stored
     auto store_part = [&](size_t off, int part, const float* o) {
       if constexpr (OUTF32) {
