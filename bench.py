@@ -599,51 +599,94 @@ def run_gla(args, world, rank, local):
 
     # ---------------------------------------------------------------- e2e
     # Host buffers in, host buffers out: each step copies its inputs from
-    # pinned host memory, runs, and copies the outputs back.
+    # pinned host memory, runs, and copies its outputs back.  Two buffer slots
+    # pipeline the steps as a server would: step i's input copies (one stream)
+    # overlap step i-1's compute and result copies (another stream), and a slot
+    # is refilled only once the step that last used it has been read and
+    # copied out.
     host = {n: x[n].pin_memory() if x[n] is not None else None
             for n in ("q", "k", "v", "g", "init_state")}
     h_out = torch.empty(B, T, H, wp.dv, dtype=torch.bfloat16).pin_memory()
     h_fin = torch.empty(B, H, wp.dk, wp.dv, dtype=torch.float32).pin_memory()
-    dsets = sets[N_SETS - 1]
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = h_out.numel() * 2 + h_fin.numel() * 4
     e2e_steps = max(3, min(args.steps, 20))
+    copy_in = torch.cuda.Stream(device=dev)
+    copy_out = torch.cuda.Stream(device=dev)
 
-    def e2e_prefill():
+    def pipelined(n_steps, h2d_fn, compute_fn, d2h_fn):
+        copy_in.wait_stream(stream)
+        copy_out.wait_stream(stream)
+        read_done, out_free = [None, None], [None, None]
+        for i in range(n_steps):
+            j = i % 2
+            if read_done[j] is not None:
+                copy_in.wait_event(read_done[j])
+            with torch.cuda.stream(copy_in):
+                h2d_fn(j)
+            e_in = torch.cuda.Event()
+            e_in.record(copy_in)
+            stream.wait_event(e_in)
+            if out_free[j] is not None:
+                stream.wait_event(out_free[j])
+            compute_fn(j)
+            e_c = torch.cuda.Event()
+            e_c.record(stream)
+            read_done[j] = e_c
+            copy_out.wait_event(e_c)
+            with torch.cuda.stream(copy_out):
+                d2h_fn(j)
+            e_o = torch.cuda.Event()
+            e_o.record(copy_out)
+            out_free[j] = e_o
+        stream.wait_stream(copy_in)
+        stream.wait_stream(copy_out)
+
+    pslot = (N_SETS - 1, N_SETS - 2)  # the device input sets and outputs of the two slots
+
+    def pre_h2d(j):
         for n, t in host.items():
             if t is not None:
-                dsets[n].copy_(t, non_blocking=True)
-        prefill(N_SETS - 1)
-        h_out.copy_(outs[N_SETS - 1], non_blocking=True)
-        h_fin.copy_(finals[N_SETS - 1], non_blocking=True)
+                sets[pslot[j]][n].copy_(t, non_blocking=True)
+
+    def pre_d2h(j):
+        h_out.copy_(outs[pslot[j]], non_blocking=True)
+        h_fin.copy_(finals[pslot[j]], non_blocking=True)
+
+    def e2e_prefill(n):
+        pipelined(n, pre_h2d, lambda j: prefill(pslot[j]), pre_d2h)
 
     hd = {n: d[n][0].pin_memory() for n in ("q", "k", "v", "g")}
     hd_out = torch.empty(wd.N, wd.H, wd.dv, dtype=torch.bfloat16).pin_memory()
     d_h2d = sum(t.numel() * t.element_size() for t in hd.values())
     d_d2h = hd_out.numel() * 2
 
-    def e2e_decode():
-        for n, dst in (("q", d_q[0]), ("k", d_k[0]), ("v", d_v[0]), ("g", d_g[0])):
-            dst.copy_(hd[n], non_blocking=True)
-        gla.decode_step(d_q[0], d_k[0], d_v[0], d_g[0], d_state, scale=wd.dk ** -0.5,
-                        out=d_out[0])
-        hd_out.copy_(d_out[0], non_blocking=True)
+    def dec_h2d(j):
+        for n, dst in (("q", d_q), ("k", d_k), ("v", d_v), ("g", d_g)):
+            dst[j].copy_(hd[n], non_blocking=True)
 
-    for _ in range(2):
-        e2e_prefill()
-        e2e_decode()
+    def dec_compute(j):
+        gla.decode_step(d_q[j], d_k[j], d_v[j], d_g[j], d_state, scale=wd.dk ** -0.5,
+                        out=d_out[j])
+
+    def dec_d2h(j):
+        hd_out.copy_(d_out[j], non_blocking=True)
+
+    def e2e_decode(n):
+        pipelined(n, dec_h2d, dec_compute, dec_d2h)
+
+    e2e_prefill(2)
+    e2e_decode(2)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_prefill()
+    e2e_prefill(e2e_steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_pre_s = max_over_ranks(a.elapsed_time(b) / 1e3, world)
     a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_decode()
+    e2e_decode(e2e_steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_dec_s = max_over_ranks(a.elapsed_time(b) / 1e3, world)
