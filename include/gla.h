@@ -280,8 +280,11 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
  *                 its operands exchanged -- dq is the prefill of (d_out, v, k),
  *                 dk and dv are prefills of (v, d_out, q) and (k, q, d_out) run
  *                 backwards in time.  Per-head gate: the tcgen05 prefill kernel
- *                 runs three times between a reversing pass and a finishing
- *                 pass.  Per-key-channel gate: dv is one reversed run of the
+ *                 runs three times between a reversing pass and a tail pass
+ *                 (dg's final-state term and suffix sums, d_init's factor);
+ *                 each run stores its gradient straight into dq, dk_out or
+ *                 dv_out, and the dq and dk runs add dg's per-token terms
+ *                 with fp32 atomics.  Per-key-channel gate: dv is one reversed run of the
  *                 per-key-channel tcgen05 prefill (whose decay falls on the
  *                 state's rows, as dv's does); dq and dk, whose decays fall on
  *                 the value side, stay on the CUDA cores.  Tensor-core results
