@@ -157,8 +157,9 @@ def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
     ``grad_dtype=torch.float32`` for bf16 inputs; ``dg`` (fp32, g's shape) and
     ``d_init`` (fp32 state) are None when not requested.
 
-    ``tensor_cores``: use the tensor-core path where it covers the call (bf16,
-    per-head gate, dk = dv = 128), with ``workspace`` (a CUDA uint8 tensor of at
+    ``tensor_cores``: use the tensor-core path where it covers the call (bf16;
+    per-head gate with dk, dv each 64 or 128, every gradient; per-key-channel
+    gate with dk = dv = 128, dv only), with ``workspace`` (a CUDA uint8 tensor of at
     least ``gla_chunk_bwd_workspace_size`` bytes) or a fresh allocation; False
     runs the fp32 CUDA-core kernels.  ``fixed_workspace``: call
     gla_chunk_bwd_fixed_workspace instead, whose workspace is the library's own

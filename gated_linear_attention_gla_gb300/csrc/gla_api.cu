@@ -232,7 +232,7 @@ size_t gla_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv, int pac
   if (!gla::chunk_bwd_tc_supported(dk, dv, fp32, vec)) return 0;
   const long long rows = packed ? (long long)T : (long long)B * T;
   if (rows * H * dk > kMaxElems) return 0;
-  return gla::chunk_bwd_tc_workspace(B, H, rows, vec);
+  return gla::chunk_bwd_tc_workspace(B, H, rows, dk, dv, vec);
 }
 
 static_assert(GLA_BWD_FIXED_WORKSPACE_BYTES == gla::kBwdFixedWorkspaceBytes,
@@ -282,7 +282,7 @@ gla_status chunk_bwd_impl(const void* q, const void* k, const void* v, const flo
                          cu_seqlens ? (size_t)(B + 1) * 4 : 0};
   // the tensor-core path runs when it covers the call and the workspace is large enough
   const size_t ws_need = gla::chunk_bwd_tc_supported(dk, dv, fp32, vec)
-                             ? gla::chunk_bwd_tc_workspace(B, H, rows, vec)
+                             ? gla::chunk_bwd_tc_workspace(B, H, rows, dk, dv, vec)
                              : 0;
   const bool use_tc = rows > 0 && ws_need > 0 && workspace != nullptr && workspace_bytes >= ws_need;
   const void* out_p[] = {dq, dk_out, dv_out, dg, d_init_state, use_tc ? workspace : nullptr};

@@ -62,7 +62,7 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                    __nv_bfloat16* __restrict__ rv, __nv_bfloat16* __restrict__ rdo,
                    float* __restrict__ rg, float* __restrict__ s0t, float* __restrict__ dfs,
                    float* __restrict__ dfst, const int32_t* __restrict__ cu, int B, int H,
-                   int T, unsigned* status) {
+                   int T, int DK, int DV, unsigned* status) {
   int s, h, blk;
   pair_and_block(H, &s, &h, &blk);
   long long start;
@@ -70,12 +70,20 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;
   int t0, t1;
   block_range(len, blk, &t0, &t1);
-  // 16-byte vectors: a token's q and k rows (16 each at d = 128), then its v
-  // and do rows; eight vectors a thread in flight at a time
-  constexpr int VK = kTcDK / 8, VV = kTcDV / 8;
-  constexpr int VPT = 2 * VK + 2 * VV;
+  // 16-byte vectors: a token's q and k rows (DK / 8 each), then its v and do
+  // rows (DV / 8 each); eight vectors a thread in flight at a time
+  const int VK = DK / 8, VV = DV / 8;
+  const int VPT = 2 * VK + 2 * VV;
   constexpr int kBatch = 8;
-  static_assert(VK == VV, "one row width");
+  // vector c of a token: its tensor (0 q, 1 k, 2 v, 3 do), index in the row, row width
+  auto which = [&](int c, int* w, int* e, int* width) {
+    if (c < 2 * VK) {
+      *w = c / VK; *e = c % VK; *width = DK;
+    } else {
+      c -= 2 * VK;
+      *w = 2 + c / VV; *e = c % VV; *width = DV;
+    }
+  };
   auto src_of = [&](int w) { return w == 0 ? q : w == 1 ? k : w == 2 ? v : d_out; };
   auto dst_of = [&](int w) { return w == 0 ? rq : w == 1 ? rk : w == 2 ? rv : rdo; };
   const int nvec = (t1 - t0) * VPT;
@@ -85,18 +93,22 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int b = 0; b < kBatch; ++b) {
       const int idx = base + b * kCopyThreads;
       if (idx < nvec) {
-        const int t = t0 + idx / VPT, c = idx % VPT;
+        const int t = t0 + idx / VPT;
+        int w, e, width;
+        which(idx % VPT, &w, &e, &width);
         const long long src = (start + t) * H + h;
-        r[b] = __ldg(reinterpret_cast<const uint4*>(src_of(c / VK) + src * kTcDK) + c % VK);
+        r[b] = __ldg(reinterpret_cast<const uint4*>(src_of(w) + src * width) + e);
       }
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int idx = base + b * kCopyThreads;
       if (idx < nvec) {
-        const int t = t0 + idx / VPT, c = idx % VPT;
+        const int t = t0 + idx / VPT;
+        int w, e, width;
+        which(idx % VPT, &w, &e, &width);
         const long long dst = (start + (len - 1 - t)) * H + h;
-        reinterpret_cast<uint4*>(dst_of(c / VK) + dst * kTcDK)[c % VK] = r[b];
+        reinterpret_cast<uint4*>(dst_of(w) + dst * width)[e] = r[b];
       }
     }
   }
@@ -105,14 +117,14 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   // the states: 32 x 32 tiles spread over the blocks of the pair, transposed through
   // shared memory so that reads and writes are both row-contiguous
   __shared__ float tile[2][32][33];
-  const size_t off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
-  constexpr int kTiles = (kTcDK / 32) * (kTcDV / 32);
+  const size_t off = ((size_t)s * H + h) * (size_t)DK * DV;
+  const int kTiles = (DK / 32) * (DV / 32);
   for (int tt = blk; tt < kTiles; tt += kBlocksPerPair) {
-    const int ti = (tt / (kTcDV / 32)) * 32, tj = (tt % (kTcDV / 32)) * 32;
+    const int ti = (tt / (DV / 32)) * 32, tj = (tt % (DV / 32)) * 32;
     const int r = threadIdx.x / 32, c = threadIdx.x % 32;  // 8 rows of 32 per pass
     __syncthreads();
     for (int rr = r; rr < 32; rr += kCopyThreads / 32) {
-      const size_t e = off + (size_t)(ti + rr) * kTcDV + tj + c;
+      const size_t e = off + (size_t)(ti + rr) * DV + tj + c;
       tile[0][rr][c] = init_state ? __ldg(init_state + e) : 0.f;
       if (d_final) {
         const float x = __ldg(d_final + e) * inv_scale;
@@ -122,7 +134,7 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     }
     __syncthreads();
     for (int rr = r; rr < 32; rr += kCopyThreads / 32) {
-      const size_t e = off + (size_t)(tj + rr) * kTcDK + ti + c;  // row j, column i
+      const size_t e = off + (size_t)(tj + rr) * DK + ti + c;  // row j, column i
       if (init_state) s0t[e] = tile[0][c][rr];
       if (d_final) dfst[e] = tile[1][c][rr];
     }
@@ -145,7 +157,7 @@ __global__ void __launch_bounds__(kScanThreads)
 bwd_tc_tail_kernel(const float* __restrict__ g, float scale, const float* __restrict__ stt,
                    const float* __restrict__ dfst, float* __restrict__ dg,
                    float* __restrict__ d_init, const int32_t* __restrict__ cu, int B, int H,
-                   int T, unsigned* status) {
+                   int T, int DK, int DV, unsigned* status) {
   __shared__ float red[kScanThreads / 32];
   __shared__ float warp_total[kScanThreads / 32];
   const long long unit = blockIdx.x;
@@ -155,10 +167,9 @@ bwd_tc_tail_kernel(const float* __restrict__ g, float scale, const float* __rest
   int len;
   if (!seq_bounds(cu, s, B, T, &start, &len, status)) return;  // whole CTA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const size_t st_off = ((size_t)s * H + h) * (size_t)kTcDK * kTcDV;
-  constexpr int kPer = kTcDK * kTcDV / 4 / kScanThreads;  // float4 a thread
-  constexpr int kBatch = 8;                                // loads in flight
-  static_assert(kPer % kBatch == 0, "whole batches");
+  const size_t st_off = ((size_t)s * H + h) * (size_t)DK * DV;
+  const int kPer = DK * DV / 4 / kScanThreads;  // float4 a thread: 4, 8 or 16
+  constexpr int kBatch = 4;                     // loads in flight (a divisor of kPer)
   if (dg && stt && dfst && len > 0) {
     float acc = 0.f;
 #pragma unroll 1
@@ -280,16 +291,16 @@ struct TcWorkspace {
   size_t rq, rk, rv, rdo, rg, s0t, dfs, dfst, stt, total;
 };
 
-TcWorkspace workspace_layout(int B, int H, long long rows) {
+TcWorkspace workspace_layout(int B, int H, long long rows, int DK, int DV) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t tok = (size_t)rows * H;
-  const size_t st = (size_t)B * H * kTcDK * kTcDV * 4;
+  const size_t st = (size_t)B * H * DK * DV * 4;
   TcWorkspace w;
   size_t o = 0;
-  w.rq = o;    o += up(tok * kTcDK * 2);
-  w.rk = o;    o += up(tok * kTcDK * 2);
-  w.rv = o;    o += up(tok * kTcDV * 2);
-  w.rdo = o;   o += up(tok * kTcDV * 2);
+  w.rq = o;    o += up(tok * DK * 2);
+  w.rk = o;    o += up(tok * DK * 2);
+  w.rv = o;    o += up(tok * DV * 2);
+  w.rdo = o;   o += up(tok * DV * 2);
   w.rg = o;    o += up(tok * 4);
   w.s0t = o;   o += up(st);
   w.dfs = o;   o += up(st);
@@ -321,13 +332,17 @@ TcVecWorkspace vec_workspace_layout(int B, int H, long long rows) {
 }  // namespace
 
 bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate) {
-  (void)vector_gate;  // the per-key-channel gate takes the tensor-core path for dv
-  return !fp32_io && dk == kTcDK && dv == kTcDV;
+  if (fp32_io) return false;
+  // per-key-channel gate: dv's run on the d = 128 per-key-channel kernel;
+  // per-head gate: every run's head sizes (d_k, d_v exchanged) are ones the
+  // per-head kernel takes as key and value sizes
+  if (vector_gate) return dk == kTcDK && dv == kTcDV;
+  return (dk == 64 || dk == 128) && (dv == 64 || dv == 128);
 }
 
-size_t chunk_bwd_tc_workspace(int B, int H, long long rows, bool vector_gate) {
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows, int dk, int dv, bool vector_gate) {
   return vector_gate ? vec_workspace_layout(B, H, rows).total
-                     : workspace_layout(B, H, rows).total;
+                     : workspace_layout(B, H, rows, dk, dv).total;
 }
 
 cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
@@ -358,7 +373,8 @@ cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
 
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream) {
   const long long rows = a.cu_seqlens ? (long long)a.T : (long long)a.B * a.T;
-  const TcWorkspace w = workspace_layout(a.B, a.H, rows);
+  const int DK = a.dk_size, DV = a.dv_size;
+  const TcWorkspace w = workspace_layout(a.B, a.H, rows, DK, DV);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
   auto fl = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
@@ -368,12 +384,12 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
       (const __nv_bfloat16*)a.d_out, a.g, 1.f / a.scale, a.init_state, a.d_final, bf(w.rq),
       bf(w.rk), bf(w.rv), bf(w.rdo), fl(w.rg), fl(w.s0t), fl(w.dfs), fl(w.dfst), a.cu_seqlens,
-      a.B, a.H, a.T, a.status);
+      a.B, a.H, a.T, DK, DV, a.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  // dg's per-token terms arrive from four CTAs each (two value slices of the dq
-  // and of the dk run) as fp32 atomics
+  // dg's per-token terms arrive from the dq and the dk run (one CTA per 64-wide
+  // output slice each) as fp32 atomics
   if (a.dg) {
     if ((e = cudaMemsetAsync(a.dg, 0, sizeof(float) * (size_t)(rows * a.H), stream)) !=
         cudaSuccess)
@@ -390,7 +406,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   c.out = a.dq;
   c.final_state = (a.dg && a.d_final) ? fl(w.stt) : nullptr;
   c.dot_rows = a.dg ? a.q : nullptr; c.dot_out = a.dg; c.dot_sign = 1.f;
-  c.dk = kTcDV; c.dv = kTcDK;
+  c.dk = DV; c.dv = DK;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
   // dk (reversed): the prefill of (v, do, q) with (dS_T / scale)^T, stored back
   // in token order, adding -k . dk to dg
@@ -399,7 +415,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   c.out = a.dk; c.out_reversed = true;
   c.final_state = nullptr;
   c.dot_rows = a.dg ? a.k : nullptr; c.dot_out = a.dg; c.dot_sign = -1.f;
-  c.dk = kTcDV; c.dv = kTcDK;
+  c.dk = DV; c.dv = DK;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
   // dv (reversed): the prefill of (k, q, do) with dS_T / scale, stored back in
   // token order; final state R_0
@@ -408,13 +424,13 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   c.out = a.dv; c.out_reversed = true;
   c.final_state = a.d_init;
   c.dot_rows = nullptr; c.dot_out = nullptr;
-  c.dk = kTcDK; c.dv = kTcDV;
+  c.dk = DK; c.dv = DV;
   if ((e = launch_chunk_tc(c, stream)) != cudaSuccess) return e;
 
   if (a.dg || a.d_init) {
     bwd_tc_tail_kernel<<<(unsigned)((long long)a.B * a.H), kScanThreads, 0, stream>>>(
         a.g, a.scale, (a.dg && a.d_final) ? fl(w.stt) : nullptr,
-        a.d_final ? fl(w.dfst) : nullptr, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T,
+        a.d_final ? fl(w.dfst) : nullptr, a.dg, a.d_init, a.cu_seqlens, a.B, a.H, a.T, DK, DV,
         a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -119,12 +119,13 @@ cudaError_t launch_chunk_bwd_head_bf16(const ChunkBwdArgs& a, cudaStream_t strea
 cudaError_t launch_chunk_bwd_head_f32(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_chan_f32(const ChunkBwdArgs& a, cudaStream_t stream);
-// the backward on the tensor cores, bf16, d_k = d_v = 128, with
-// chunk_bwd_tc_workspace(B, H, rows, vector_gate) bytes of workspace: per-head
-// gate, every gradient from three prefill runs; per-key-channel gate, dv from
-// one run of the per-key-channel prefill (dq, dk on the CUDA cores)
+// the backward on the tensor cores, bf16, with chunk_bwd_tc_workspace(B, H,
+// rows, dk, dv, vector_gate) bytes of workspace: per-head gate (d_k, d_v in
+// {64, 128}), every gradient from three prefill runs; per-key-channel gate
+// (d_k = d_v = 128), dv from one run of the per-key-channel prefill (dq, dk on
+// the CUDA cores)
 bool chunk_bwd_tc_supported(int dk, int dv, bool fp32_io, bool vector_gate);
-size_t chunk_bwd_tc_workspace(int B, int H, long long rows, bool vector_gate);
+size_t chunk_bwd_tc_workspace(int B, int H, long long rows, int dk, int dv, bool vector_gate);
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_tc_vec_dv(const ChunkBwdArgs& a, void* workspace,
                                        cudaStream_t stream);

@@ -275,7 +275,8 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
  *   d_init_state  fp32 [B, H, dk, dv], or NULL (not written)
  *   workspace     device scratch owned by the caller, or NULL; with at least
  *                 gla_chunk_bwd_workspace_size(...) bytes (256-byte aligned),
- *                 bf16 I/O and dk = dv = 128, the call uses the tensor cores:
+ *                 bf16 I/O and dk, dv each 64 or 128 (the per-key-channel
+ *                 gate: dk = dv = 128), the call uses the tensor cores:
  *                 the gradient of the recurrence is the same recurrence with
  *                 its operands exchanged -- dq is the prefill of (d_out, v, k),
  *                 dk and dv are prefills of (v, d_out, q) and (k, q, d_out) run

@@ -266,7 +266,12 @@ def test_chunk_bwd_workspace_size(L):
     assert nv >= tok * 128 * (3 * 2 + 4) + 2 * 4 * 128 * 128 * 4
     assert nv < tok * 128 * (3 * 2 + 4 + 4) + 2 * 4 * 128 * 128 * 4
     assert ws(2, 4, 256, 96, 192, 0, 0) == 0
-    assert ws(2, 4, 256, 128, 64, 0, 0) == 0
+    assert ws(2, 4, 256, 128, 192, 0, 0) == 0
+    assert ws(2, 4, 256, 64, 64, 0, E.GLA_FLAG_VECTOR_GATE) == 0
+    # per-head gate, head sizes 64 and 128 in any pair: the same sections at their widths
+    for dk, dv in ((64, 64), (64, 128), (128, 64)):
+        assert ws(2, 4, 256, dk, dv, 0, 0) == tok * (2 * dk + 2 * dv) * 2 + tok * 4 + \
+            4 * 2 * 4 * dk * dv * 4
     assert ws(0, 4, 256, 128, 128, 0, 0) == 0
 
 

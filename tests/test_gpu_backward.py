@@ -348,6 +348,29 @@ def test_tc_chunk_boundaries(T):
     check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label=f"tc T={T}")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_tc_head_sizes_64(dk, dv):
+    """Head sizes 64 on the tensor-core path: the three runs take (d_v, d_k),
+    (d_v, d_k) and (d_k, d_v) as their key and value sizes (a 64 key size runs
+    zero-padded to 128, a 64 value size as one slice).  Packed sequences with an
+    empty one and a ragged tail, fp32 and bf16 gradients."""
+    x, gr = inputs("varlen", lengths=[300, 0, 129, 1], H=3, dk=dk, dv=dv)
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label=f"tc {dk}x{dv}")
+    g16 = run_gpu(x, gr, tc=True)
+    for a, b in zip(g16[:3], got[:3]):
+        assert a.dtype == torch.bfloat16 and torch.equal(a, b.to(torch.bfloat16))
+    torch.testing.assert_close(got[4][1].cpu(), gr["d_final_state"][1], rtol=1e-6, atol=0)
+
+
+def test_tc_head_size_64_strong_decays():
+    """d_k = d_v = 64 with gates around -40 (every chunk wide in all three runs)."""
+    x, gr = inputs(B=1, T=300, H=2, dk=64, dv=64, g_mu=-2.0, g_div=0.05)
+    xc = dict(x, g=x["g"].clamp(min=-30.0))
+    got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
+    check(got[:3] + (None,) + got[4:], run_ref(xc, gr), tol=TOL_GRAD_TC, label="tc 64 strong")
+
+
 def test_tc_zero_gate():
     """g = 0 (no decay): the gradients are those of causal linear attention."""
     x, gr = inputs(B=1, T=200, H=2)
