@@ -9,6 +9,9 @@ largest width), over static buffers, with the states kept in a pool of pages
 addressed by slot (``gla_decode_step_slots``): a batch of n <= W live rows is
 copied into the first n rows of the static buffers, the remaining W - n rows
 get slot -1 (rows the kernel skips), and the graph of width W is replayed.
+Rows past the widest batch since the last clean-up already hold -1, so the
+padding costs a fill launch only on a step whose batch is narrower than the
+previous one.
 
 The state pool, the dtypes and the head sizes are fixed at construction.  The
 fast path is ``buffers(n)`` (views of the static inputs, for the producer of
@@ -74,6 +77,7 @@ class DecodeGraphs:
         self.g = torch.zeros((W, H, dk) if vector_gate else (W, H), dtype=torch.float32,
                              device=dev)
         self.slots = torch.full((W,), -1, dtype=torch.int32, device=dev)
+        self._dirty = 0  # slots rows at or past this index hold -1
         self.out = torch.zeros(W, H, dv, dtype=out_dtype or dtype, device=dev)
         self.graphs = {}
         side = torch.cuda.Stream(device=dev)
@@ -100,6 +104,7 @@ class DecodeGraphs:
         """Views of the first ``n`` rows of the static inputs (q, k, v, g, slots)
         for the next ``run(n)``."""
         pick_bucket(self.buckets, n)
+        self._dirty = max(self._dirty, n)  # the caller writes slots rows [0, n)
         return {"q": self.q[:n], "k": self.k[:n], "v": self.v[:n], "g": self.g[:n],
                 "slots": self.slots[:n]}
 
@@ -108,8 +113,9 @@ class DecodeGraphs:
         slots distinct pool pages): pad to the bucket with slot -1 rows and
         replay its graph.  Returns out [n, H, dv]."""
         w = pick_bucket(self.buckets, n)
-        if w > n:
-            self.slots[n:w].fill_(-1)
+        if self._dirty > n:  # a wider batch ran before: its extra rows back to -1
+            self.slots[n:self._dirty].fill_(-1)
+        self._dirty = n
         self.graphs[w].replay()
         return self.out[:n]
 
