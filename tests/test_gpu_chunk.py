@@ -174,11 +174,13 @@ def test_minus_inf_gate_inside_chunks(cuda_ok, gate):
 
 
 @pytest.mark.parametrize("gate", ["scalar", "vector"])
-@pytest.mark.parametrize("positions", [[5, 40, 90], [0, 1, 2, 127], [64, 65, 66, 200, 201, 202]])
+@pytest.mark.parametrize("positions", [[5, 40, 90], [0, 1, 2, 127], [64, 65, 66, 200, 201, 202],
+                                       [10, 20, 30, 40, 50]])
 def test_several_resets_in_one_chunk(cuda_ok, positions, gate):
-    """Three or more -inf gates in one chunk push its decay span past 2^96: the
-    per-head kernel takes its explicit-decay path for that chunk, the
-    per-key-channel kernel its token-by-token path."""
+    """-inf gates (clamped at -30, 43 in log2 each): three or more in one chunk
+    push its decay span past 2^96 -- two such chunks in a row in the third
+    case -- so the per-head kernel takes its explicit-decay path for them and
+    the per-key-channel kernel its token-by-token path."""
     x = small(B=2, T=300, H=2, gate=gate)
     g = x["g"].clone()
     g[:, positions] = float("-inf")
