@@ -6,9 +6,10 @@
 //     o += sigmoid(q . (aug * k)) * v                 (self-augmentation)
 //     o  = o / sqrt(mean_j o_j^2 + eps) * w[h]        (head RMSNorm)
 //     o *= silu(z)                                    (output gate)
-// each step optional.  One warp per (token, head): the two dot products are
-// warp reductions, every lane owns dv / 32 adjacent columns (and dk / 32 key
-// channels), so each tensor is read as one contiguous span per warp.  A pure
+// each step optional.  Sixteen lanes per (token, head): the two dot products
+// are reductions over those lanes, every lane owns dv / 16 adjacent columns
+// (and dk / 16 key channels), so each tensor is read as one contiguous span
+// per unit.  A pure
 // stream over o, q, k, v and z (HBM-bound); the decode kernel fuses the same
 // steps instead.
 #include "gla_internal.cuh"
@@ -18,11 +19,7 @@ namespace {
 
 constexpr int kEpiWarps = 8;
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
+
 
 // N consecutive elements as fp32: 16-, 8- or 4-byte loads for even N (the
 // caller's tensors are 16-byte aligned and every run starts on a multiple of
@@ -47,7 +44,18 @@ __device__ __forceinline__ void load_run(const T* __restrict__ p, float (&x)[N])
       }
     }
   } else {  // bf16: pairs in 32-bit words
-    if constexpr (N % 4 == 0) {
+    if constexpr (N % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < N; i += 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + i));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[i + 2 * e] = __uint_as_float(w[e] << 16);
+          x[i + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+      }
+    } else if constexpr (N % 4 == 0) {
 #pragma unroll
       for (int i = 0; i < N; i += 4) {
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + i));
@@ -69,10 +77,23 @@ __device__ __forceinline__ void load_run(const T* __restrict__ p, float (&x)[N])
 
 template <int N, typename T>
 __device__ __forceinline__ void store_run(T* __restrict__ p, const float (&x)[N]) {
-  if constexpr (sizeof(T) == 4) {
+  if constexpr (sizeof(T) == 4 && N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4)
+      *reinterpret_cast<float4*>(p + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+  } else if constexpr (sizeof(T) == 4) {
 #pragma unroll
     for (int i = 0; i < N; i += 2)
       *reinterpret_cast<float2*>(p + i) = make_float2(x[i], x[i + 1]);
+  } else if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+      auto pack = [&](int e) {
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[i + 2 * e])) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[i + 2 * e + 1])) << 16);
+      };
+      *reinterpret_cast<uint4*>(p + i) = make_uint4(pack(0), pack(1), pack(2), pack(3));
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
@@ -82,20 +103,36 @@ __device__ __forceinline__ void store_run(T* __restrict__ p, const float (&x)[N]
   }
 }
 
-// One warp per (row, head): lane l owns the dv / 32 adjacent columns from
-// l * dv / 32 and the dk / 32 adjacent key channels from l * dk / 32, read and
-// written as runs (every access of the warp is one contiguous span).
+// kEpiLanes lanes per (row, head), two units a warp: lane l of a unit owns the
+// dv / kEpiLanes adjacent columns from l * dv / kEpiLanes and the dk /
+// kEpiLanes adjacent key channels from l * dk / kEpiLanes, read and written as
+// runs (16-byte vectors at d = 128 in bf16; each unit's access is one
+// contiguous span).
+constexpr int kEpiLanes = 16;
+
+// sum over the kEpiLanes lanes of a unit (an aligned group of the warp)
+__device__ __forceinline__ float unit_sum(float x) {
+#pragma unroll
+  for (int off = kEpiLanes / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
 template <typename IO, typename OUT, int DK, int DV>
 __global__ void __launch_bounds__(kEpiWarps * 32)
 epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __restrict__ k,
                 const IO* __restrict__ v, const float* __restrict__ aug,
                 const float* __restrict__ norm_w, float eps, const IO* __restrict__ z,
                 long long units, int H) {
-  constexpr int PER = DV / 32;   // columns per lane
-  constexpr int PK = DK / 32;    // key channels per lane
-  const int lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * kEpiWarps + (threadIdx.x >> 5);  // row * H + h
-  if (unit >= units) return;
+  constexpr int PER = DV / kEpiLanes;   // columns per lane
+  constexpr int PK = DK / kEpiLanes;    // key channels per lane
+  static_assert(DV % kEpiLanes == 0 && DK % kEpiLanes == 0, "whole runs");
+  const int lane = (threadIdx.x & 31) % kEpiLanes;
+  const long long unit0 = (long long)blockIdx.x * kEpiWarps * (32 / kEpiLanes) +
+                          (threadIdx.x >> 5) * (32 / kEpiLanes) + (threadIdx.x & 31) / kEpiLanes;
+  // a unit past the end still joins its warp's shuffles, on unit 0's data, and
+  // stores nothing
+  const bool valid = unit0 < units;
+  const long long unit = valid ? unit0 : 0;  // row * H + h
   const int h = (int)(unit % H);
   const long long ob = unit * DV + lane * PER;
   const long long kb = unit * DK + lane * PK;
@@ -114,7 +151,7 @@ epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __res
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < PK; ++i) s = fmaf(qv[i] * av[i], kv[i], s);
-    s = warp_sum(s);
+    s = unit_sum(s);
     const float gate = 1.f / (1.f + expf(-s));
 #pragma unroll
     for (int c = 0; c < PER; ++c) o[c] = fmaf(gate, vv[c], o[c]);
@@ -123,7 +160,7 @@ epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __res
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < PER; ++c) ss = fmaf(o[c], o[c], ss);
-    ss = warp_sum(ss);
+    ss = unit_sum(ss);
     const float r = rsqrtf(ss / DV + eps);
 #pragma unroll
     for (int c = 0; c < PER; ++c) o[c] *= r * w[c];
@@ -132,13 +169,14 @@ epilogue_kernel(OUT* __restrict__ out, const IO* __restrict__ q, const IO* __res
 #pragma unroll
     for (int c = 0; c < PER; ++c) o[c] *= zz[c] / (1.f + expf(-zz[c]));
   }
-  store_run<PER>(out + ob, o);
+  if (valid) store_run<PER>(out + ob, o);
 }
 
 template <typename IO, typename OUT, int DK>
 cudaError_t launch_dv(const EpilogueArgs& a, cudaStream_t stream) {
   const long long units = a.rows * a.H;
-  const unsigned grid = (unsigned)((units + kEpiWarps - 1) / kEpiWarps);
+  const long long per_cta = (long long)kEpiWarps * (32 / kEpiLanes);
+  const unsigned grid = (unsigned)((units + per_cta - 1) / per_cta);
 #define GLA_EPI(DV)                                                                          \
   epilogue_kernel<IO, OUT, DK, DV><<<grid, kEpiWarps * 32, 0, stream>>>(                     \
       (OUT*)a.out, (const IO*)a.q, (const IO*)a.k, (const IO*)a.v, a.aug, a.norm_w, a.eps,   \
