@@ -597,8 +597,28 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
       // its parity's phase of the chunk barrier may be reused
       if (c >= 2 && !wait_w(kAck0 + (c & 1), ph((c - 2) >> 1))) { ok = false; break; }
       if (tid == 256) wide_ring[c & 3] = wide ? 1 : 0;
-      if (!wait_w(kQKFull, ph(c))) { ok = false; break; }
       if (!wide) {
+        // state pass first: S <- diag(exp G_L) S in TMEM, S' = its bf16 copy.  It
+        // needs only the previous chunk's MMA4, so it runs while Q and K land.
+        if (last_tc && !wait_w(kSFull, ph(n - 1))) { ok = false; break; }
+        tc_fence_after();
+        float sv[64];
+        s_load(sv, !s_in_tmem);
+        const float dec = exp2f(totr * kLog2e);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) sv[j] *= dec;
+        s_store(sv);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(sb + hf * kPanel + sw128_offset(si, cc)) =
+              make_uint4(pack_bf16x2(sv[8 * cc], sv[8 * cc + 1]),
+                         pack_bf16x2(sv[8 * cc + 2], sv[8 * cc + 3]),
+                         pack_bf16x2(sv[8 * cc + 4], sv[8 * cc + 5]),
+                         pack_bf16x2(sv[8 * cc + 6], sv[8 * cc + 7]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(kSbReady);
+        if (!wait_w(kQKFull, ph(c))) { ok = false; break; }
         // pass 2: Q' = q exp(G - G_L) in place, Kt = k exp(G_L - G) as hi (in
         // place) + lo; rows past the sequence end are zeroed
         float G0 = off0 * kLog2e, G1 = off1 * kLog2e;
@@ -628,29 +648,11 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
           vote[c & 1] = 0;  // read by all before the last barrier; next used by chunk c + 2
         }
         warp_arrive(kScaled0 + (c & 1));
-        // state pass: S <- diag(exp G_L) S in TMEM, S' = its bf16 copy
-        if (last_tc && !wait_w(kSFull, ph(n - 1))) { ok = false; break; }
-        tc_fence_after();
-        float sv[64];
-        s_load(sv, !s_in_tmem);
-        const float dec = exp2f(totr * kLog2e);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) sv[j] *= dec;
-        s_store(sv);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(sb + hf * kPanel + sw128_offset(si, cc)) =
-              make_uint4(pack_bf16x2(sv[8 * cc], sv[8 * cc + 1]),
-                         pack_bf16x2(sv[8 * cc + 2], sv[8 * cc + 3]),
-                         pack_bf16x2(sv[8 * cc + 4], sv[8 * cc + 5]),
-                         pack_bf16x2(sv[8 * cc + 6], sv[8 * cc + 7]));
-        fence_proxy_async_smem();
-        tc_fence_before();
-        warp_arrive(kSbReady);
         s_in_tmem = true;
         last_tc = true;
         ++n;
       } else {
+        if (!wait_w(kQKFull, ph(c))) { ok = false; break; }
         warp_arrive(kScaled0 + (c & 1));
         if (last_tc && !wait_w(kSFull, ph(n - 1))) { ok = false; break; }
         if (!wait_w(kVFull, ph(c))) { ok = false; break; }

@@ -212,18 +212,19 @@ def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
             yield from group_sync()          # wide vote
             if c >= 2:
                 yield ("wait", ("Ack", c & 1), (c - 2) >> 1)
-            yield ("wait", ("QKFull",), c)
             if not wide(c):
+                if last_tc:                  # the state pass first
+                    yield ("wait", ("SFull",), n - 1)
+                yield ("arrive", ("SbReady",))
+                yield ("wait", ("QKFull",), c)
                 yield from group_sync()      # done with g
                 if first:
                     yield ("arrive", ("GEmpty",))
                 yield ("arrive", ("Scaled", c & 1))
-                if last_tc:
-                    yield ("wait", ("SFull",), n - 1)
-                yield ("arrive", ("SbReady",))
                 last_tc = True
                 n += 1
             else:
+                yield ("wait", ("QKFull",), c)
                 yield ("arrive", ("Scaled", c & 1))
                 if last_tc:
                     yield ("wait", ("SFull",), n - 1)
