@@ -1,0 +1,142 @@
+"""The tensor-core prefill's rounding scheme, emulated on the CPU.
+
+The per-head tcgen05 prefill multiplies bf16 operands into fp32 accumulators.
+Per chunk of 128 tokens (G the in-chunk prefix sums of the clamped gate in log2
+units, L the last token) it forms W_j = 2^(G_L - G_j), splits W V into a bf16
+hi part and a bf16 lo part (the rest), rounds P' = causal(Q K^T) to bf16 once
+and keeps a lo part of P' on the four 32 x 32 diagonal blocks only; the output
+is 2^(G_t - G_L) (Q bf16(2^G_L S) + P' (W V)) with both W V parts and the
+diagonal lo pass, and the state takes 2^G_L S + K^T (W V hi + lo).  A chunk
+whose span G_0 - G_L exceeds 96 takes the explicit path (P = A 2^(G_t - G_j)
+on the causal part, raw V).
+
+This test restates that arithmetic in numpy (bf16 rounding to nearest-even;
+products of bf16 values exact, sums in fp64 -- tighter than the hardware's
+fp32 accumulation, which the GPU parity tests cover) and checks the scheme
+against the oracle: with its lo parts it meets the output bar (2e-2 of the
+RMS) and the state bar (1e-3), and without them it misses them -- on the
+workload's gates as on strong decays.  It pins the design of the kernel's
+numerics, not the kernel: the GPU tests compare the kernel itself.
+"""
+import numpy as np
+import torch
+
+import gla_inputs
+import oracle
+from parity import rel_max
+
+C = 128
+LOG2E = 1.4426950408889634
+
+
+def bf16(x):
+    """Round fp32 values to bf16 (nearest, ties to even), returned as fp32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def emulate(x, lo=True):
+    """The chunked bf16 scheme over dense inputs; ``lo`` keeps the W V lo part
+    and the diagonal lo part of P'."""
+    q = x["q"].float().numpy()
+    k = x["k"].float().numpy()
+    v = x["v"].float().numpy()
+    g = np.maximum(x["g"].numpy().astype(np.float32), -30.0)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    s0 = x["init_state"]
+    out = np.zeros((B, T, H, dv))
+    fin = np.zeros((B, H, dk, dv))
+    causal = np.tril(np.ones((C, C), bool))
+    diag = (np.arange(C)[:, None] // 32) == (np.arange(C)[None, :] // 32)
+    for b in range(B):
+        for h in range(H):
+            S = (s0[b, h].numpy() if s0 is not None else np.zeros((dk, dv))).astype(np.float32)
+            for c0 in range(0, T, C):
+                n = min(C, T - c0)
+                Q = np.zeros((C, dk), np.float32)
+                K = np.zeros((C, dk), np.float32)
+                V = np.zeros((C, dv), np.float32)
+                Q[:n], K[:n], V[:n] = q[b, c0:c0 + n, h], k[b, c0:c0 + n, h], v[b, c0:c0 + n, h]
+                G = np.zeros(C, np.float32)
+                G[:n] = np.cumsum(g[b, c0:c0 + n, h]) * np.float32(LOG2E)
+                G[n:] = G[n - 1]
+                GL = G[-1]
+                A = Q.astype(np.float64) @ K.T.astype(np.float64)
+                W = np.exp2(GL - G)
+                W[n:] = 0.0
+                wv = (W[:, None] * V).astype(np.float32)
+                hi = bf16(wv)
+                lo_part = bf16(wv - hi) if lo else np.zeros_like(hi)
+                if G[0] - GL <= 96:
+                    P = np.where(causal, A, 0.0).astype(np.float32)
+                    Ph = bf16(P)
+                    Pl = np.where(diag, bf16(P - Ph), 0.0) if lo else np.zeros((C, C))
+                    O = (Q.astype(np.float64) @ bf16(np.exp2(GL) * S).astype(np.float64)
+                         + Ph.astype(np.float64) @ (hi.astype(np.float64) + lo_part)
+                         + Pl @ hi.astype(np.float64))
+                    o = x["scale"] * np.exp2(G - GL)[:, None] * O
+                else:
+                    D = np.exp2(np.minimum(G[:, None] - G[None, :], 0.0))
+                    P = np.where(causal, A * D, 0.0).astype(np.float32)
+                    Ph = bf16(P)
+                    Pl = np.where(diag, bf16(P - Ph), 0.0) if lo else np.zeros((C, C))
+                    O = (np.exp2(G)[:, None] * (Q.astype(np.float64) @ bf16(S).astype(np.float64))
+                         + (Ph.astype(np.float64) + Pl) @ V.astype(np.float64))
+                    o = x["scale"] * O
+                out[b, c0:c0 + n, h] = o[:n]
+                S = (np.exp2(GL) * S.astype(np.float64)
+                     + K.T.astype(np.float64) @ (hi.astype(np.float64) + lo_part)).astype(np.float32)
+            fin[b, h] = S
+    return out, fin
+
+
+def inputs(mu=None, **kw):
+    x = gla_inputs.prefill_inputs(gla_inputs.WORKLOADS["prefill"], seed=11, **kw)
+    if mu is not None:
+        gen = torch.Generator().manual_seed(5)
+        x["g"] = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
+    return x
+
+
+def errors(x, lo=True):
+    o_ref, s_ref = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                    init_state=x["init_state"])
+    o, s = emulate(x, lo)
+    return rel_max(o, o_ref), rel_max(s, s_ref)
+
+
+def test_lo_parts_are_needed_on_the_workload_gates():
+    """The prefill workload's gates (logsigmoid(N(3, 1))), four chunks and a
+    ragged tail.  With the lo parts: output 1.4e-2, state 1.9e-5 of their RMS.
+    Rounded once instead, the state misses its bar ninefold (9e-3) and the
+    output misses its own (2.3e-2)."""
+    x = inputs(B=1, T=600, H=2)
+    e_o, e_s = errors(x)
+    assert e_o <= 1.6e-2 and e_s <= 1e-4, (e_o, e_s)
+    e_o_plain, e_s_plain = errors(x, lo=False)
+    assert e_o_plain > 2e-2 and e_s_plain > 1e-3, (e_o_plain, e_s_plain)
+
+
+def test_lo_parts_are_needed_under_strong_decay():
+    """Gates logsigmoid(N(0, 1)) (about -0.8 a token): a row's output is
+    dominated by its last few tokens, so rounding P' and W V once shows --
+    3.1e-2 without the lo parts, 1.1e-2 with them."""
+    x = inputs(mu=0.0, B=2, T=400, H=2)
+    e_o, e_s = errors(x)
+    assert e_o <= 1.2e-2 and e_s <= 1e-4, (e_o, e_s)
+    e_o_plain, _ = errors(x, lo=False)
+    assert e_o_plain > 2e-2, e_o_plain
+
+
+def test_explicit_path_on_wide_chunks():
+    """Gates around -3 a token: every chunk's span passes 2^96 and takes the
+    explicit path, P = A 2^(G_t - G_j) with raw V.  The diagonal lo part of P
+    carries it: 9e-4 with it, 2.4e-2 without."""
+    x = inputs(mu=-3.0, B=1, T=300, H=2)
+    e_o, e_s = errors(x)
+    assert e_o <= 2e-3 and e_s <= 1e-4, (e_o, e_s)
+    e_o_plain, _ = errors(x, lo=False)
+    assert e_o_plain > 2e-2, e_o_plain
