@@ -23,7 +23,8 @@ and ``backward`` -- the chunked backward (gla_chunk_bwd) on the prefill
 workload's sizes, with its roofline against the CUDA cores' fp32 FMA peak.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference for parity, a
-deliberately plain program) on a bounded sample of the same workload.
+deliberately plain program) on the same prefill workload, whole (about 0.2 s
+per step on 16 host cores, so K steps end within seconds).
 
 Multi-GPU (torchrun): every rank runs its own replica (the (sequence, head)
 units are independent, so there is no data-path collective); the process
@@ -35,7 +36,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -75,6 +75,21 @@ def prefill_flops(w, B, T, rows=None) -> int:
     per token and head 2 * (C * (dk + dv) + 2 * dk * dv)."""
     rows = B * T if rows is None else rows
     return 2 * (w.chunk * (w.dk + w.dv) + 2 * w.dk * w.dv) * rows * w.H
+
+
+def prefill_config(world: int) -> dict:
+    """The ``config`` of both arms' JSON lines: the prefill workload the
+    headline value is measured on."""
+    wp = gla_inputs.WORKLOADS["prefill"]
+    pb = prefill_bytes(wp, wp.B, wp.T)
+    return {
+        "workload": f"simple-GLA chunked prefill B={wp.B} H={wp.H} T={wp.T} dk=dv={wp.dk} "
+                    f"chunk={wp.chunk} bf16 I/O, fp32 states",
+        "global_batch": wp.B * world, "seq_len": wp.T, "heads": wp.H, "dk": wp.dk,
+        "dv": wp.dv, "chunk": wp.chunk, "parallelism": f"replicas x{world}",
+        "l2": f"{N_SETS} rotating prefill input sets "
+              f"({N_SETS * pb / 1e6:.0f} MB > 129 MB L2); decode state 1.34 GB",
+    }
 
 
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops per FMA at
@@ -134,17 +149,18 @@ def kernel_source_hash(name: str) -> str:
 
 
 def profiled_traffic(summary: str, source: str):
-    """DRAM bytes per launch recorded in a committed ncu summary, or None when
-    the summary is missing or the kernel source changed since it was taken."""
-    path = os.path.join(PROFILE_DIR, summary)
+    """DRAM bytes per launch recorded beside a committed ncu summary (the
+    ``.json`` of the same name: ``traffic_bytes_per_launch`` and the kernel
+    source's hash), or None when it is missing or the kernel source changed
+    since the capture."""
+    path = os.path.join(PROFILE_DIR, os.path.splitext(summary)[0] + ".json")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
-    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_t or not m_h or m_h.group(1) != kernel_source_hash(source):
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash(source):
         return None
-    return float(m_t.group(1))
+    return float(rec["traffic_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------ clocks
@@ -265,6 +281,19 @@ def cpu_baseline(budget_s: float = 10.0):
     prefill = dict(value=wp.B * wp.T * reps / dt, unit="tokens/s", cores=cores, kind="oracle",
                    sample=f"full prefill workload (B={wp.B}, T={wp.T}, H={wp.H}, d={wp.dk}) "
                           f"x {reps}, fp64 token-by-token recurrence, {dt:.1f} s")
+    # the same program on one core: the first sequence of the workload (all heads)
+    one = {n: x[n][:1].contiguous() for n in ("q", "k", "v", "g", "init_state")}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.recurrent(one["q"], one["k"], one["v"], one["g"], x["scale"],
+                         init_state=one["init_state"], nthreads=1)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s / 3:
+            break
+    dt1 = time.perf_counter() - t0
+    prefill["one_core"] = dict(value=wp.T * reps / dt1, unit="tokens/s", cores=1,
+                               sample=f"one sequence (T={wp.T}, H={wp.H}) x {reps}, "
+                                      f"{dt1:.1f} s")
     wd = gla_inputs.WORKLOADS["decode"]
     d = gla_inputs.decode_inputs(wd, steps=1)
     reps, t0 = 0, time.perf_counter()
@@ -724,16 +753,10 @@ def run_gla(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded normal q, k, v; logsigmoid gates; no dataset)",
-        "config": {
-            "workload": f"simple-GLA chunked prefill B={B} H={H} T={T} dk=dv={wp.dk} "
-                        f"chunk={wp.chunk} bf16 I/O, fp32 states",
-            "global_batch": B * world, "seq_len": T, "heads": H, "dk": wp.dk, "dv": wp.dv,
-            "chunk": wp.chunk, "parallelism": f"replicas x{world}",
-            "l2": f"{N_SETS} rotating prefill input sets "
-                  f"({N_SETS * pb / 1e6:.0f} MB > 129 MB L2); decode state 1.34 GB",
-        },
+        "config": prefill_config(world),
         "prefill": {
-            "ms_per_call": statistics.mean(pre_ms), "tokens_per_call": B * T,
+            "ms_per_call": statistics.mean(pre_ms),
+            "ms_per_call_median": statistics.median(pre_ms), "tokens_per_call": B * T,
             "calls": args.steps,
             "roofline": {
                 "kernel": "chunk_tc_kernel", "bound": "hbm", "achieved": pre_gbs, "peak": hbm,
@@ -752,6 +775,7 @@ def run_gla(args, world, rank, local):
             "workload": f"decode step N={wd.N} H={wd.H} dk=dv={wd.dk}, fp32 state in place, "
                         f"{DECODE_STEPS} consecutive steps per timing",
             "ms_per_step": dec_launch_s * 1e3,
+            "ms_per_step_median": statistics.median(dec_ms) / DECODE_STEPS,
             "roofline": dec_roof,
         },
         "e2e": {"value": B * T * e2e_steps * world / e2e_pre_s, "unit": "tokens/s",
@@ -861,9 +885,7 @@ def run_reference(args, world, rank):
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded normal q, k, v; logsigmoid gates; no dataset)",
-        "config": {"workload": f"simple-GLA chunked prefill B={wp.B} H={wp.H} T={wp.T} "
-                               f"dk=dv={wp.dk} chunk={wp.chunk} bf16 I/O, fp32 states",
-                   "global_batch": wp.B, "seq_len": wp.T, "parallelism": "host cores"},
+        "config": prefill_config(world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -163,7 +163,9 @@ def chunk_bwd(q, k, v, g, d_out, scale: Optional[float] = None, init_state=None,
     least ``gla_chunk_bwd_workspace_size`` bytes) or a fresh allocation; False
     runs the fp32 CUDA-core kernels.  ``fixed_workspace``: call
     gla_chunk_bwd_fixed_workspace instead, whose workspace is the library's own
-    fixed device buffer (nothing is allocated; ``workspace`` is ignored).
+    fixed device buffer (nothing is allocated; ``workspace`` is ignored); a
+    call whose workspace need exceeds that buffer raises GlaError
+    (GLA_ERR_UNSUPPORTED).
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("d_out", d_out)):
         _check(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")

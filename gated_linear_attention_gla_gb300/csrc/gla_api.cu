@@ -5,6 +5,7 @@
 // array) is checked on the device; see seq_bounds() in gla_internal.cuh.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -63,11 +64,15 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 constexpr long long kMaxElems = 1ll << 40;  // per tensor; keeps index arithmetic exact
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+// the text of the calling thread's most recent non-CUDA failure that carries
+// one (empty: the most recent failure was a CUDA error, or there was none)
+thread_local char g_last_text[192] = "";
 
 // Map a CUDA result to a status, remembering the error for gla_last_error_string.
 gla_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return GLA_OK;
   g_last_cuda_error = e;
+  g_last_text[0] = '\0';
   return GLA_ERR_CUDA;
 }
 
@@ -78,6 +83,7 @@ extern "C" {
 const char* gla_version(void) { return "0.1.0"; }
 
 const char* gla_last_error_string(void) {
+  if (g_last_text[0] != '\0') return g_last_text;
   return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
@@ -348,13 +354,21 @@ gla_status gla_chunk_bwd_fixed_workspace(const void* q, const void* k, const voi
                      dg, d_init_state, cu_seqlens, B, H, T, dk, dv, nullptr, 0, stream, flags,
                      true);
   if (st != GLA_OK) return st;
-  // the library's buffer is used (and its module loaded) only when the
-  // tensor-core path covers the call and its workspace fits
+  // The library's buffer is used (and its module loaded) only when the
+  // tensor-core path covers the call; a call whose workspace need exceeds the
+  // buffer is rejected before anything is enqueued.
   void* ws = nullptr;
   if (B > 0 && H > 0 && T > 0) {
     const size_t need = gla_chunk_bwd_workspace_size(B, H, T, dk, dv, cu_seqlens != nullptr,
                                                      flags);
-    if (need > 0 && need <= gla::kBwdFixedWorkspaceBytes) {
+    if (need > gla::kBwdFixedWorkspaceBytes) {
+      std::snprintf(g_last_text, sizeof(g_last_text),
+                    "gla_chunk_bwd_fixed_workspace: the call needs %zu bytes of workspace, "
+                    "the fixed buffer holds %zu",
+                    need, gla::kBwdFixedWorkspaceBytes);
+      return GLA_ERR_UNSUPPORTED;
+    }
+    if (need > 0) {
       cudaError_t err;
       ws = gla::bwd_fixed_workspace(&err);
       if (!ws) return cuda_status(err);

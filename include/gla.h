@@ -305,15 +305,39 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
                          size_t workspace_bytes, gla_stream_t stream, unsigned flags);
 
 /*
- * gla_chunk_bwd_fixed_workspace -- gla_chunk_bwd without a caller workspace:
- * the tensor-core path takes its workspace from a fixed device buffer inside
- * the library (GLA_BWD_FIXED_WORKSPACE_BYTES, a static device array placed on
- * the GPU when this function first needs it), so the call allocates nothing.
- * Calls whose workspace need (gla_chunk_bwd_workspace_size) exceeds the buffer,
- * or that the tensor-core path does not cover, run on the CUDA cores.
- * Arguments, results and errors as gla_chunk_bwd.  The buffer is one per GPU:
- * calls that use it must not overlap in time (issue them on one stream, or
- * synchronise between them).
+ * gla_chunk_bwd_fixed_workspace -- gla_chunk_bwd for callers that cannot
+ * allocate device memory when they need the gradient (code running inside a
+ * caching allocator's callbacks, real-time threads that must not take the
+ * driver's allocation lock, embedders whose memory is reserved up front): the
+ * tensor-core path takes its workspace from a fixed device buffer inside the
+ * library, so the call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).  The pages have no counterpart of this entry
+ * point; it is a deployment convenience.
+ *
+ * The buffer is a static device array of GLA_BWD_FIXED_WORKSPACE_BYTES
+ * (384 MiB).  With CUDA's lazy module loading (CUDA_MODULE_LOADING=LAZY, the
+ * default) it is placed on a GPU the first time this function needs it there;
+ * with eager loading every process that loads libgla.so reserves it on every
+ * GPU it uses, forward-only users included.  Once placed it stays until the
+ * process exits.  The first call that needs it on a device looks up its
+ * device address (cudaGetSymbolAddress) and caches it: make that first call
+ * before capturing any stream into a CUDA graph.
+ *
+ * Sizes: a call whose workspace need (gla_chunk_bwd_workspace_size) exceeds
+ * the buffer is rejected with GLA_ERR_UNSUPPORTED before anything is enqueued,
+ * and gla_last_error_string() states the need and the limit (with d_k = d_v =
+ * 128 and 16 heads the buffer covers about 20,000 tokens, e.g. ten sequences
+ * of 2,048);
+ * such a call can go to gla_chunk_bwd with workspace = NULL, which runs the
+ * CUDA-core kernels and needs no workspace either.  Calls that the tensor-core
+ * path does not cover (fp32 I/O, other head sizes) need no workspace and run
+ * on the CUDA cores as with gla_chunk_bwd.
+ *
+ * Sharing: every call on a GPU uses the same buffer, and a call overwrites
+ * what the previous one left there (each call writes every workspace byte it
+ * reads, so nothing depends on earlier contents).  Calls that overlap in time
+ * on the GPU race on it: issue them on one stream, or synchronise between them.
+ * Arguments, results and errors otherwise as gla_chunk_bwd.
  */
 #define GLA_BWD_FIXED_WORKSPACE_BYTES ((size_t)384 << 20)
 gla_status gla_chunk_bwd_fixed_workspace(const void *q, const void *k, const void *v,
@@ -354,8 +378,10 @@ const char *gla_status_string(gla_status status);
  */
 gla_status gla_status_sync(gla_stream_t stream);
 
-/* Text of the CUDA error behind the calling thread's most recent GLA_ERR_CUDA
- * (static storage, never NULL; "no error" if there was none). */
+/* Text of the calling thread's most recent failure: the CUDA error behind a
+ * GLA_ERR_CUDA, or the size limit behind gla_chunk_bwd_fixed_workspace's
+ * GLA_ERR_UNSUPPORTED (thread-local storage, never NULL; "no error" if there
+ * was none). */
 const char *gla_last_error_string(void);
 
 /* Library version, "major.minor.patch". */

@@ -289,6 +289,27 @@ def test_chunk_bwd_fixed_workspace_rejects_before_launch(L):
     assert call(T=-1) == E.GLA_ERR_INVALID_ARG
 
 
+def test_chunk_bwd_fixed_workspace_rejects_oversize_on_the_host(L):
+    """A call whose workspace need exceeds the fixed 384 MiB buffer is rejected
+    on the host, before any CUDA call (there is no GPU here, so a CUDA call
+    would have failed with GLA_ERR_CUDA instead), and the message names the
+    need and the limit."""
+    big = [(i + 1) << 32 for i in range(12)]  # fake device addresses 4 GiB apart
+    B, H, T = 16, 16, 2048
+    need = _binding.chunk_bwd_workspace_size(B, H, T, 128, 128, False, 0)
+    assert need > 384 << 20
+    rc = _binding.gla_chunk_bwd_fixed_workspace(*big[:4], 0.1, big[4], big[5], big[6],
+                                                *big[7:12], 0, B, H, T, 128, 128, 0, 0)
+    assert rc == E.GLA_ERR_UNSUPPORTED
+    msg = L.gla_last_error_string().decode()
+    assert str(need) in msg and str(384 << 20) in msg, msg
+    # a smaller call with the same pointers gets past this check and fails only
+    # where it needs the GPU
+    rc = _binding.gla_chunk_bwd_fixed_workspace(*big[:4], 0.1, big[4], big[5], big[6],
+                                                *big[7:12], 0, 2, H, T, 128, 128, 0, 0)
+    assert rc == E.GLA_ERR_CUDA
+
+
 def test_chunk_fwd_mixer_rejects_before_launch(L):
     def call(**kw):
         a = dict(q=FAKE[0], k=FAKE[1], v=FAKE[2], g=FAKE[3], init=FAKE[4], out=FAKE[5],

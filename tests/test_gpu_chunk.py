@@ -5,8 +5,8 @@ I/O, chunk sizes 16/32/64) and the bf16 tensor-core path (chunk 128) -- at
 sizes the oracle finishes in seconds that still span several chunks and a
 ragged tail, the edge cases (T = 1, T < chunk, empty and length-1 packed
 sequences, no initial/final state, in-place state, g = -inf), the method's
-invariants on the GPU path, and every workload at full size on sampled
-(sequence, head) pairs.
+invariants on the GPU path, and every workload at full size, every element
+of the output and final state.
 """
 import numpy as np
 import pytest
@@ -338,35 +338,31 @@ def test_continuation_from_final_state(cuda_ok):
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads, sampled (sequence, head) pairs recomputed by the oracle.
+# Full-size workloads, every element against the oracle.
 # ---------------------------------------------------------------------------
-def _sampled_check(x, out, fin, pairs):
-    cu = x["cu_seqlens"]
-    errs_o, errs_s = [], []
-    for (s, h) in pairs:
-        if cu is None:
-            sl = (slice(s, s + 1), slice(None), slice(h, h + 1))
-        else:
-            a, b = int(cu[s]), int(cu[s + 1])
-            sl = (slice(0, 1), slice(a, b), slice(h, h + 1))
-        sub = {n: x[n][sl].contiguous() for n in ("q", "k", "v", "g")}
-        init = None if x["init_state"] is None else x["init_state"][s:s + 1, h:h + 1]
-        o_ref, s_ref = oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], x["scale"],
-                                        init_state=init)
-        errs_o.append(rel_max(to_np(out[sl]), o_ref))
-        errs_s.append(rel_max(to_np(fin[s:s + 1, h:h + 1]), s_ref))
-    assert max(errs_o) <= out_tol(x["q"].dtype), errs_o
-    assert max(errs_s) <= TOL_STATE, errs_s
-
-
 @pytest.mark.parametrize("name", ["prefill", "vector", "varlen", "laplace"])
-def test_full_size_workload_sampled(cuda_ok, name):
+def test_full_size_workload(cuda_ok, name):
+    """The whole output and final-state tensors of each full-size workload
+    against the oracle's token-by-token recurrence (in the launch
+    configuration the bench times).  The tolerance applies to the fp32 output
+    of the same call; the bf16 output is that result rounded once, and its own
+    error is printed beside it for the reader."""
+    gla = _gla()
     w = gla_inputs.WORKLOADS[name]
     x = gla_inputs.prefill_inputs(w)
-    out, fin = run_gpu(x)
-    B = fin.shape[0]
-    rng = np.random.default_rng(1)
-    pairs = {(0, 0), (B - 1, w.H - 1)}
-    while len(pairs) < 6:
-        pairs.add((int(rng.integers(B)), int(rng.integers(w.H))))
-    _sampled_check(x, out, fin, sorted(pairs))
+    args = (cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]))
+    kw = dict(scale=x["scale"], init_state=cuda(x["init_state"]),
+              cu_seqlens=cuda(x["cu_seqlens"]), chunk=x["chunk"])
+    out16, fin16 = gla.chunk_fwd(*args, **kw)
+    out32, fin = gla.chunk_fwd(*args, out_dtype=torch.float32, **kw)
+    gla.status_sync()
+    check_bf16_rounding(out16, out32)
+    assert torch.equal(fin16, fin)
+    o_ref, s_ref = run_ref(x)
+    e_o = rel_max(to_np(out32), o_ref)
+    e_o16 = rel_max(to_np(out16), o_ref)
+    e_s = rel_max(to_np(fin), s_ref)
+    print(f"{name}: output (fp32 result) {e_o:.3e}, output (bf16 tensor) {e_o16:.3e}, "
+          f"final state {e_s:.3e}")
+    assert e_o <= out_tol(torch.bfloat16), f"output error {e_o:.3e}"
+    assert e_s <= TOL_STATE, f"state error {e_s:.3e}"
