@@ -112,6 +112,10 @@ cudaError_t launch_epilogue(const EpilogueArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
+// the two-pass tensor-core prefill (state pass + output pass), per-head gate,
+// bf16 inputs: the forward's path for chunk 128
+bool chunk_split_supported(const ChunkArgs& a);
+cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_vec_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
 // the chunked backward, one launcher per (gate, I/O dtype)

@@ -256,11 +256,12 @@ def vector_arrival_counts():
     return n
 
 
-def run_schedule(nch, wide, seed, vector=False, **kw):
+def run_schedule(nch, wide, seed, vector=False, roles=None, need=None, **kw):
     """Returns None when every role finishes, else a description of the fault."""
     rnd = random.Random(seed)
-    roles = (vector_kernel_roles if vector else kernel_roles)(nch, wide, **kw)
-    need = vector_arrival_counts() if vector else arrival_counts()
+    if roles is None:
+        roles = (vector_kernel_roles if vector else kernel_roles)(nch, wide, **kw)
+        need = vector_arrival_counts() if vector else arrival_counts()
     pending, done = defaultdict(int), defaultdict(int)
     step = {n: next(g, None) for n, g in roles.items()}
     speed = {n: rnd.choice([0.02, 1.0, 1.0, 8.0]) for n in roles}
@@ -330,3 +331,198 @@ def test_single_p_barrier_is_caught():
     faults = [run_schedule(nch, WIDE_PATTERNS["none"], seed, single_p_barrier=True)
               for nch in range(2, 6) for seed in range(200)]
     assert any(f is not None and f.startswith("alias") and "PFull" in f for f in faults)
+
+
+# ---------------------------------------------------------------------------
+# The two-pass prefill (gla_chunk_split.cu): the state pass and the output pass.
+# ---------------------------------------------------------------------------
+ST_STAGES, ST_SLOTS, OUT_SLOTS = 3, 4, 4
+
+
+def state_pass_roles(nch):
+    """chunk_state_kernel: producer (gate sums, K / V loads), MMA (U = K^T W V),
+    four (W V) split warps, four scan warps (the state in registers; the scan
+    of chunk c also reads chunk c + 1's gate slot for the staged tile)."""
+    def producer():
+        for c in range(nch):
+            if c >= ST_SLOTS:
+                yield ("wait", ("GFree", c % ST_SLOTS), c // ST_SLOTS - 1)
+            yield ("arrive", ("GReady", c % ST_SLOTS))
+            if c >= ST_STAGES:
+                yield ("wait", ("KVEmpty", c % ST_STAGES), c // ST_STAGES - 1)
+            yield ("arrive", ("KVFull", c % ST_STAGES))
+
+    def mma():
+        for c in range(nch):
+            st = c % ST_STAGES
+            yield ("wait", ("KVFull", st), c // ST_STAGES)
+            yield ("wait", ("WVReady", st), c // ST_STAGES)
+            if c >= 2:
+                yield ("wait", ("UFree", c & 1), c // 2 - 1)
+            yield ("arrive", ("UFull", c & 1))
+            yield ("arrive", ("KVEmpty", st))
+
+    def split():
+        for c in range(nch):
+            yield ("wait", ("GReady", c % ST_SLOTS), c // ST_SLOTS)
+            yield ("wait", ("KVFull", c % ST_STAGES), c // ST_STAGES)
+            yield ("arrive", ("WVReady", c % ST_STAGES))
+            yield ("arrive", ("GFree", c % ST_SLOTS))
+
+    def scan():
+        for c in range(nch):
+            yield ("wait", ("GReady", c % ST_SLOTS), c // ST_SLOTS)
+            yield ("wait", ("UFull", c & 1), c >> 1)
+            yield ("arrive", ("UFree", c & 1))
+            if c + 1 < nch:
+                yield ("wait", ("GReady", (c + 1) % ST_SLOTS), (c + 1) // ST_SLOTS)
+            yield ("arrive", ("GFree", c % ST_SLOTS))
+
+    roles = {"producer": producer(), "mma": mma()}
+    for w in range(4):
+        roles[f"split{w}"] = split()
+        roles[f"scan{w}"] = scan()
+    need = {("UFree", 0): 4, ("UFree", 1): 4}
+    for i in range(ST_STAGES):
+        need[("WVReady", i)] = 4
+    for i in range(ST_SLOTS):
+        need[("GFree", i)] = 8
+    return roles, need
+
+
+def output_pass_roles(tiles):
+    """chunk_out_kernel over a list of tiles (c > 0, has_state, wide): producer
+    (gate sums, Q / K / staged-tile loads), MMA issuer (MMA1(k), MMA2(k - 1),
+    MMA3(k)), V loader, four P' warps, four output warps, four state-tile warps;
+    a final "done" slot ends every role."""
+    n = len(tiles)
+
+    def producer():
+        for k in range(n + 1):
+            if k >= OUT_SLOTS:
+                yield ("wait", ("GFree", k % OUT_SLOTS), k // OUT_SLOTS - 1)
+            yield ("arrive", ("GReady", k % OUT_SLOTS))
+            if k == n:
+                return
+            if k >= 2:
+                yield ("wait", ("QEmpty", k & 1), (k >> 1) - 1)
+            yield ("arrive", ("QFull", k & 1))
+            if k >= 1:
+                yield ("wait", ("KEmpty",), k - 1)
+            yield ("arrive", ("KFull",))
+            if tiles[k][0]:
+                if k >= 1:
+                    yield ("wait", ("SEmpty",), k - 1)
+                yield ("arrive", ("SRaw",))
+
+    def mma():
+        for k in range(n + 1):
+            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
+            yield ("arrive", ("GFree", k % OUT_SLOTS))
+            done = k == n
+            if not done:
+                yield ("wait", ("QFull", k & 1), k >> 1)
+                yield ("wait", ("KFull",), k)
+                if k >= 2:
+                    yield ("wait", ("AFree", k & 1), (k >> 1) - 1)
+                yield ("arrive", ("AFull", k & 1))
+                yield ("arrive", ("KEmpty",))
+            if k >= 1:
+                pb = (k - 1) & 1
+                yield ("wait", ("PFull", pb), (k - 1) >> 1)
+                yield ("wait", ("VFull",), k - 1)
+                yield ("arrive", ("OFull", pb))
+                yield ("arrive", ("VEmpty",))
+                yield ("arrive", ("AFree", pb))
+            if done:
+                return
+            yield ("wait", ("SFull",), k)
+            if k >= 2:
+                yield ("wait", ("OFree", k & 1), (k >> 1) - 1)
+            yield ("arrive", ("O3Full", k & 1))
+            yield ("arrive", ("SEmpty",))
+            yield ("arrive", ("QEmpty", k & 1))
+
+    def vload():
+        for k in range(n + 1):
+            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
+            if k < n:
+                if k >= 1:
+                    yield ("wait", ("VEmpty",), k - 1)
+                yield ("arrive", ("VFull",))
+            yield ("arrive", ("GFree", k % OUT_SLOTS))
+
+    def pbuild():
+        for k in range(n + 1):
+            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
+            if k == n:
+                yield ("arrive", ("GFree", k % OUT_SLOTS))
+                return
+            _, has_state, wide = tiles[k]
+            yield ("wait", ("AFull", k & 1), k >> 1)
+            if wide and has_state:
+                yield ("wait", ("O3Full", k & 1), k >> 1)
+            yield ("arrive", ("PFull", k & 1))
+            yield ("arrive", ("GFree", k % OUT_SLOTS))
+
+    def output():
+        for k in range(n + 1):
+            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
+            if k == n:
+                yield ("arrive", ("GFree", k % OUT_SLOTS))
+                return
+            yield ("wait", ("OFull", k & 1), k >> 1)
+            yield ("arrive", ("OFree", k & 1))
+            yield ("arrive", ("GFree", k % OUT_SLOTS))
+
+    def state_tile():
+        nraw = 0
+        for k in range(n + 1):
+            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
+            if k == n:
+                yield ("arrive", ("GFree", k % OUT_SLOTS))
+                return
+            staged, has_state, _ = tiles[k]
+            if staged:
+                yield ("wait", ("SRaw",), nraw)
+                nraw += 1
+            elif k >= 1:
+                yield ("wait", ("SEmpty",), k - 1)
+            yield ("arrive", ("SFull",))
+            yield ("arrive", ("GFree", k % OUT_SLOTS))
+
+    roles = {"producer": producer(), "mma": mma(), "vload": vload()}
+    for w in range(4):
+        roles[f"pbuild{w}"] = pbuild()
+        roles[f"output{w}"] = output()
+        roles[f"stile{w}"] = state_tile()
+    need = {("SFull",): 4, ("PFull", 0): 4, ("PFull", 1): 4, ("OFree", 0): 4, ("OFree", 1): 4}
+    for i in range(OUT_SLOTS):
+        need[("GFree", i)] = 14
+    return roles, need
+
+
+def test_state_pass_protocol():
+    for nch in range(0, 10):
+        for seed in range(150):
+            roles, need = state_pass_roles(nch)
+            fault = run_schedule(nch, None, seed, roles=roles, need=need)
+            assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
+
+
+@pytest.mark.parametrize("pattern", ["plain", "chunk0_first", "wide_mix", "no_state"])
+def test_output_pass_protocol(pattern):
+    # tiles as a CTA walks them: (staged tile, has a state, wide)
+    def tile(k):
+        if pattern == "plain":
+            return (True, True, False)
+        if pattern == "chunk0_first":
+            return (k % 5 != 0, True, k % 7 == 3)
+        if pattern == "wide_mix":
+            return (k % 3 != 0, True, k % 2 == 1)
+        return (k % 4 != 0, k % 4 != 0, k % 3 == 0)
+    for n in range(0, 11):
+        for seed in range(120):
+            roles, need = output_pass_roles([tile(k) for k in range(n)])
+            fault = run_schedule(n, None, seed, roles=roles, need=need)
+            assert fault is None, f"{n} tiles, seed {seed}: {fault}"
