@@ -95,7 +95,7 @@ const char* gla_chunk_fwd_kernel(int dk, int dv, int chunk, unsigned flags) {
   a.fp32_io = (flags & GLA_FLAG_FP32_IO) != 0;
   a.fp32_out = a.fp32_io || (flags & GLA_FLAG_FP32_OUT) != 0;
   a.vector_gate = (flags & GLA_FLAG_VECTOR_GATE) != 0;
-  return (gla::chunk_split_supported(a) || gla::chunk_tc_vec_supported(a)) ? "tensor_core"
+  return (gla::chunk_tc_supported(a) || gla::chunk_tc_vec_supported(a)) ? "tensor_core"
                                                                         : "cuda_core";
 }
 
@@ -191,8 +191,8 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
   // bf16 I/O with chunk 128 runs on the tensor cores whenever that kernel covers
   // the shape; if it cannot be launched the call fails (no quiet substitution).
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (rows > 0 && gla::chunk_split_supported(a))
-    err = gla::launch_chunk_split(a, s);
+  if (rows > 0 && gla::chunk_tc_supported(a))
+    err = gla::launch_chunk_tc(a, s);
   else if (rows > 0 && gla::chunk_tc_vec_supported(a))
     err = gla::launch_chunk_tc_vec(a, s);
   else
@@ -516,6 +516,7 @@ gla_status gla_status_sync(gla_stream_t stream) {
   if (word != 0 && (err = cudaMemset(p, 0, sizeof(unsigned))) != cudaSuccess)
     return cuda_status(err);
   if (word & gla::kDevTimeout) return GLA_ERR_TIMEOUT;
+  if (word & gla::kDevLayout) return GLA_ERR_UNSUPPORTED;
   if (word & gla::kDevBadSeqlens) return GLA_ERR_INVALID_ARG;
   return GLA_OK;
 }

@@ -11,6 +11,7 @@ namespace gla {
 enum : unsigned {
   kDevBadSeqlens = 1u << 0,  // a cu_seqlens entry was out of order or out of range
   kDevTimeout = 1u << 1,     // a bounded mbarrier wait gave up
+  kDevLayout = 1u << 2,      // a kernel's shared-memory window was not 1024-byte aligned
   // (kDevBadSeqlens also flags a decode slot index outside the state pool)
 };
 
@@ -112,10 +113,6 @@ cudaError_t launch_epilogue(const EpilogueArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
-// the two-pass tensor-core prefill (state pass + output pass), per-head gate,
-// bf16 inputs: the forward's path for chunk 128
-bool chunk_split_supported(const ChunkArgs& a);
-cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_vec_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
 // the chunked backward, one launcher per (gate, I/O dtype)

@@ -374,7 +374,9 @@ const char *gla_status_string(gla_status status);
  * gla_status_sync -- wait for `stream`, then read and clear the current GPU's
  * device status word.  Returns GLA_ERR_CUDA if the stream reports a CUDA error,
  * otherwise the most severe device-side status seen since the last call
- * (GLA_ERR_TIMEOUT over GLA_ERR_INVALID_ARG over GLA_OK).
+ * (GLA_ERR_TIMEOUT over GLA_ERR_UNSUPPORTED over GLA_ERR_INVALID_ARG over
+ * GLA_OK).  GLA_ERR_UNSUPPORTED here means a tensor-core kernel found its
+ * shared-memory window not 1024-byte aligned and wrote nothing.
  */
 gla_status gla_status_sync(gla_stream_t stream);
 

@@ -33,8 +33,9 @@ GATE_WARPS = 8     # per-key-channel kernel
 
 def kernel_roles(nch, wide, single_p_barrier=False):
     """Generators of ("wait", barrier, phase) / ("arrive", barrier) /
-    ("bar_sync",) steps, one per warp role (warps of a group are separate
-    roles: each arrives once per barrier phase)."""
+    ("bar_sync",) steps, one per warp role of the per-head kernel (warps of a
+    group are separate roles: each arrives once per barrier phase).  The MMA
+    issuers: A (MMA1), B (MMA3 then MMA2), C (MMA4 into the chunk's own U)."""
     K = SLOTS
     pfull = (lambda c: ("PFull",)) if single_p_barrier else (lambda c: ("PFull", c & 1))
     pphase = (lambda c: c) if single_p_barrier else (lambda c: c >> 1)
@@ -47,11 +48,11 @@ def kernel_roles(nch, wide, single_p_barrier=False):
             if c >= 2:
                 yield ("wait", ("QKEmpty", c & 1), (c >> 1) - 1)
             yield ("arrive", ("QKFull", c & 1))  # the TMA transaction completes it
-            if c >= 1:
-                yield ("wait", ("VEmpty",), c - 1)
-            yield ("arrive", ("VFull",))
+            if c >= 2:
+                yield ("wait", ("VEmpty", c & 1), (c >> 1) - 1)
+            yield ("arrive", ("VFull", c & 1))
 
-    def mma1():  # warp 1
+    def issuer_a():  # warp 1: MMA1
         for c in range(nch):
             st = c & 1
             yield ("wait", ("QKFull", st), c >> 1)
@@ -60,30 +61,31 @@ def kernel_roles(nch, wide, single_p_barrier=False):
             yield ("arrive", ("AFull", st))
             yield ("arrive", ("QKEmpty", st))
 
-    def mma2():  # warp 2
-        for c in range(nch):
-            st = c & 1
-            yield ("wait", pfull(c), pphase(c))
-            yield ("wait", ("O3Full", st), c >> 1)
-            yield ("wait", ("VtFull", st), c >> 1)
-            yield ("arrive", ("GFree", c % K))
-            yield ("arrive", ("OFull", st))
-            yield ("arrive", ("AFree", st))
-            yield ("arrive", ("VtFree", st))
-            if wide(c):
-                yield ("arrive", ("VEmpty",))
-
-    def mma34():  # warp 3: MMA3 then MMA4 of each chunk
+    def issuer_b():  # warp 2: MMA3, then MMA2
         for c in range(nch):
             st = c & 1
             yield ("wait", ("QKFull", st), c >> 1)
-            yield ("wait", ("VtFull", st), c >> 1)
             yield ("wait", ("SReady",), c)
             if c >= 2:
                 yield ("wait", ("OFree", st), (c >> 1) - 1)
-            yield ("wait", ("GReady", c % K), c // K)
             yield ("arrive", ("O3Full", st))
-            yield ("arrive", ("SFull",))
+            yield ("arrive", ("SFree",))
+            yield ("arrive", ("QKEmpty", st))
+            yield ("wait", pfull(c), pphase(c))
+            yield ("wait", ("VFull", st), c >> 1)
+            yield ("arrive", ("OFull", st))
+            yield ("arrive", ("AFree", st))
+            yield ("arrive", ("VEmpty", st))
+
+    def issuer_c():  # warp 3: MMA4 into U of the chunk's parity
+        for c in range(nch):
+            st = c & 1
+            yield ("wait", ("QKFull", st), c >> 1)
+            yield ("wait", ("VtFull",), c)
+            if c >= 2:
+                yield ("wait", ("UFree", st), (c >> 1) - 1)
+            yield ("arrive", ("UFull", st))
+            yield ("arrive", ("VtFree",))
             yield ("arrive", ("QKEmpty", st))
 
     def mask():  # warps 4..7: P' of chunk c, then the output of chunk c - 1
@@ -92,52 +94,53 @@ def kernel_roles(nch, wide, single_p_barrier=False):
                 st = c & 1
                 yield ("wait", ("GReady", c % K), c // K)
                 yield ("wait", ("AFull", st), c >> 1)
+                yield ("arrive", ("GFree", c % K))
                 if wide(c):
                     yield ("wait", ("O3Full", st), c >> 1)
                 yield ("arrive", pfull(c))
-                yield ("arrive", ("GFree", c % K))
             if c >= 1:
                 d = c - 1
                 yield ("wait", ("OFull", d & 1), d >> 1)
                 yield ("arrive", ("OFree", d & 1))
 
-    def state(first):  # warps 8..15: W V split of chunk c + 1, then the pass over S_c
-        def split(c):
-            yield ("wait", ("GReady", c % K), c // K)
-            yield ("arrive", ("GFree", c % K))
-            if c >= 2:
-                yield ("wait", ("VtFree", c & 1), (c >> 1) - 1)
-            yield ("wait", ("VFull",), c)
-            if not wide(c):
-                yield ("bar_sync",)
-                if first:
-                    yield ("arrive", ("VEmpty",))
-            yield ("arrive", ("VtFull", c & 1))
-
+    def state():  # warps 8..15: split of chunk c + 1, state step c, S'_c
         for c in range(-1, nch):
-            last = c + 1 == nch
-            if not last:
-                yield from split(c + 1)
+            n = c + 1
+            if n < nch:
+                yield ("wait", ("GReady", n % K), n // K)
+                yield ("wait", ("VFull", n & 1), n >> 1)
+                if n >= 1:
+                    yield ("wait", ("VtFree",), n - 1)
+                yield ("arrive", ("VtFull",))
+                yield ("arrive", ("VEmpty", n & 1))
             if c >= 0:
-                yield ("wait", ("SFull",), c)
-            if not last:
+                yield ("wait", ("UFull", c & 1), c >> 1)
+                yield ("arrive", ("UFree", c & 1))
+            if n < nch:
+                if c >= 0:
+                    yield ("wait", ("SFree",), c)
                 yield ("arrive", ("SReady",))
+            if c >= 0:
+                yield ("arrive", ("GFree", c % K))
 
-    roles = {"producer": producer(), "mma1": mma1(), "mma2": mma2(), "mma34": mma34()}
+    roles = {"producer": producer(), "issuer_a": issuer_a(), "issuer_b": issuer_b(),
+             "issuer_c": issuer_c()}
     for w in range(MASK_WARPS):
         roles[f"mask{w}"] = mask()
     for w in range(STATE_WARPS):
-        roles[f"state{w}"] = state(w == 0)
+        roles[f"state{w}"] = state()
     return roles
 
 
 def arrival_counts():
     """Arrivals per phase of the per-head kernel's barriers (default 1)."""
-    n = {("QKEmpty", 0): 2, ("QKEmpty", 1): 2, ("PFull",): MASK_WARPS, ("PFull", 0): MASK_WARPS,
+    n = {("QKEmpty", 0): 3, ("QKEmpty", 1): 3, ("PFull",): MASK_WARPS, ("PFull", 0): MASK_WARPS,
          ("PFull", 1): MASK_WARPS, ("OFree", 0): MASK_WARPS, ("OFree", 1): MASK_WARPS,
-         ("VtFull", 0): STATE_WARPS, ("VtFull", 1): STATE_WARPS, ("SReady",): STATE_WARPS}
+         ("VEmpty", 0): 1 + STATE_WARPS, ("VEmpty", 1): 1 + STATE_WARPS,
+         ("UFree", 0): STATE_WARPS, ("UFree", 1): STATE_WARPS, ("VtFull",): STATE_WARPS,
+         ("SReady",): STATE_WARPS}
     for i in range(SLOTS):
-        n[("GFree", i)] = MASK_WARPS + STATE_WARPS + 1
+        n[("GFree", i)] = MASK_WARPS + STATE_WARPS
     return n
 
 
@@ -331,198 +334,3 @@ def test_single_p_barrier_is_caught():
     faults = [run_schedule(nch, WIDE_PATTERNS["none"], seed, single_p_barrier=True)
               for nch in range(2, 6) for seed in range(200)]
     assert any(f is not None and f.startswith("alias") and "PFull" in f for f in faults)
-
-
-# ---------------------------------------------------------------------------
-# The two-pass prefill (gla_chunk_split.cu): the state pass and the output pass.
-# ---------------------------------------------------------------------------
-ST_STAGES, ST_SLOTS, OUT_SLOTS = 3, 4, 4
-
-
-def state_pass_roles(nch):
-    """chunk_state_kernel: producer (gate sums, K / V loads), MMA (U = K^T W V),
-    four (W V) split warps, four scan warps (the state in registers; the scan
-    of chunk c also reads chunk c + 1's gate slot for the staged tile)."""
-    def producer():
-        for c in range(nch):
-            if c >= ST_SLOTS:
-                yield ("wait", ("GFree", c % ST_SLOTS), c // ST_SLOTS - 1)
-            yield ("arrive", ("GReady", c % ST_SLOTS))
-            if c >= ST_STAGES:
-                yield ("wait", ("KVEmpty", c % ST_STAGES), c // ST_STAGES - 1)
-            yield ("arrive", ("KVFull", c % ST_STAGES))
-
-    def mma():
-        for c in range(nch):
-            st = c % ST_STAGES
-            yield ("wait", ("KVFull", st), c // ST_STAGES)
-            yield ("wait", ("WVReady", st), c // ST_STAGES)
-            if c >= 2:
-                yield ("wait", ("UFree", c & 1), c // 2 - 1)
-            yield ("arrive", ("UFull", c & 1))
-            yield ("arrive", ("KVEmpty", st))
-
-    def split():
-        for c in range(nch):
-            yield ("wait", ("GReady", c % ST_SLOTS), c // ST_SLOTS)
-            yield ("wait", ("KVFull", c % ST_STAGES), c // ST_STAGES)
-            yield ("arrive", ("WVReady", c % ST_STAGES))
-            yield ("arrive", ("GFree", c % ST_SLOTS))
-
-    def scan():
-        for c in range(nch):
-            yield ("wait", ("GReady", c % ST_SLOTS), c // ST_SLOTS)
-            yield ("wait", ("UFull", c & 1), c >> 1)
-            yield ("arrive", ("UFree", c & 1))
-            if c + 1 < nch:
-                yield ("wait", ("GReady", (c + 1) % ST_SLOTS), (c + 1) // ST_SLOTS)
-            yield ("arrive", ("GFree", c % ST_SLOTS))
-
-    roles = {"producer": producer(), "mma": mma()}
-    for w in range(4):
-        roles[f"split{w}"] = split()
-        roles[f"scan{w}"] = scan()
-    need = {("UFree", 0): 4, ("UFree", 1): 4}
-    for i in range(ST_STAGES):
-        need[("WVReady", i)] = 4
-    for i in range(ST_SLOTS):
-        need[("GFree", i)] = 8
-    return roles, need
-
-
-def output_pass_roles(tiles):
-    """chunk_out_kernel over a list of tiles (c > 0, has_state, wide): producer
-    (gate sums, Q / K / staged-tile loads), MMA issuer (MMA1(k), MMA2(k - 1),
-    MMA3(k)), V loader, four P' warps, four output warps, four state-tile warps;
-    a final "done" slot ends every role."""
-    n = len(tiles)
-
-    def producer():
-        for k in range(n + 1):
-            if k >= OUT_SLOTS:
-                yield ("wait", ("GFree", k % OUT_SLOTS), k // OUT_SLOTS - 1)
-            yield ("arrive", ("GReady", k % OUT_SLOTS))
-            if k == n:
-                return
-            if k >= 2:
-                yield ("wait", ("QEmpty", k & 1), (k >> 1) - 1)
-            yield ("arrive", ("QFull", k & 1))
-            if k >= 1:
-                yield ("wait", ("KEmpty",), k - 1)
-            yield ("arrive", ("KFull",))
-            if tiles[k][0]:
-                if k >= 1:
-                    yield ("wait", ("SEmpty",), k - 1)
-                yield ("arrive", ("SRaw",))
-
-    def mma():
-        for k in range(n + 1):
-            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
-            yield ("arrive", ("GFree", k % OUT_SLOTS))
-            done = k == n
-            if not done:
-                yield ("wait", ("QFull", k & 1), k >> 1)
-                yield ("wait", ("KFull",), k)
-                if k >= 2:
-                    yield ("wait", ("AFree", k & 1), (k >> 1) - 1)
-                yield ("arrive", ("AFull", k & 1))
-                yield ("arrive", ("KEmpty",))
-            if k >= 1:
-                pb = (k - 1) & 1
-                yield ("wait", ("PFull", pb), (k - 1) >> 1)
-                yield ("wait", ("VFull",), k - 1)
-                yield ("arrive", ("OFull", pb))
-                yield ("arrive", ("VEmpty",))
-                yield ("arrive", ("AFree", pb))
-            if done:
-                return
-            yield ("wait", ("SFull",), k)
-            if k >= 2:
-                yield ("wait", ("OFree", k & 1), (k >> 1) - 1)
-            yield ("arrive", ("O3Full", k & 1))
-            yield ("arrive", ("SEmpty",))
-            yield ("arrive", ("QEmpty", k & 1))
-
-    def vload():
-        for k in range(n + 1):
-            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
-            if k < n:
-                if k >= 1:
-                    yield ("wait", ("VEmpty",), k - 1)
-                yield ("arrive", ("VFull",))
-            yield ("arrive", ("GFree", k % OUT_SLOTS))
-
-    def pbuild():
-        for k in range(n + 1):
-            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
-            if k == n:
-                yield ("arrive", ("GFree", k % OUT_SLOTS))
-                return
-            _, has_state, wide = tiles[k]
-            yield ("wait", ("AFull", k & 1), k >> 1)
-            if wide and has_state:
-                yield ("wait", ("O3Full", k & 1), k >> 1)
-            yield ("arrive", ("PFull", k & 1))
-            yield ("arrive", ("GFree", k % OUT_SLOTS))
-
-    def output():
-        for k in range(n + 1):
-            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
-            if k == n:
-                yield ("arrive", ("GFree", k % OUT_SLOTS))
-                return
-            yield ("wait", ("OFull", k & 1), k >> 1)
-            yield ("arrive", ("OFree", k & 1))
-            yield ("arrive", ("GFree", k % OUT_SLOTS))
-
-    def state_tile():
-        nraw = 0
-        for k in range(n + 1):
-            yield ("wait", ("GReady", k % OUT_SLOTS), k // OUT_SLOTS)
-            if k == n:
-                yield ("arrive", ("GFree", k % OUT_SLOTS))
-                return
-            staged, has_state, _ = tiles[k]
-            if staged:
-                yield ("wait", ("SRaw",), nraw)
-                nraw += 1
-            elif k >= 1:
-                yield ("wait", ("SEmpty",), k - 1)
-            yield ("arrive", ("SFull",))
-            yield ("arrive", ("GFree", k % OUT_SLOTS))
-
-    roles = {"producer": producer(), "mma": mma(), "vload": vload()}
-    for w in range(4):
-        roles[f"pbuild{w}"] = pbuild()
-        roles[f"output{w}"] = output()
-        roles[f"stile{w}"] = state_tile()
-    need = {("SFull",): 4, ("PFull", 0): 4, ("PFull", 1): 4, ("OFree", 0): 4, ("OFree", 1): 4}
-    for i in range(OUT_SLOTS):
-        need[("GFree", i)] = 14
-    return roles, need
-
-
-def test_state_pass_protocol():
-    for nch in range(0, 10):
-        for seed in range(150):
-            roles, need = state_pass_roles(nch)
-            fault = run_schedule(nch, None, seed, roles=roles, need=need)
-            assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
-
-
-@pytest.mark.parametrize("pattern", ["plain", "chunk0_first", "wide_mix", "no_state"])
-def test_output_pass_protocol(pattern):
-    # tiles as a CTA walks them: (staged tile, has a state, wide)
-    def tile(k):
-        if pattern == "plain":
-            return (True, True, False)
-        if pattern == "chunk0_first":
-            return (k % 5 != 0, True, k % 7 == 3)
-        if pattern == "wide_mix":
-            return (k % 3 != 0, True, k % 2 == 1)
-        return (k % 4 != 0, k % 4 != 0, k % 3 == 0)
-    for n in range(0, 11):
-        for seed in range(120):
-            roles, need = output_pass_roles([tile(k) for k in range(n)])
-            fault = run_schedule(n, None, seed, roles=roles, need=need)
-            assert fault is None, f"{n} tiles, seed {seed}: {fault}"
