@@ -278,7 +278,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);  // warp-uniform
   const uint32_t sbase = smem_u32(smem);
   if (tid == 0) GLA_TRACE_POINT(0, 30, 0);
 
@@ -384,38 +384,40 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------- issuer A: MMA1 A = Q K^T
-    if (lane == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (!wait(kQKFull0 + st, ph(c >> 1))) break;
-        if (c >= 2 && !wait(kAFree0 + st, ph((c >> 1) - 1))) break;
-        tc_fence_after();
-        GLA_TRACE_POINT(0, 3, c);
-        const uint32_t q_s = sbase + kOffQK + st * kQKStage;
-        const uint64_t qd = sdesc_sw128(q_s, 16, 1024), kd = sdesc_sw128(q_s + kQBytes, 16, 1024);
+    // (the whole warp waits and forms the descriptors; one lane issues)
+    for (int c = 0; c < nch; ++c) {
+      const int st = c & 1;
+      if (!wait_w(kQKFull0 + st, ph(c >> 1))) break;
+      if (c >= 2 && !wait_w(kAFree0 + st, ph((c >> 1) - 1))) break;
+      tc_fence_after();
+      GLA_TRACE_POINT(0, 3, c);
+      const uint32_t q_s = sbase + kOffQK + st * kQKStage;
+      const uint64_t qd = sdesc_sw128(q_s, 16, 1024), kd = sdesc_sw128(q_s + kQBytes, 16, 1024);
+      if (elect_one_sync()) {
         for (int kk = 0; kk < nks; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
           mma_bf16(tmem + kColA + st * 128, desc_add(qd, off), desc_add(kd, off), kIdQK, kk > 0);
         }
         mma_commit(&bars[kAFull0 + st]);
         mma_commit(&bars[kQKEmpty0 + st]);
-        mma_issued = true;
       }
+      __syncwarp();
+      mma_issued = true;
     }
   } else if (warp == 2) {
     // ---------------------- issuer B: MMA3 O = Q S', then MMA2 O += P' V
-    if (lane == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (!wait(kQKFull0 + st, ph(c >> 1))) break;
-        if (!wait(kSReady, ph(c))) break;  // S'_{c-1} hi / lo in shared memory
-        if (c >= 2 && !wait(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
-        tc_fence_after();
-        GLA_TRACE_POINT(0, 4, c);
-        const uint32_t q_s = sbase + kOffQK + st * kQKStage;
-        const uint64_t qd = sdesc_sw128(q_s, 16, 1024);
-        const uint64_t hd = sdesc_sw128(sbase + kOffShi, kPanel, 1024);
-        const uint64_t ld = sdesc_sw128(sbase + kOffSlo, kPanel, 1024);
+    for (int c = 0; c < nch; ++c) {
+      const int st = c & 1;
+      if (!wait_w(kQKFull0 + st, ph(c >> 1))) break;
+      if (!wait_w(kSReady, ph(c))) break;  // S'_{c-1} hi / lo in shared memory
+      if (c >= 2 && !wait_w(kOFree0 + st, ph((c >> 1) - 1))) break;  // output(c-2) read O
+      tc_fence_after();
+      GLA_TRACE_POINT(0, 4, c);
+      const uint32_t q_s = sbase + kOffQK + st * kQKStage;
+      const uint64_t qd = sdesc_sw128(q_s, 16, 1024);
+      const uint64_t hd = sdesc_sw128(sbase + kOffShi, kPanel, 1024);
+      const uint64_t ld = sdesc_sw128(sbase + kOffSlo, kPanel, 1024);
+      if (elect_one_sync()) {
         for (int kk = 0; kk < nks; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
           mma_bf16(tmem + kColO + st * kDVS, desc_add(qd, off), desc_add(hd, kk * 2048), kIdQS,
@@ -429,13 +431,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_commit(&bars[kO3Full0 + st]);
         mma_commit(&bars[kSFree]);
         mma_commit(&bars[kQKEmpty0 + st]);
-        mma_issued = true;
-        // MMA2: P' (A operand in TMEM: hi / lo pairs in place) times the raw V
-        if (!wait(kPFull0 + st, ph(c >> 1))) break;
-        if (!wait(kVFull0 + st, ph(c >> 1))) break;
-        tc_fence_after();
-        const uint32_t a_p = tmem + kColA + st * 128;
-        const uint64_t vd = sdesc_sw128(sbase + kOffV + st * kTile, kPanel, 1024);
+      }
+      __syncwarp();
+      mma_issued = true;
+      // MMA2: P' (A operand in TMEM: hi / lo pairs in place) times the raw V
+      if (!wait_w(kPFull0 + st, ph(c >> 1))) break;
+      if (!wait_w(kVFull0 + st, ph(c >> 1))) break;
+      tc_fence_after();
+      GLA_TRACE_POINT(0, 5, c);
+      const uint32_t a_p = tmem + kColA + st * 128;
+      const uint64_t vd = sdesc_sw128(sbase + kOffV + st * kTile, kPanel, 1024);
+      if (elect_one_sync()) {
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
@@ -446,21 +452,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_commit(&bars[kAFree0 + st]);
         mma_commit(&bars[kVEmpty0 + st]);
       }
+      __syncwarp();
     }
   } else if (warp == 3) {
     // -------------------------------------- issuer C: MMA4 U = K^T (W V)
-    if (lane == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (!wait(kQKFull0 + st, ph(c >> 1))) break;
-        if (!wait(kVtFull, ph(c))) break;  // (W V) hi / lo of chunk c
-        if (c >= 2 && !wait(kUFree0 + st, ph((c >> 1) - 1))) break;
-        tc_fence_after();
-        GLA_TRACE_POINT(0, 6, c);
-        const uint32_t k_s = sbase + kOffQK + st * kQKStage + kQBytes;
-        const uint64_t kd = sdesc_sw128(k_s, kPanel, 1024);
-        const uint64_t hd = sdesc_sw128(sbase + kOffWVhi, kPanel, 1024);
-        const uint64_t ld = sdesc_sw128(sbase + kOffWVlo, kPanel, 1024);
+    for (int c = 0; c < nch; ++c) {
+      const int st = c & 1;
+      if (!wait_w(kQKFull0 + st, ph(c >> 1))) break;
+      if (!wait_w(kVtFull, ph(c))) break;  // (W V) hi / lo of chunk c
+      if (c >= 2 && !wait_w(kUFree0 + st, ph((c >> 1) - 1))) break;
+      tc_fence_after();
+      GLA_TRACE_POINT(0, 6, c);
+      const uint32_t k_s = sbase + kOffQK + st * kQKStage + kQBytes;
+      const uint64_t kd = sdesc_sw128(k_s, kPanel, 1024);
+      const uint64_t hd = sdesc_sw128(sbase + kOffWVhi, kPanel, 1024);
+      const uint64_t ld = sdesc_sw128(sbase + kOffWVlo, kPanel, 1024);
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(tmem + kColU + st * kDVS, desc_add(kd, kk * 2048), desc_add(hd, kk * 2048),
@@ -472,8 +479,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_commit(&bars[kUFull0 + st]);
         mma_commit(&bars[kVtFree]);
         mma_commit(&bars[kQKEmpty0 + st]);
-        mma_issued = true;
       }
+      __syncwarp();
+      mma_issued = true;
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ mask group
@@ -766,8 +774,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         drain_bar(&bars[kVFull0 + st], issued_v[st]);
       }
     }
-    if (warp >= 1 && warp <= 3 && lane == 0 && mma_issued) {
-      mma_commit(&bars[kDrain + warp - 1]);
+    if (warp >= 1 && warp <= 3 && mma_issued) {
+      // the lane that issued this warp's MMAs commits them to the drain barrier
+      if (elect_one_sync()) mma_commit(&bars[kDrain + warp - 1]);
+      __syncwarp();
       (void)mbar_wait_bounded(&bars[kDrain + warp - 1], 0u, kWaitLimitNs);
     }
   }
