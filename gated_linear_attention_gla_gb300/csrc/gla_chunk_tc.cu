@@ -32,8 +32,9 @@
 // Each issuer waits only for its own operands.
 //
 // Roles (16 warps):
-//   warp 0       producer: prefix sums of g and the chunk's flags (all lanes),
-//                the TMA loads of a 2-stage Q/K ring and a 2-buffer V ring
+//   warp 0       producer: the TMA loads of a 2-stage Q/K ring and a 2-buffer
+//                V ring (lane 0; the first two chunks' before anything else),
+//                prefix sums of g and the chunk's flags (all lanes)
 //   warp 1       issuer A (MMA1), TMEM allocation
 //   warp 2       issuer B (MMA3, then MMA2)
 //   warp 3       issuer C (MMA4)
@@ -186,40 +187,52 @@ __device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float G2r
   tmem_ld_32x32b_x32(a_row, a);
 #pragma unroll 1
   for (int cb = 0; cb < 4; ++cb) {
-    uint32_t hi[16], lo[16];
     if (cb <= q4) {
       tmem_ld_wait_x32(a);
       const bool diag = cb == q4;
       const float4* w4 = reinterpret_cast<const float4*>(arr + 32 * cb);
+      // half h: columns 16 h .. 16 h + 15 of the block -> hi pairs at 8 h, lo
+      // pairs at 16 + 8 h (columns whose A values are already in registers);
+      // then the next block's same half is loaded into the freed registers
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 wv = w4[e4];
-        const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
-        float x[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 32 * cb + 4 * e4 + i;
-          const float av = __uint_as_float(a[4 * e4 + i]);
-          if constexpr (WIDE) {
-            x[i] = j <= r ? av * exp2f(G2r - wa[i]) : 0.f;
-          } else {
-            x[i] = (diag && j > r) ? 0.f : av * wa[i];
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int e = 16 * hf + 4 * e4;
+          const float4 wv = w4[4 * hf + e4];
+          const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+          float x[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = 32 * cb + e + i;
+            const float av = __uint_as_float(a[e + i]);
+            if constexpr (WIDE) {
+              x[i] = j <= r ? av * exp2f(G2r - wa[i]) : 0.f;
+            } else {
+              x[i] = (diag && j > r) ? 0.f : av * wa[i];
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t h2 = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+            hi[2 * e4 + i] = h2;
+            lo[2 * e4 + i] = pack_bf16x2(x[2 * i] - bf16lo(h2), x[2 * i + 1] - bf16hi(h2));
           }
         }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t h2 = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-          hi[2 * e4 + i] = h2;
-          lo[2 * e4 + i] = pack_bf16x2(x[2 * i] - bf16lo(h2), x[2 * i + 1] - bf16hi(h2));
-        }
+        if (cb < q4)
+          tmem_ld_32x32b_x16(a_row + 32 * (cb + 1) + 16 * hf,
+                             *reinterpret_cast<uint32_t(*)[16]>(a + 16 * hf));
+        tmem_st_32x32b_x8(a_row + 32 * cb + 8 * hf, hi);
+        tmem_st_32x32b_x8(a_row + 32 * cb + 16 + 8 * hf, lo);
       }
-      if (cb < q4) tmem_ld_32x32b_x32(a_row + 32 * (cb + 1), a);
     } else {
+      uint32_t z[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      tmem_st_32x32b_x16(a_row + 32 * cb, z);
+      tmem_st_32x32b_x16(a_row + 32 * cb + 16, z);
     }
-    tmem_st_32x32b_x16(a_row + 32 * cb, hi);
-    tmem_st_32x32b_x16(a_row + 32 * cb + 16, lo);
   }
 }
 
@@ -313,6 +326,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (c < nch && t < len) prefetch_l2(p.g + (start + t) * p.H + h);
       }
     };
+    // lane 0: the TMA loads of chunk c (after its ring stages are free)
+    auto issue_loads = [&](int c) -> bool {
+      const int st = c & 1;
+      const int row = packed ? (int)(start + (long long)c * kC) : c * kC;
+      if (c >= 2 && !wait(kQKEmpty0 + st, ph((c >> 1) - 1))) return false;
+      uint8_t* q_s = smem + kOffQK + st * kQKStage;
+      uint8_t* k_s = q_s + kQBytes;
+      mbar_arrive_expect_tx(&bars[kQKFull0 + st], kQKStage);
+#pragma unroll
+      for (int pn = 0; pn < kDK / 64; ++pn) {
+        tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
+        tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
+      }
+      ++issued_qk[st];
+      GLA_TRACE_POINT(0, 1, c);
+      if (c >= 2 && !wait(kVEmpty0 + st, ph((c >> 1) - 1))) return false;
+      mbar_arrive_expect_tx(&bars[kVFull0 + st], kTile);
+      tma_load_4d(smem + kOffV + st * kTile, &tmV, &bars[kVFull0 + st], sl * kDVS, h, row, bidx);
+      ++issued_v[st];
+      GLA_TRACE_POINT(0, 2, c);
+      return true;
+    };
+    // the first two chunks' tiles need no free stage: start them before the gates
+    if (lane == 0)
+      for (int c = 0; c < 2 && c < nch; ++c) (void)issue_loads(c);
     for (int c = 0; c < 3; ++c) prefetch_gates(c);
     for (int c = 0; c < nch; ++c) {
       float gv[4];
@@ -355,30 +393,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       warp_arrive(kGReady0 + c % kSlots);
       if (lane == 0) {
-        const int st = c & 1;
         GLA_TRACE_POINT(0, 0, c);
-        const int row = packed ? (int)(start + (long long)c * kC) : c * kC;
-        if (c >= 2 && !wait(kQKEmpty0 + st, ph((c >> 1) - 1))) ok = false;
-        if (ok) {
-          uint8_t* q_s = smem + kOffQK + st * kQKStage;
-          uint8_t* k_s = q_s + kQBytes;
-          mbar_arrive_expect_tx(&bars[kQKFull0 + st], kQKStage);
-#pragma unroll
-          for (int pn = 0; pn < kDK / 64; ++pn) {
-            tma_load_4d(q_s + pn * kPanel, &tmQ, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
-            tma_load_4d(k_s + pn * kPanel, &tmK, &bars[kQKFull0 + st], pn * 64, h, row, bidx);
-          }
-          ++issued_qk[st];
-          GLA_TRACE_POINT(0, 1, c);
-        }
-        if (ok && c >= 2 && !wait(kVEmpty0 + st, ph((c >> 1) - 1))) ok = false;
-        if (ok) {
-          mbar_arrive_expect_tx(&bars[kVFull0 + st], kTile);
-          tma_load_4d(smem + kOffV + st * kTile, &tmV, &bars[kVFull0 + st], sl * kDVS, h, row,
-                      bidx);
-          ++issued_v[st];
-          GLA_TRACE_POINT(0, 2, c);
-        }
+        if (c >= 2) ok = issue_loads(c);
       }
       if (__any_sync(0xffffffffu, !ok)) break;
     }

@@ -40,17 +40,19 @@ def kernel_roles(nch, wide, single_p_barrier=False):
     pfull = (lambda c: ("PFull",)) if single_p_barrier else (lambda c: ("PFull", c & 1))
     pphase = (lambda c: c) if single_p_barrier else (lambda c: c >> 1)
 
-    def producer():  # warp 0: gate sums (all lanes), then TMA (lane 0)
+    def producer():  # warp 0: TMA of chunks 0, 1 first; then per chunk gate sums, TMA (c >= 2)
+        for c in range(min(2, nch)):
+            yield ("arrive", ("QKFull", c & 1))  # the TMA transaction completes it
+            yield ("arrive", ("VFull", c & 1))
         for c in range(nch):
             if c >= K:
                 yield ("wait", ("GFree", c % K), c // K - 1)
             yield ("arrive", ("GReady", c % K))
             if c >= 2:
                 yield ("wait", ("QKEmpty", c & 1), (c >> 1) - 1)
-            yield ("arrive", ("QKFull", c & 1))  # the TMA transaction completes it
-            if c >= 2:
+                yield ("arrive", ("QKFull", c & 1))
                 yield ("wait", ("VEmpty", c & 1), (c >> 1) - 1)
-            yield ("arrive", ("VFull", c & 1))
+                yield ("arrive", ("VFull", c & 1))
 
     def issuer_a():  # warp 1: MMA1
         for c in range(nch):
