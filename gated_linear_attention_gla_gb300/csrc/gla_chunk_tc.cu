@@ -534,7 +534,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int part = 0; part < 4; ++part) {
           uint32_t v[16];
           tmem_ld_32x32b_x16(tmem + lane_off + kColO + b * kDVS + 16 * part, v);
-          tmem_ld_wait();
+          tmem_ld_wait_x16(v);
           if (part == 3) {
             tc_fence_before();
             warp_arrive(kOFree0 + b);
@@ -646,7 +646,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           for (int part = 0; part < 4; ++part) {
             uint32_t v[16];
             tmem_ld_32x32b_x16(o_row + 16 * part, v);
-            tmem_ld_wait();
+            tmem_ld_wait_x16(v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(e * __uint_as_float(v[j]));
             tmem_st_32x32b_x16(o_row + 16 * part, v);

@@ -357,7 +357,7 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
       for (int part = 0; part < kD / 16; ++part) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(tmem + lane_off + kColO + ob * kD + 16 * part, v);
-        tmem_ld_wait();
+        tmem_ld_wait_x16(v);
         if (part == kD / 16 - 1) {
           tc_fence_before();
           warp_arrive(kOFree0 + ob);
@@ -462,7 +462,7 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         for (int q = 0; q < 4; ++q) {
           uint32_t v[16];
           tmem_ld_32x32b_x16(tmem + lane_off + kColS + 64 * hf + 16 * q, v);
-          tmem_ld_wait();
+          tmem_ld_wait_x16(v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) sv[16 * q + j] = __uint_as_float(v[j]);
         }
