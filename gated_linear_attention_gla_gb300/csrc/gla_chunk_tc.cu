@@ -149,10 +149,10 @@ __device__ __forceinline__ uint32_t ph(int k) { return static_cast<uint32_t>(k) 
 __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity,
                                            volatile int* abort_flag, unsigned* status) {
   if (*abort_flag) return false;
-  if (mbar_try_wait(bar, parity, 20000u)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -163,7 +163,7 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity,
 }
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
                                          volatile int* abort_flag, unsigned* status) {
-  if (!*abort_flag && mbar_try_wait(bar, parity, 20000u)) return true;
+  if (!*abort_flag && mbar_try_wait(bar, parity)) return true;
   return wait_bar_slow(bar, parity, abort_flag, status);
 }
 

@@ -36,17 +36,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 // Test for completion of the phase with the given parity.  A thread whose
-// phase is not complete yet is suspended (it issues nothing) until the phase
-// completes or about `suspend_ns` nanoseconds pass.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
-                                              uint32_t suspend_ns = 1000000u) {
+// phase is not complete yet may be suspended for a while (the hardware's own
+// time limit) before the answer is false; callers loop with a wall-time bound.
+// (An explicit suspend-time hint made the prefill slower: hand-offs between
+// warp roles wait on wake-ups.)
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return done != 0;
 }
