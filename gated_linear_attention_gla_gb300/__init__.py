@@ -21,7 +21,8 @@ from . import _binding
 from ._binding import (GLA_FLAG_FP32_IO, GLA_FLAG_FP32_OUT, GLA_FLAG_VECTOR_GATE,  # noqa: F401
                        GlaError, lib, status_string, version)
 
-__all__ = ["chunk_fwd", "chunk_bwd", "decode_step", "status_sync", "GlaError", "lib", "version",
+__all__ = ["chunk_fwd", "chunk_bwd", "decode_step", "status_sync", "set_wait_limit_ns", "GlaError",
+           "lib", "version",
            "GLA_FLAG_FP32_IO", "GLA_FLAG_FP32_OUT", "GLA_FLAG_VECTOR_GATE"]
 
 
@@ -279,6 +280,14 @@ def decode_step(q, k, v, g, state, scale: Optional[float] = None, out=None, stre
     if rc != 0:
         raise GlaError(rc, name)
     return out
+
+
+def set_wait_limit_ns(nanoseconds: int) -> int:
+    """Wall-time limit of the tensor-core prefill kernels' hand-off waits
+    (process-wide; 0 restores the default, 2 s).  Returns the previous setting.
+    A wait that runs out ends the kernel early: the next status_sync() raises
+    GlaError with GLA_ERR_TIMEOUT (5) and the call's outputs are undefined."""
+    return _binding.gla_set_wait_limit_ns(nanoseconds)
 
 
 def status_sync(stream=None) -> int:

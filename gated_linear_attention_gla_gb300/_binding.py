@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.gla_chunk_fwd_kernel.restype = ctypes.c_char_p
             L.gla_last_error_string.argtypes = []
             L.gla_last_error_string.restype = ctypes.c_char_p
+            L.gla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.gla_set_wait_limit_ns.restype = ctypes.c_uint64
             _lib = L
     return _lib
 
@@ -189,3 +191,8 @@ def chunk_fwd_kernel(dk, dv, chunk, flags):
 
 def gla_status_sync(stream) -> int:
     return lib().gla_status_sync(stream or None)
+
+
+def gla_set_wait_limit_ns(nanoseconds) -> int:
+    """Set the tensor-core kernels' hand-off wait limit (0: default); returns the previous one."""
+    return int(lib().gla_set_wait_limit_ns(int(nanoseconds)))

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -76,11 +77,24 @@ gla_status cuda_status(cudaError_t e) {
   return GLA_ERR_CUDA;
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{0};  // 0: the default
+
 }  // namespace
+
+namespace gla {
+uint64_t handoff_wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v != 0 ? v : kDefaultWaitLimitNs;
+}
+}  // namespace gla
 
 extern "C" {
 
 const char* gla_version(void) { return "0.1.0"; }
+
+uint64_t gla_set_wait_limit_ns(uint64_t nanoseconds) {
+  return g_wait_limit_ns.exchange(nanoseconds, std::memory_order_relaxed);
+}
 
 const char* gla_last_error_string(void) {
   if (g_last_text[0] != '\0') return g_last_text;

@@ -75,7 +75,7 @@ constexpr int kDVS = 64;       // value columns per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kMaskWarps = 4;
 constexpr int kStateWarps = 8;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitNs = kDefaultWaitLimitNs;  // the drains' limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWideSpan = 96.f;      // log2 chunk decay span above which a chunk is "wide"
 constexpr int kSlots = 3;              // gate ring: chunks c (mask), c + 1 (state), c + 2
@@ -137,6 +137,7 @@ struct TcParams {
   float* dot_out;
   float dot_sign;
   unsigned* status;
+  uint64_t wait_ns;  // limit of the hand-off waits (the drain keeps kWaitLimitNs)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -147,14 +148,15 @@ __device__ __forceinline__ uint32_t ph(int k) { return static_cast<uint32_t>(k) 
 // inline test, then an out-of-line loop (kept out of line to keep the
 // kernel's code small).
 __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity,
-                                           volatile int* abort_flag, unsigned* status) {
+                                           volatile int* abort_flag, unsigned* status,
+                                           uint64_t limit_ns) {
   if (*abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, kDevTimeout);
       return false;
@@ -162,12 +164,13 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity,
   }
 }
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
-                                         volatile int* abort_flag, unsigned* status) {
+                                         volatile int* abort_flag, unsigned* status,
+                                         uint64_t limit_ns) {
   if (!*abort_flag && mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, abort_flag, status);
+  return wait_bar_slow(bar, parity, abort_flag, status, limit_ns);
 }
 
-// On abort: wait (bounded) until the last of `issued` transactions counted on
+// Teardown: wait (bounded) until the last of `issued` transactions counted on
 // `bar` has landed, so that no copy into shared memory is in flight at exit.
 __device__ __forceinline__ void drain_bar(uint64_t* bar, int issued) {
   if (issued > 0) (void)mbar_wait_bounded(bar, (uint32_t)(issued - 1) & 1u, kWaitLimitNs);
@@ -296,7 +299,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (tid == 0) GLA_TRACE_POINT(0, 30, 0);
 
   auto wait = [&](int b, uint32_t parity) -> bool {
-    return wait_bar(&bars[b], parity, abort_flag, p.status);
+    return wait_bar(&bars[b], parity, abort_flag, p.status, p.wait_ns);
   };
   auto wait_w = [&](int b, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, wait(b, parity));
@@ -782,20 +785,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
   }
 
-  if (*abort_flag) {
-    // let every copy into this CTA's shared memory and every MMA land first
-    if (warp == 0 && lane == 0) {
-      for (int st = 0; st < 2; ++st) {
-        drain_bar(&bars[kQKFull0 + st], issued_qk[st]);
-        drain_bar(&bars[kVFull0 + st], issued_v[st]);
-      }
+  // Teardown, also after an abort: every copy into this CTA's shared memory and
+  // every MMA (with its commits' barrier arrivals) lands before the CTA ends.
+  if (warp == 0 && lane == 0) {
+    for (int st = 0; st < 2; ++st) {
+      drain_bar(&bars[kQKFull0 + st], issued_qk[st]);
+      drain_bar(&bars[kVFull0 + st], issued_v[st]);
     }
-    if (warp >= 1 && warp <= 3 && mma_issued) {
-      // the lane that issued this warp's MMAs commits them to the drain barrier
-      if (elect_one_sync()) mma_commit(&bars[kDrain + warp - 1]);
-      __syncwarp();
-      (void)mbar_wait_bounded(&bars[kDrain + warp - 1], 0u, kWaitLimitNs);
-    }
+  }
+  if (warp >= 1 && warp <= 3 && mma_issued) {
+    // the lane that issued this warp's MMAs commits them to the drain barrier
+    if (elect_one_sync()) mma_commit(&bars[kDrain + warp - 1]);
+    __syncwarp();
+    (void)mbar_wait_bounded(&bars[kDrain + warp - 1], 0u, kWaitLimitNs);
+  }
+  if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+    // a role that gave up may have left tensor-memory accesses unwaited
+    tmem_ld_wait();
+    tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
@@ -859,6 +866,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream) {
   p.final_state = a.final_state; p.cu_seqlens = a.cu_seqlens;
   p.B = a.B; p.H = a.H; p.T = a.T; p.DK = a.dk; p.DV = a.dv; p.nslices = a.dv / kDVS;
   p.status = a.status;
+  p.wait_ns = handoff_wait_limit_ns();
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   p.out_reversed = a.out_reversed;
   p.dot_rows = static_cast<const __nv_bfloat16*>(a.dot_rows);

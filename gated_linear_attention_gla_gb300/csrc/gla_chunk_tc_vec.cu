@@ -60,7 +60,7 @@ constexpr int kThreads = 512;  // 16 warps
 constexpr int kMaskWarps = 4;
 constexpr int kGateWarps = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitNs = kDefaultWaitLimitNs;  // the drains' limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWideSpan = 100.f;  // log2 span above which a chunk is processed token by token
 
@@ -91,7 +91,7 @@ constexpr uint32_t kColS = 384;   // 128: the running state, fp32
 enum Bar {
   kGFull = 0, kGEmpty, kQKFull, kQKEmpty, kVFull, kVEmpty, kScaled0, kScaled1, kSbReady,
   kAFull, kPFull0, kPFull1, kSFull, kOFull0, kOFull1, kOFree0, kOFree1, kAck0, kAck1,
-  kGateSync, kNumBars
+  kGateSync, kDrain, kNumBars
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
@@ -110,6 +110,7 @@ struct VecParams {
   int out_v8;        // out is 32-byte aligned: 256-bit stores
   int out_reversed;  // token t of a sequence stored at row len - 1 - t
   unsigned* status;
+  uint64_t wait_ns;  // limit of the hand-off waits (the drain keeps kWaitLimitNs)
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -176,7 +177,7 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
   extern __shared__ __align__(1024) uint8_t smem[];
   // the layout assumes a 1024-byte aligned base (the 128-byte swizzle atoms)
   if ((smem_u32(smem) & 1023u) != 0) {
-    if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+    if (threadIdx.x == 0) atomicOr(p.status, kDevLayout);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -224,12 +225,21 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
 
+  // a hand-off wait: gives up once the CTA is aborting, or after p.wait_ns
+  // (then it starts the abort)
   auto wait = [&](int b, uint32_t parity) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait_bounded(&bars[b], parity, kWaitLimitNs)) return true;
-    *abort_flag = 1;
-    atomicOr(p.status, kDevTimeout);
-    return false;
+    if (mbar_try_wait(&bars[b], parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait(&bars[b], parity)) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.wait_ns) {
+        *abort_flag = 1;
+        atomicOr(p.status, kDevTimeout);
+        return false;
+      }
+    }
   };
   // the same, decided for the whole warp (full-warp roles never split on a wait)
   auto wait_w = [&](int b, uint32_t parity) -> bool {
@@ -241,6 +251,11 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (lane == 0) mbar_arrive(&bars[b]);
   };
 
+  // the TMA transactions the producer started on kGFull, kQKFull, kVFull (one
+  // per chunk each), for the teardown drain
+  int issued_g = 0, issued_qk = 0, issued_v = 0;
+  bool mma_issued = false;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -250,6 +265,7 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (c >= 1 && !wait(kGEmpty, ph(c - 1))) break;
         mbar_arrive_expect_tx(&bars[kGFull], kGBytes);
         tma_load_4d(gsm, &tmG, &bars[kGFull], 0, h, row, bidx);
+        ++issued_g;
         if (c >= 1 && !wait(kQKEmpty, ph(c - 1))) break;
         mbar_arrive_expect_tx(&bars[kQKFull], 2 * kTile);
 #pragma unroll
@@ -257,11 +273,13 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
           tma_load_4d(smem + kOffQ + pn * kPanel, &tmQ, &bars[kQKFull], pn * 64, h, row, bidx);
           tma_load_4d(smem + kOffK + pn * kPanel, &tmK, &bars[kQKFull], pn * 64, h, row, bidx);
         }
+        ++issued_qk;
         if (c >= 1 && !wait(kVEmpty, ph(c - 1))) break;
         mbar_arrive_expect_tx(&bars[kVFull], kTile);
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn)
           tma_load_4d(smem + kOffV + pn * kPanel, &tmV, &bars[kVFull], pn * 64, h, row, bidx);
+        ++issued_v;
         // every tile is single-buffered, so chunk c + 1's loads can only be issued
         // once chunk c has released them: fetch its tiles into L2 now, so that
         // those loads then wait for L2 rather than HBM
@@ -280,22 +298,23 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Per tensor-core chunk (index n among them): MMA1, MMA3, MMA4, then MMA2.
-    if (lane == 0) {
-      const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
-      const uint64_t kd = sdesc_sw128(sbase + kOffK, 16, 1024);
-      const uint64_t kld = sdesc_sw128(sbase + kOffKlo, 16, 1024);
-      const uint64_t ktd = sdesc_sw128(sbase + kOffK, kPanel, 1024);    // Kt^T (MN-major)
-      const uint64_t ktld = sdesc_sw128(sbase + kOffKlo, kPanel, 1024);
-      const uint64_t sd = sdesc_sw128(sbase + kOffSb, kPanel, 1024);
-      const uint64_t vd = sdesc_sw128(sbase + kOffV, kPanel, 1024);
-      int n = 0;
-      for (int c = 0; c < nch; ++c) {
-        if (!wait(kScaled0 + (c & 1), ph(c >> 1))) break;
-        const bool wide = wide_ring[c & 3] != 0;
-        mbar_arrive(&bars[kAck0 + (c & 1)]);
-        if (wide) continue;  // processed by the gate group
-        const int ob = n & 1;
-        tc_fence_after();
+    // The whole warp waits and forms the descriptors; one elected lane issues.
+    const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
+    const uint64_t kd = sdesc_sw128(sbase + kOffK, 16, 1024);
+    const uint64_t kld = sdesc_sw128(sbase + kOffKlo, 16, 1024);
+    const uint64_t ktd = sdesc_sw128(sbase + kOffK, kPanel, 1024);    // Kt^T (MN-major)
+    const uint64_t ktld = sdesc_sw128(sbase + kOffKlo, kPanel, 1024);
+    const uint64_t sd = sdesc_sw128(sbase + kOffSb, kPanel, 1024);
+    const uint64_t vd = sdesc_sw128(sbase + kOffV, kPanel, 1024);
+    int n = 0;
+    for (int c = 0; c < nch; ++c) {
+      if (!wait_w(kScaled0 + (c & 1), ph(c >> 1))) break;
+      const bool wide = wide_ring[c & 3] != 0;
+      warp_arrive(kAck0 + (c & 1));
+      if (wide) continue;  // processed by the gate group
+      const int ob = n & 1;
+      tc_fence_after();
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
@@ -307,15 +326,22 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
           mma_bf16(tmem + kColA, desc_add(qd, off), desc_add(kld, off), kIdQK, 1);
         }
         mma_commit(&bars[kAFull]);
-        if (!wait(kSbReady, ph(n))) break;
-        if (n >= 2 && !wait(kOFree0 + ob, ph((n >> 1) - 1))) break;  // output(n-2) read O
-        tc_fence_after();
+      }
+      __syncwarp();
+      mma_issued = true;
+      if (!wait_w(kSbReady, ph(n))) break;
+      if (n >= 2 && !wait_w(kOFree0 + ob, ph((n >> 1) - 1))) break;  // output(n-2) read O
+      tc_fence_after();
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_bf16(tmem + kColO + ob * kD, desc_add(qd, (kk >> 2) * kPanel + (kk & 3) * 32),
                    desc_add(sd, kk * 2048), kIdQS, kk > 0);
-        if (!wait(kVFull, ph(c))) break;
-        tc_fence_after();
+      }
+      __syncwarp();
+      if (!wait_w(kVFull, ph(c))) break;
+      tc_fence_after();
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(tmem + kColS, desc_add(ktd, kk * 2048), desc_add(vd, kk * 2048), kIdKV, 1);
@@ -324,9 +350,12 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
           mma_bf16(tmem + kColS, desc_add(ktld, kk * 2048), desc_add(vd, kk * 2048), kIdKV, 1);
         mma_commit(&bars[kSFull]);    // S complete; S' no longer read
         mma_commit(&bars[kQKEmpty]);  // Q', Kt hi and lo no longer read
-        if (!wait(kPFull0 + ob, ph(n >> 1))) break;
-        tc_fence_after();
-        const uint32_t a_p = tmem + kColA;
+      }
+      __syncwarp();
+      if (!wait_w(kPFull0 + ob, ph(n >> 1))) break;
+      tc_fence_after();
+      const uint32_t a_p = tmem + kColA;
+      if (elect_one_sync()) {
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16_tmem_a(tmem + kColO + ob * kD, a_p + 8 * kk, desc_add(vd, kk * 2048), kIdPV, 1);
@@ -336,8 +365,9 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
                           kIdPV, 1);
         mma_commit(&bars[kOFull0 + ob]);
         mma_commit(&bars[kVEmpty]);  // V no longer read
-        ++n;
       }
+      __syncwarp();
+      ++n;
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ mask group
@@ -687,9 +717,23 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
   }
 
-  if (*abort_flag) {
-#pragma unroll 1
-    for (int i = 0; i < 1000; ++i) __nanosleep(1000);
+  // Teardown, also after an abort: every copy into this CTA's shared memory and
+  // every MMA (with its commits' barrier arrivals) lands before the CTA ends.
+  if (warp == 0 && lane == 0) {
+    if (issued_g > 0) (void)mbar_wait_bounded(&bars[kGFull], (issued_g - 1) & 1, kWaitLimitNs);
+    if (issued_qk > 0) (void)mbar_wait_bounded(&bars[kQKFull], (issued_qk - 1) & 1, kWaitLimitNs);
+    if (issued_v > 0) (void)mbar_wait_bounded(&bars[kVFull], (issued_v - 1) & 1, kWaitLimitNs);
+  }
+  if (warp == 1 && mma_issued) {
+    // the lane that issued the MMAs commits them to the drain barrier
+    if (elect_one_sync()) mma_commit(&bars[kDrain]);
+    __syncwarp();
+    (void)mbar_wait_bounded(&bars[kDrain], 0u, kWaitLimitNs);
+  }
+  if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+    // a role that gave up may have left tensor-memory accesses unwaited
+    tmem_ld_wait();
+    tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
@@ -751,6 +795,7 @@ cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream) {
   p.scale = a.scale; p.init_state = a.init_state; p.out = a.out;
   p.final_state = a.final_state; p.cu_seqlens = a.cu_seqlens;
   p.B = a.B; p.H = a.H; p.T = a.T; p.status = a.status;
+  p.wait_ns = handoff_wait_limit_ns();
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   p.out_reversed = a.out_reversed;
   const long long ctas = (long long)a.B * a.H;

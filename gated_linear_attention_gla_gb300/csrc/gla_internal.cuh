@@ -106,6 +106,12 @@ struct ChunkBwdArgs {
   unsigned* status;
 };
 
+// Wall-time limit of the tensor-core prefill kernels' hand-off waits, read at
+// each launch (process-wide; set by gla_set_wait_limit_ns, default 2 s).  Their
+// teardown drains keep the default.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+uint64_t handoff_wait_limit_ns();
+
 // Kernel launchers (one per translation unit).  They assume validated arguments
 // and a non-empty problem, and return the launch error.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -35,7 +35,7 @@
  *                    workspace, gla_chunk_bwd_fixed_workspace runs it on a
  *                    buffer of the library's own.
  *   gla_status_sync, gla_status_string, gla_last_error_string, gla_version,
- *   gla_chunk_fwd_kernel
+ *   gla_chunk_fwd_kernel, gla_set_wait_limit_ns
  *                    diagnostics.
  *
  * Conventions shared by every entry point
@@ -385,6 +385,22 @@ gla_status gla_status_sync(gla_stream_t stream);
  * GLA_ERR_UNSUPPORTED (thread-local storage, never NULL; "no error" if there
  * was none). */
 const char *gla_last_error_string(void);
+
+/*
+ * gla_set_wait_limit_ns -- the wall-time limit of the waits with which the
+ * warp roles of the tensor-core prefill kernels (gla_chunk_fwd, the mixer and
+ * backward calls that run them) hand chunks to one another; 0 restores the
+ * default, 2 s.  Process-wide, read at each launch; returns the previous
+ * setting (0 = the default).  A wait that runs out makes the kernel stop
+ * issuing work, let its own copies and matrix products land (with the default
+ * limit), release its tensor memory and return: gla_status_sync then reports
+ * GLA_ERR_TIMEOUT and the call's outputs are undefined.  For tests of that
+ * path: a limit shorter than a chunk's hand-offs (about a microsecond) makes
+ * the next call fail that way, and the call after the default is restored
+ * runs normally.  The pages have no counterpart (failure handling is the
+ * library's own).
+ */
+uint64_t gla_set_wait_limit_ns(uint64_t nanoseconds);
 
 /* Library version, "major.minor.patch". */
 const char *gla_version(void);

@@ -1,5 +1,6 @@
 """The C ABI library on the host: it builds, loads, exports every declared
 symbol, and rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
 import os
 import re
 
@@ -326,3 +327,14 @@ def test_chunk_fwd_mixer_rejects_before_launch(L):
     assert call(aug=FAKE[5]) == E.GLA_ERR_INVALID_ARG        # aug inside out
     assert call(q=FAKE[0] + 8) == E.GLA_ERR_MISALIGNED       # the prefill's own checks
     assert call(out=FAKE[0]) == E.GLA_ERR_INVALID_ARG
+
+
+def test_wait_limit_setting_round_trips(L):
+    """gla_set_wait_limit_ns is host-only: it returns the previous setting."""
+    L.gla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.gla_set_wait_limit_ns.restype = ctypes.c_uint64
+    old = L.gla_set_wait_limit_ns(12345)
+    try:
+        assert L.gla_set_wait_limit_ns(777) == 12345
+    finally:
+        assert L.gla_set_wait_limit_ns(old) == 777

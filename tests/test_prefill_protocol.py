@@ -15,6 +15,12 @@ pattern of "wide" chunks (the explicit-decay path):
   the barrier it waits for (it would then wait for a phase that has already
   passed and time out).
 
+TMA transactions and MMA commits are asynchronous: the barrier arrival lands
+later, in the order the role started them.  Each role that starts them drains
+them before the CTA ends, and a run may abort at any step (a bounded wait ran
+out): every role then gives up at its next wait and runs only its drain; the
+model checks that every role ends and that nothing is still in flight.
+
 The model must be kept in step with the kernel: a role's steps appear in the
 same order as in its source.  ``test_single_p_barrier_is_caught`` plants the
 mistake of an earlier revision (one P'-ready barrier instead of one per chunk
@@ -42,17 +48,18 @@ def kernel_roles(nch, wide, single_p_barrier=False):
 
     def producer():  # warp 0: TMA of chunks 0, 1 first; then per chunk gate sums, TMA (c >= 2)
         for c in range(min(2, nch)):
-            yield ("arrive", ("QKFull", c & 1))  # the TMA transaction completes it
-            yield ("arrive", ("VFull", c & 1))
+            yield ("async", ("QKFull", c & 1))  # the TMA transaction completes it
+            yield ("async", ("VFull", c & 1))
         for c in range(nch):
             if c >= K:
                 yield ("wait", ("GFree", c % K), c // K - 1)
             yield ("arrive", ("GReady", c % K))
             if c >= 2:
                 yield ("wait", ("QKEmpty", c & 1), (c >> 1) - 1)
-                yield ("arrive", ("QKFull", c & 1))
+                yield ("async", ("QKFull", c & 1))
                 yield ("wait", ("VEmpty", c & 1), (c >> 1) - 1)
-                yield ("arrive", ("VFull", c & 1))
+                yield ("async", ("VFull", c & 1))
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def issuer_a():  # warp 1: MMA1
         for c in range(nch):
@@ -60,8 +67,9 @@ def kernel_roles(nch, wide, single_p_barrier=False):
             yield ("wait", ("QKFull", st), c >> 1)
             if c >= 2:
                 yield ("wait", ("AFree", st), (c >> 1) - 1)
-            yield ("arrive", ("AFull", st))
-            yield ("arrive", ("QKEmpty", st))
+            yield ("async", ("AFull", st))
+            yield ("async", ("QKEmpty", st))
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def issuer_b():  # warp 2: MMA3, then MMA2
         for c in range(nch):
@@ -70,14 +78,15 @@ def kernel_roles(nch, wide, single_p_barrier=False):
             yield ("wait", ("SReady",), c)
             if c >= 2:
                 yield ("wait", ("OFree", st), (c >> 1) - 1)
-            yield ("arrive", ("O3Full", st))
-            yield ("arrive", ("SFree",))
-            yield ("arrive", ("QKEmpty", st))
+            yield ("async", ("O3Full", st))
+            yield ("async", ("SFree",))
+            yield ("async", ("QKEmpty", st))
             yield ("wait", pfull(c), pphase(c))
             yield ("wait", ("VFull", st), c >> 1)
-            yield ("arrive", ("OFull", st))
-            yield ("arrive", ("AFree", st))
-            yield ("arrive", ("VEmpty", st))
+            yield ("async", ("OFull", st))
+            yield ("async", ("AFree", st))
+            yield ("async", ("VEmpty", st))
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def issuer_c():  # warp 3: MMA4 into U of the chunk's parity
         for c in range(nch):
@@ -86,9 +95,10 @@ def kernel_roles(nch, wide, single_p_barrier=False):
             yield ("wait", ("VtFull",), c)
             if c >= 2:
                 yield ("wait", ("UFree", st), (c >> 1) - 1)
-            yield ("arrive", ("UFull", st))
-            yield ("arrive", ("VtFree",))
-            yield ("arrive", ("QKEmpty", st))
+            yield ("async", ("UFull", st))
+            yield ("async", ("VtFree",))
+            yield ("async", ("QKEmpty", st))
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def mask():  # warps 4..7: P' of chunk c, then the output of chunk c - 1
         for c in range(nch + 1):
@@ -155,13 +165,14 @@ def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
         for c in range(nch):
             if c >= 1:
                 yield ("wait", ("GEmpty",), c - 1)
-            yield ("arrive", ("GFull",))
+            yield ("async", ("GFull",))
             if c >= 1:
                 yield ("wait", ("QKEmpty",), c - 1)
-            yield ("arrive", ("QKFull",))
+            yield ("async", ("QKFull",))
             if c >= 1:
                 yield ("wait", ("VEmpty",), c - 1)
-            yield ("arrive", ("VFull",))
+            yield ("async", ("VFull",))
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def issuer():  # warp 1, lane 0: MMA1, MMA3, MMA4, MMA2 per tensor-core chunk
         n = 0
@@ -170,17 +181,18 @@ def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
             yield ("arrive", ("Ack", c & 1))
             if wide(c):
                 continue
-            yield ("arrive", ("AFull",))
+            yield ("async", ("AFull",))
             yield ("wait", ("SbReady",), n)
             if n >= 2:
                 yield ("wait", ("OFree", n & 1), (n >> 1) - 1)
             yield ("wait", ("VFull",), c)
-            yield ("arrive", ("SFull",))
-            yield ("arrive", ("QKEmpty",))
+            yield ("async", ("SFull",))
+            yield ("async", ("QKEmpty",))
             yield ("wait", ("PFull", n & 1), n >> 1)
-            yield ("arrive", ("OFull", n & 1))
-            yield ("arrive", ("VEmpty",))
+            yield ("async", ("OFull", n & 1))
+            yield ("async", ("VEmpty",))
             n += 1
+        yield ("drain",)  # its last copies / commits land before the CTA exits
 
     def mask():  # warps 4..7
         n, pending = 0, False
@@ -261,19 +273,55 @@ def vector_arrival_counts():
     return n
 
 
-def run_schedule(nch, wide, seed, vector=False, roles=None, need=None, **kw):
-    """Returns None when every role finishes, else a description of the fault."""
+def run_schedule(nch, wide, seed, vector=False, roles=None, need=None, abort_at=None,
+                 drain_on_abort=True, **kw):
+    """Returns None when every role finishes, else a description of the fault.
+
+    ("async", bar) steps are the TMA transactions and MMA commits a role starts:
+    the barrier arrival happens later, at a time the scheduler picks, in the
+    order the role started them (one thread's commits complete in order).
+    ("drain",) waits until the role's own started operations have all landed.
+    With ``abort_at``, a bounded wait runs out after that many scheduler steps:
+    from then on every role gives up at its next wait (as the kernels' waits do
+    once the abort flag is set) and runs only its teardown, a drain for the
+    roles that start asynchronous operations.  Every role must reach the end
+    with no operation of its own still in flight."""
     rnd = random.Random(seed)
     if roles is None:
         roles = (vector_kernel_roles if vector else kernel_roles)(nch, wide, **kw)
         need = vector_arrival_counts() if vector else arrival_counts()
     pending, done = defaultdict(int), defaultdict(int)
+    inflight = defaultdict(list)  # role -> barriers of its started operations, oldest first
     step = {n: next(g, None) for n, g in roles.items()}
     speed = {n: rnd.choice([0.02, 1.0, 1.0, 8.0]) for n in roles}
     in_bar_sync = set()
+    aborted, nsteps = False, 0
+
+    def arrive(bar):
+        pending[bar] += 1
+        if pending[bar] == need.get(bar, 1):
+            pending[bar] = 0
+            done[bar] += 1
+
+    def teardown(n):
+        if drain_on_abort:
+            yield ("drain",)
+
     while True:
+        if abort_at is not None and not aborted and nsteps >= abort_at:
+            aborted = True
+        if aborted:
+            for n in list(step):
+                s = step[n]
+                if s is not None and s[0] in ("wait", "bar_sync"):
+                    roles[n] = teardown(n)
+                    step[n] = next(roles[n], None)
+                    in_bar_sync.discard(n)
         live = [n for n in step if step[n] is not None]
+        landing = [n for n in inflight if inflight[n]]
         if not live:
+            if landing:
+                return "end with operations in flight: " + ", ".join(landing)
             return None
         if len(in_bar_sync) == STATE_WARPS:
             for n in in_bar_sync:
@@ -288,20 +336,29 @@ def run_schedule(nch, wide, seed, vector=False, roles=None, need=None, **kw):
                     return f"alias: {n} waits for phase {s[2]} of {s[1]}, {done[s[1]]} completed"
                 if done[s[1]] > s[2]:
                     ready.append(n)
-            elif s[0] == "arrive" or n not in in_bar_sync:
+            elif s[0] == "drain":
+                if not inflight[n]:
+                    ready.append(n)
+            elif s[0] in ("arrive", "async") or n not in in_bar_sync:
                 ready.append(n)
-        if not ready:
+        if not ready and not landing:
             return "deadlock: " + ", ".join(f"{n} at {step[n]}" for n in live)
-        n = rnd.choices(ready, weights=[speed[m] for m in ready])[0]
+        nsteps += 1
+        choices = ready + [("land", m) for m in landing]
+        weights = [speed[m] for m in ready] + [1.0] * len(landing)
+        pick = rnd.choices(choices, weights=weights)[0]
+        if isinstance(pick, tuple):
+            arrive(inflight[pick[1]].pop(0))
+            continue
+        n = pick
         s = step[n]
         if s[0] == "bar_sync":
             in_bar_sync.add(n)
             continue
         if s[0] == "arrive":
-            pending[s[1]] += 1
-            if pending[s[1]] == need.get(s[1], 1):
-                pending[s[1]] = 0
-                done[s[1]] += 1
+            arrive(s[1])
+        elif s[0] == "async":
+            inflight[n].append(s[1])
         step[n] = next(roles[n], None)
 
 
@@ -336,3 +393,24 @@ def test_single_p_barrier_is_caught():
     faults = [run_schedule(nch, WIDE_PATTERNS["none"], seed, single_p_barrier=True)
               for nch in range(2, 6) for seed in range(200)]
     assert any(f is not None and f.startswith("alias") and "PFull" in f for f in faults)
+
+
+@pytest.mark.parametrize("vector", [False, True], ids=["per_head", "per_key_channel"])
+def test_abort_drains_and_ends(vector):
+    """A wait that runs out at any point: every role ends, each with its own
+    copies and MMA commits landed (the drain), and none waits on another."""
+    for pattern in ("none", "odd"):
+        wide = WIDE_PATTERNS[pattern]
+        for nch in range(1, 7):
+            for seed in range(60):
+                abort_at = random.Random(1000 + seed).randrange(0, 40 * nch + 20)
+                fault = run_schedule(nch, wide, seed, vector=vector, abort_at=abort_at)
+                assert fault is None, f"{pattern}, {nch} chunks, seed {seed}, abort at {abort_at}: {fault}"
+
+
+def test_abort_without_drain_is_caught():
+    """The planted mistake: a teardown that only waits out a fixed time (no
+    drain) lets a CTA end with a copy or a commit still in flight."""
+    faults = [run_schedule(nch, WIDE_PATTERNS["none"], seed, abort_at=ab, drain_on_abort=False)
+              for nch in range(2, 5) for seed in range(40) for ab in (5, 15, 30)]
+    assert any(f is not None and f.startswith("end with operations in flight") for f in faults)
