@@ -314,7 +314,7 @@ SIDE_WORKLOADS = {
     "vector": ("chunk_tc_vec_kernel", "chunk_tc_vec_kernel.vector_b8_h16_t4096.md",
                "gla_chunk_tc_vec.cu"),
     "varlen": ("chunk_tc_kernel", None, "gla_chunk_tc.cu"),
-    "laplace": ("chunk_tc_kernel", None, "gla_chunk_tc.cu"),
+    "laplace": ("chunk_tc_kernel", "chunk_tc_kernel.laplace_b8_h16_t2048.md", "gla_chunk_tc.cu"),
 }
 
 
@@ -820,19 +820,29 @@ def run_profile_case(args):
         def call():
             gla.chunk_bwd(*bargs, **bkw)
         nbytes = 0
-    elif args.profile in ("prefill", "vector", "varlen"):
-        w = gla_inputs.WORKLOADS[args.profile]
+    elif args.profile in ("prefill", "vector", "varlen", "laplace", "fp32", "mixer"):
+        # fp32: the prefill workload with fp32 q, k, v, out (the CUDA-core kernel);
+        # mixer: the prefill workload with the mixer's steps after the readout
+        w = gla_inputs.WORKLOADS[args.profile if args.profile not in ("fp32", "mixer")
+                                 else "prefill"]
         x = gla_inputs.prefill_inputs(w)
         q, k, v, g = (x[n].to(dev) for n in ("q", "k", "v", "g"))
+        if args.profile == "fp32":
+            q, k, v = q.float(), k.float(), v.float()
         s0 = x["init_state"].to(dev) if x["init_state"] is not None else None
         cu = x["cu_seqlens"].to(dev) if x["cu_seqlens"] is not None else None
+        kw = dict(scale=x["scale"], init_state=s0, cu_seqlens=cu, chunk=w.chunk)
+        if args.profile == "mixer":
+            m = gla_inputs.mixer_inputs(w, q.shape[:-2])
+            kw["mixer"] = {n: (t.to(dev) if torch.is_tensor(t) else t) for n, t in m.items()}
 
         def call():
-            gla.chunk_fwd(q, k, v, g, scale=x["scale"], init_state=s0, cu_seqlens=cu,
-                          chunk=w.chunk)
+            gla.chunk_fwd(q, k, v, g, **kw)
         nseq = (len(x["cu_seqlens"]) - 1) if cu is not None else w.B
         rows = q.numel() // (w.H * w.dk)
         nbytes = prefill_bytes(w, nseq, 0, rows=rows)
+        if args.profile == "fp32":  # q, k, v and out in fp32: twice their bf16 bytes
+            nbytes += 2 * rows * w.H * (2 * w.dk + w.dv) + 2 * rows * w.H * w.dv
     else:
         w = gla_inputs.WORKLOADS["decode"]
         d = gla_inputs.decode_inputs(w, steps=1, N=args.decode_n)
@@ -904,8 +914,8 @@ def main(argv=None):
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--no-side-workloads", action="store_true",
                     help="skip timing the vector-gate and varlen prefill workloads")
-    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "decode", "backward",
-                                          "backward-tc"],
+    ap.add_argument("--profile", choices=["prefill", "vector", "varlen", "laplace", "fp32",
+                                          "mixer", "decode", "backward", "backward-tc"],
                     default=None,
                     help="run one kernel alone (for ncu captures) instead of the bench")
     ap.add_argument("--decode-n", type=int, default=1280,
