@@ -204,14 +204,20 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
 
   // bf16 I/O with chunk 128 runs on the tensor cores whenever that kernel covers
   // the shape; if it cannot be launched the call fails (no quiet substitution).
+  // The per-key-channel tensor-core kernel applies the mixer's steps itself
+  // (its CTAs own whole output rows); the other kernels are followed by the
+  // epilogue pass.
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (rows > 0 && gla::chunk_tc_supported(a))
+  bool mixed = false;
+  if (rows > 0 && gla::chunk_tc_supported(a)) {
     err = gla::launch_chunk_tc(a, s);
-  else if (rows > 0 && gla::chunk_tc_vec_supported(a))
-    err = gla::launch_chunk_tc_vec(a, s);
-  else
+  } else if (rows > 0 && gla::chunk_tc_vec_supported(a)) {
+    err = gla::launch_chunk_tc_vec(a, s, mixer);
+    mixed = mixer != nullptr;
+  } else {
     err = gla::launch_chunk_simt(a, s);
-  if (err == cudaSuccess && mixer && rows > 0) {
+  }
+  if (err == cudaSuccess && mixer && !mixed && rows > 0) {
     gla::EpilogueArgs e = *mixer;
     e.out = out; e.q = q; e.k = k; e.v = v; e.rows = rows; e.H = H; e.dk = dk; e.dv = dv;
     e.fp32_io = fp32; e.fp32_out = f32out;

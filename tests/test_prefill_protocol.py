@@ -156,11 +156,13 @@ def arrival_counts():
     return n
 
 
-def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
+def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2, mix=False):
     """The per-key-channel kernel.  Chunks the gate group finds "wide" are
     processed by it token by token (one group barrier per token) and skip the
     MMAs; the others run the tensor-core path.  The gate group's barrier is an
-    mbarrier whose phases the warps count themselves."""
+    mbarrier whose phases the warps count themselves.  With ``mix`` (the
+    mixer's steps inside the kernel) the mask warps read each chunk's Q' and
+    Kt rows and release the Q/K buffer too."""
     def producer():  # warp 0, lane 0
         for c in range(nch):
             if c >= 1:
@@ -202,6 +204,8 @@ def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
                 yield ("wait", ("Scaled", c & 1), c >> 1)
                 yield ("arrive", ("Ack", c & 1))
                 tc = not wide(c)
+                if mix:
+                    yield ("arrive", ("QKEmpty",))
                 if tc:
                     yield ("wait", ("AFull",), n)
                     yield ("arrive", ("PFull", n & 1))
@@ -265,8 +269,9 @@ def vector_kernel_roles(nch, wide, tokens_in_wide_chunk=2):
     return roles
 
 
-def vector_arrival_counts():
-    n = {("Scaled", 0): GATE_WARPS, ("Scaled", 1): GATE_WARPS, ("SbReady",): GATE_WARPS,
+def vector_arrival_counts(mix=False):
+    n = {("QKEmpty",): 1 + MASK_WARPS if mix else 1,
+         ("Scaled", 0): GATE_WARPS, ("Scaled", 1): GATE_WARPS, ("SbReady",): GATE_WARPS,
          ("GateSync",): GATE_WARPS, ("PFull", 0): MASK_WARPS, ("PFull", 1): MASK_WARPS,
          ("OFree", 0): MASK_WARPS, ("OFree", 1): MASK_WARPS,
          ("Ack", 0): 1 + MASK_WARPS, ("Ack", 1): 1 + MASK_WARPS}
@@ -289,7 +294,7 @@ def run_schedule(nch, wide, seed, vector=False, roles=None, need=None, abort_at=
     rnd = random.Random(seed)
     if roles is None:
         roles = (vector_kernel_roles if vector else kernel_roles)(nch, wide, **kw)
-        need = vector_arrival_counts() if vector else arrival_counts()
+        need = vector_arrival_counts(kw.get("mix", False)) if vector else arrival_counts()
     pending, done = defaultdict(int), defaultdict(int)
     inflight = defaultdict(list)  # role -> barriers of its started operations, oldest first
     step = {n: next(g, None) for n, g in roles.items()}
@@ -379,13 +384,14 @@ def test_protocol_has_no_deadlock_or_alias(pattern):
             assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
 
 
+@pytest.mark.parametrize("mix", [False, True], ids=["plain", "mixer"])
 @pytest.mark.parametrize("pattern", sorted(WIDE_PATTERNS) + ["first_two", "runs"])
-def test_vector_protocol_has_no_deadlock_or_alias(pattern):
+def test_vector_protocol_has_no_deadlock_or_alias(pattern, mix):
     extra = {"first_two": lambda c: c < 2, "runs": lambda c: (c // 3) % 2 == 1}
     wide = WIDE_PATTERNS.get(pattern) or extra[pattern]
     for nch in range(0, 9):
         for seed in range(120):
-            fault = run_schedule(nch, wide, seed, vector=True)
+            fault = run_schedule(nch, wide, seed, vector=True, mix=mix)
             assert fault is None, f"{nch} chunks, seed {seed}: {fault}"
 
 
