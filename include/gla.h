@@ -321,7 +321,11 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
  * GPU it uses, forward-only users included.  Once placed it stays until the
  * process exits.  The first call that needs it on a device looks up its
  * device address (cudaGetSymbolAddress) and caches it: make that first call
- * before capturing any stream into a CUDA graph.
+ * before capturing any stream into a CUDA graph.  If the buffer cannot be
+ * placed (not enough free memory when the module loads), the call returns
+ * GLA_ERR_CUDA with the runtime's reason in gla_last_error_string(), and the
+ * runtime's last-error state is cleared so that later calls are not charged
+ * with it.
  *
  * Sizes: a call whose workspace need (gla_chunk_bwd_workspace_size) exceeds
  * the buffer is rejected with GLA_ERR_UNSUPPORTED before anything is enqueued,
