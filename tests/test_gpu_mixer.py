@@ -210,3 +210,15 @@ def test_vector_mixer_packed(cuda_ok):
     o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
                                 init_state=x["init_state"], cu_seqlens=x["cu_seqlens"])
     _check_fused(o, y, o_ref, x, m, "all")
+
+
+@pytest.mark.parametrize("g_mu,g_div", [(2.0, 4.0), (-1.0, 1.0)], ids=["tensor_core", "wide"])
+def test_vector_mixer_bf16_output_is_the_fp32_result_rounded(cuda_ok, g_mu, g_div):
+    """The fused per-key-channel kernel computes the same fp32 values for either
+    output type and rounds them once for a bf16 output (tensor-core chunks and
+    wide chunks, which apply the steps in the token-by-token path)."""
+    from parity import check_bf16_rounding
+    x, m = _vector_case(seed=47, g_mu=g_mu, g_div=g_div)
+    _, y32 = _run_vector(x, m, torch.float32)
+    _, y16 = _run_vector(x, m, torch.bfloat16)
+    check_bf16_rounding(y16, y32)
