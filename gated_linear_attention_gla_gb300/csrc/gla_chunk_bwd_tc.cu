@@ -53,6 +53,9 @@ __device__ __forceinline__ void block_range(int len, int blk, int* t0, int* t1) 
 // Reversed copies of q, k, v, do (token t of a sequence to position len-1-t),
 // the gate shifted by one token (position tau holds g of natural token
 // len - tau, position 0 holds 0), S_0^T, dS_T / scale and its transpose.
+// The head sizes are template parameters so that the per-vector index
+// arithmetic divides by constants.
+template <int DK, int DV>
 __global__ void __launch_bounds__(kCopyThreads)
 bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ d_out,
@@ -62,7 +65,7 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                    __nv_bfloat16* __restrict__ rv, __nv_bfloat16* __restrict__ rdo,
                    float* __restrict__ rg, float* __restrict__ s0t, float* __restrict__ dfs,
                    float* __restrict__ dfst, const int32_t* __restrict__ cu, int B, int H,
-                   int T, int DK, int DV, unsigned* status) {
+                   int T, unsigned* status) {
   int s, h, blk;
   pair_and_block(H, &s, &h, &blk);
   long long start;
@@ -72,8 +75,8 @@ bwd_tc_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   block_range(len, blk, &t0, &t1);
   // 16-byte vectors: a token's q and k rows (DK / 8 each), then its v and do
   // rows (DV / 8 each); eight vectors a thread in flight at a time
-  const int VK = DK / 8, VV = DV / 8;
-  const int VPT = 2 * VK + 2 * VV;
+  constexpr int VK = DK / 8, VV = DV / 8;
+  constexpr int VPT = 2 * VK + 2 * VV;
   constexpr int kBatch = 8;
   // vector c of a token: its tensor (0 q, 1 k, 2 v, 3 do), index in the row, row width
   auto which = [&](int c, int* w, int* e, int* width) {
@@ -380,11 +383,13 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, void* workspace, cudaStre
   auto fl = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
   const unsigned grid = (unsigned)((long long)a.B * a.H * kBlocksPerPair);
 
-  bwd_tc_prep_kernel<<<grid, kCopyThreads, 0, stream>>>(
+  auto prep = DK == 64 ? (DV == 64 ? bwd_tc_prep_kernel<64, 64> : bwd_tc_prep_kernel<64, 128>)
+                       : (DV == 64 ? bwd_tc_prep_kernel<128, 64> : bwd_tc_prep_kernel<128, 128>);
+  prep<<<grid, kCopyThreads, 0, stream>>>(
       (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
       (const __nv_bfloat16*)a.d_out, a.g, 1.f / a.scale, a.init_state, a.d_final, bf(w.rq),
       bf(w.rk), bf(w.rv), bf(w.rdo), fl(w.rg), fl(w.s0t), fl(w.dfs), fl(w.dfst), a.cu_seqlens,
-      a.B, a.H, a.T, DK, DV, a.status);
+      a.B, a.H, a.T, a.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
