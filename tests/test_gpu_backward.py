@@ -316,9 +316,10 @@ def test_tc_strong_decays_take_the_wide_path():
     three prefill runs, forward and reversed.  As for the CUDA-core path, the
     reference is the oracle at max(g, -30).  dg is then ~1e-4 of its per-token
     terms x_t = sum_i (q dq - k dk), and its error is the suffix sum of those
-    terms' own errors (the gradients' bf16-level ~1e-2 at most, a few 1e-3
-    typically): a random walk over up to T tokens, held to
-    1e-2 sqrt(T) RMS(x) (measured 5.2e-2 RMS(x) at T = 300, bound 0.17)."""
+    terms' own errors.  With the prefill's hi + lo operands the gradients are
+    within ~4e-5 of their RMS, and the measured dg error is 1.0e-3 RMS(x) at
+    T = 300 (it was 5.2e-2 with operands rounded once); the bound is three
+    times the measurement."""
     T = 300
     x, gr = inputs(B=1, T=T, H=2, g_mu=-2.0, g_div=0.05)
     xc = dict(x, g=x["g"].clamp(min=-30.0))
@@ -329,7 +330,7 @@ def test_tc_strong_decays_take_the_wide_path():
     err = float(np.max(np.abs(to_np(got[3]) - ref[3])))
     scale_x = float(np.sqrt(np.mean(terms * terms)))
     print(f"tc strong dg: max err {err / scale_x:.2e} RMS(x)")
-    assert err <= 1e-2 * np.sqrt(T) * scale_x
+    assert err <= 3e-3 * scale_x
 
 
 def test_tc_minus_inf_gate_resets():
