@@ -33,15 +33,19 @@ pytestmark = pytest.mark.gpu
 
 TOL_GRAD = 1e-4
 TOL_DG = 1e-3
-# tensor-core path: the prefill kernel's accuracy (bf16 operands, fp32
-# accumulation), the bf16 output tolerance applied to fp32 results
+# tensor-core paths.  The per-key-channel dv run (its prefill rounds P' once
+# off the diagonal blocks): the bf16 output tolerance applied to fp32 results.
 TOL_GRAD_TC = 2e-2
-# dg on that path is a suffix sum over up to T tokens of 128-channel dot
-# products of the inputs with those gradients: the per-term errors add up
-# along the suffix like the terms themselves, so the relative error stays near
-# the gradients' but its maximum over a long sequence grows (2.3e-2 measured at
-# T = 2048): 5e-2
-TOL_DG_TC = 5e-2
+# The per-head path (three runs of the per-head prefill, whose S', P' and W V
+# enter as bf16 hi + lo): gradients measured within 4.5e-5 of their RMS on
+# every case below, dg within 1.8e-4 (a suffix sum over up to T tokens of
+# 128-channel dot products; full size, T = 2048); bounds about five times the
+# measurements.
+TOL_GRAD_TC_HEAD = 3e-4
+TOL_DG_TC = 1e-3
+# strong decays: the reference is the oracle at the clamped gate, and d_init
+# (the gradient through the first token's decay) measured 1.3e-3 there
+TOL_GRAD_TC_STRONG = 5e-3
 
 
 def _gla():
@@ -234,7 +238,7 @@ def test_tc_per_key_channel_gate_packed_and_full_size():
 def test_tc_backward_matches_oracle():
     x, gr = inputs(B=2, T=300, H=3)   # two full 128-token chunks and a ragged tail
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label="tc")
 
 
 def test_tc_bf16_gradients_are_the_fp32_ones_rounded():
@@ -249,7 +253,7 @@ def test_tc_bf16_gradients_are_the_fp32_ones_rounded():
 def test_tc_packed_with_empty_and_short_sequences():
     x, gr = inputs("varlen", lengths=[300, 0, 1, 129, 128, 5], H=2)
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc packed")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label="tc packed")
     # the empty sequence hands d_final through (as (d_final / scale) * scale)
     torch.testing.assert_close(got[4][1].cpu(), gr["d_final_state"][1], rtol=1e-6, atol=0)
 
@@ -257,7 +261,7 @@ def test_tc_packed_with_empty_and_short_sequences():
 def test_tc_optional_inputs_and_outputs_left_out():
     x, gr = inputs(B=2, T=200, H=2)
     got = run_gpu(x, gr, grad_dtype=torch.float32, init=False, final=False, tc=True)
-    check(got, run_ref(x, gr, init=False, final=False), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC,
+    check(got, run_ref(x, gr, init=False, final=False), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC,
           label="tc no init/final")
     dq, dk, dv, dg, d0 = run_gpu(x, gr, grad_dtype=torch.float32, need_dg=False,
                                  need_d_init=False, init=False, final=False, tc=True)
@@ -270,14 +274,14 @@ def test_tc_full_size():
     path: every element of every gradient against the oracle."""
     x, gr = inputs()
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc full size")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label="tc full size")
 
 
 @pytest.mark.parametrize("T", [1, 127, 128, 129, 256])
 def test_tc_chunk_boundaries(T):
     x, gr = inputs(B=2, T=T, H=2)
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label=f"tc T={T}")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label=f"tc T={T}")
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
@@ -288,7 +292,7 @@ def test_tc_head_sizes_64(dk, dv):
     empty one and a ragged tail, fp32 and bf16 gradients."""
     x, gr = inputs("varlen", lengths=[300, 0, 129, 1], H=3, dk=dk, dv=dv)
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label=f"tc {dk}x{dv}")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label=f"tc {dk}x{dv}")
     g16 = run_gpu(x, gr, tc=True)
     for a, b in zip(g16[:3], got[:3]):
         assert a.dtype == torch.bfloat16 and torch.equal(a, b.to(torch.bfloat16))
@@ -300,7 +304,8 @@ def test_tc_head_size_64_strong_decays():
     x, gr = inputs(B=1, T=300, H=2, dk=64, dv=64, g_mu=-2.0, g_div=0.05)
     xc = dict(x, g=x["g"].clamp(min=-30.0))
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got[:3] + (None,) + got[4:], run_ref(xc, gr), tol=TOL_GRAD_TC, label="tc 64 strong")
+    check(got[:3] + (None,) + got[4:], run_ref(xc, gr), tol=TOL_GRAD_TC_STRONG,
+          label="tc 64 strong")
 
 
 def test_tc_zero_gate():
@@ -308,7 +313,7 @@ def test_tc_zero_gate():
     x, gr = inputs(B=1, T=200, H=2)
     x["g"] = torch.zeros_like(x["g"])
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(x, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc g=0")
+    check(got, run_ref(x, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label="tc g=0")
 
 
 def test_tc_strong_decays_take_the_wide_path():
@@ -325,7 +330,7 @@ def test_tc_strong_decays_take_the_wide_path():
     xc = dict(x, g=x["g"].clamp(min=-30.0))
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
     ref = run_ref(xc, gr)
-    check(got[:3] + (None,) + got[4:], ref, tol=TOL_GRAD_TC, label="tc strong")
+    check(got[:3] + (None,) + got[4:], ref, tol=TOL_GRAD_TC_STRONG, label="tc strong")
     terms = (to_np(x["q"]) * ref[0] - to_np(x["k"]) * ref[1]).sum(-1)
     err = float(np.max(np.abs(to_np(got[3]) - ref[3])))
     scale_x = float(np.sqrt(np.mean(terms * terms)))
@@ -340,7 +345,7 @@ def test_tc_minus_inf_gate_resets():
     x["g"][0, 130, :] = float("-inf")
     xc = dict(x, g=x["g"].clamp(min=-30.0))
     got = run_gpu(x, gr, grad_dtype=torch.float32, tc=True)
-    check(got, run_ref(xc, gr), tol=TOL_GRAD_TC, tol_dg=TOL_DG_TC, label="tc -inf")
+    check(got, run_ref(xc, gr), tol=TOL_GRAD_TC_HEAD, tol_dg=TOL_DG_TC, label="tc -inf")
 
 
 def test_tc_per_key_channel_strong_decays():
