@@ -366,3 +366,8 @@ def test_full_size_workload(cuda_ok, name):
           f"final state {e_s:.3e}")
     assert e_o <= out_tol(torch.bfloat16), f"output error {e_o:.3e}"
     assert e_s <= TOL_STATE, f"state error {e_s:.3e}"
+    if name != "vector":
+        # the per-head kernel's S', P' and W V enter as bf16 hi + lo: measured
+        # 3.0e-5 .. 5.6e-5 (output) and 2.2e-5 .. 3.0e-5 (state); a regression
+        # to operands rounded once (2.5e-2 here) fails these
+        assert e_o <= 3e-4 and e_s <= 3e-4, (e_o, e_s)
