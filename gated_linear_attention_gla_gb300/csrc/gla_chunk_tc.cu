@@ -576,7 +576,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (!wait_w(kOFull0 + b, ph(c >> 1))) return false;  // MMA2(c)
       tc_fence_after();
-#pragma unroll 1
       if (warp == 4 && lane == 0) GLA_TRACE_POINT(0, 9, c);
       for (int part = 0; part < 2; ++part) {
         uint32_t v[32];

@@ -222,3 +222,16 @@ def test_vector_mixer_bf16_output_is_the_fp32_result_rounded(cuda_ok, g_mu, g_di
     _, y32 = _run_vector(x, m, torch.float32)
     _, y16 = _run_vector(x, m, torch.bfloat16)
     check_bf16_rounding(y16, y32)
+
+
+def test_vector_mixer_full_size(cuda_ok):
+    """The fused per-key-channel mixer on the whole full-size vector workload
+    (B=8, T=4096, H=16), every element: its composite against the exact one,
+    next to the two-step composite of the same kernel's plain readout."""
+    w = gla_inputs.WORKLOADS["vector"]
+    x = gla_inputs.prefill_inputs(w)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2])
+    o, y = _run_vector(x, m, torch.float32)
+    o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                init_state=x["init_state"])
+    _check_fused(o, y, o_ref, x, m, "all")
