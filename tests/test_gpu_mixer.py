@@ -1,7 +1,8 @@
 """The mixer's steps after the readout (self-augmentation, head RMSNorm, SiLU
 output gate) on the GPU, against the fp64 oracle: after every prefill kernel
-(gla_chunk_fwd_mixer: the prefill, then a pass over its output) and fused into
-the decode step.
+(gla_chunk_fwd_mixer: inside the per-key-channel kernel; a pass over the
+output after the per-head and CUDA-core kernels) and fused into the decode
+step.
 
 The check is split in two.  The readout o itself must match the oracle within
 the output tolerance (as everywhere); the epilogue, applied by the GPU to that
@@ -235,3 +236,72 @@ def test_vector_mixer_full_size(cuda_ok):
     o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
                                 init_state=x["init_state"])
     _check_fused(o, y, o_ref, x, m, "all")
+
+
+def _per_head_case(seed=51, w="prefill", **over):
+    w = gla_inputs.WORKLOADS[w]
+    kw = dict(B=2, T=300, H=4)
+    kw.update(over)
+    x = gla_inputs.prefill_inputs(w, seed=seed, **kw)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2], seed=seed, H=kw["H"])
+    return x, m
+
+
+def _run_per_head(x, m):
+    """The per-head kernel's plain readout and its mixer call (the kernel, then
+    the pass over its output), fp32 outputs, and the oracle's readout."""
+    gla = _gla()
+    mix = {k: cuda(v) if torch.is_tensor(v) else v for k, v in m.items()}
+    args = (cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["g"]))
+    kw = dict(scale=x["scale"], init_state=cuda(x["init_state"]), chunk=128,
+              out_dtype=torch.float32)
+    if x["cu_seqlens"] is not None:
+        kw["cu_seqlens"] = cuda(x["cu_seqlens"])
+    o, _ = gla.chunk_fwd(*args, **kw)
+    y, _ = gla.chunk_fwd(*args, mixer=mix, **kw)
+    gla.status_sync()
+    o_ref, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["scale"],
+                                init_state=x["init_state"], cu_seqlens=x["cu_seqlens"])
+    return o, y, o_ref
+
+
+def _check_two_step(o, y, o_ref, x, m):
+    assert rel_max(to_np(o), o_ref) <= out_tol(torch.bfloat16)
+    e = rel_max(to_np(y), _ref_epilogue(to_np(o), x, m, "all"))
+    assert e <= 1e-5, f"epilogue error {e:.3e}"
+
+
+@pytest.mark.parametrize("mu", [-3.0, 8.0], ids=["wide", "weak"])
+def test_per_head_mixer_strong_and_weak_decay(cuda_ok, mu):
+    """g = logsigmoid(N(mu, 1)): mu = -3 makes every chunk "wide" (the explicit
+    decays), mu = 8 keeps nearly all memory."""
+    x, m = _per_head_case()
+    gen = torch.Generator().manual_seed(53)
+    x["g"] = torch.nn.functional.logsigmoid(torch.randn(x["g"].shape, generator=gen) + mu)
+    _check_two_step(*_run_per_head(x, m), x, m)
+
+
+def test_per_head_mixer_packed(cuda_ok):
+    """Packed sequences, an empty one and a one-token one among them."""
+    x, m = _per_head_case(lengths=[300, 0, 1, 129], H=2)
+    _check_two_step(*_run_per_head(x, m), x, m)
+
+
+def test_per_head_mixer_zero_scale(cuda_ok):
+    """scale = 0: the readout is exactly zero and the steps still apply (the
+    self-augmentation term alone reaches the output)."""
+    x, m = _per_head_case(seed=55)
+    x["scale"] = 0.0
+    o, y, o_ref = _run_per_head(x, m)
+    assert float(o.abs().max()) == 0.0
+    _check_two_step(o, y, o_ref, x, m)
+
+
+@pytest.mark.parametrize("wname", ["prefill", "laplace"])
+def test_per_head_mixer_full_size(cuda_ok, wname):
+    """The per-head kernel and the pass on the whole full-size workload, every
+    element."""
+    w = gla_inputs.WORKLOADS[wname]
+    x = gla_inputs.prefill_inputs(w)
+    m = gla_inputs.mixer_inputs(w, x["q"].shape[:-2])
+    _check_two_step(*_run_per_head(x, m), x, m)
