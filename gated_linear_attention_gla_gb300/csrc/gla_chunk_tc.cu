@@ -626,7 +626,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float* slot = slot_of(c);
         const float ar = slot[r];
         const bool wide = slot[129] != 0.f;
-        f = wide ? 1.f : (ar != 0.f ? 1.f / ar : 0.f);
         if (!wait_w(kAFull0 + b, ph(c >> 1))) break;
         tc_fence_after();
         const uint32_t a_row = tmem + lane_off + kColA + b * 128;
@@ -657,6 +656,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(kPFull0 + b);
+        // the row factor of this chunk's output (written next iteration), off
+        // the path from the A wait to P'-ready
+        f = wide ? 1.f : (ar != 0.f ? 1.f / ar : 0.f);
         if (warp == 4 && lane == 0) GLA_TRACE_POINT(0, 8, c);
       }
       if (c >= 1 && !output(c - 1, fprev)) break;
