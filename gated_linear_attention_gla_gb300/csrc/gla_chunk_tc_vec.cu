@@ -122,6 +122,15 @@ struct VecParams {
 
 // logistic sigmoid and SiLU with the fast exponential and reciprocal (the
 // mixer's gate runs once per output element; 1 / inf = 0 gives the limits)
+// 2^x by the hardware approximation (PTX ex2.approx.ftz): for the operand
+// scaling, whose exponents stay within [-100, 100] on the tensor-core chunks, so
+// that no result is subnormal; it gives the same bits as exp2f there and skips
+// exp2f's handling of the ranges outside.
+__device__ __forceinline__ float ex2_(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
@@ -832,7 +841,7 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
         // pass 2: Q' = q exp(G - G_L) in place, Kt = k exp(G_L - G) as hi (in
         // place) + lo; rows past the sequence end are zeroed
         float G0 = off0 * kLog2e, G1 = off1 * kLog2e;
-#pragma unroll 4
+#pragma unroll 8
         for (int t = 32 * rg; t < 32 * rg + 32; ++t) {
           const uint32_t eo = pair_offset(t, pr);
           uint32_t qo = 0u, kh = 0u, kl = 0u;
@@ -842,8 +851,8 @@ chunk_tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ,
             G1 += fmaxf(gv.y, -kGateClamp) * kLog2e;
             const uint32_t qraw = *reinterpret_cast<const uint32_t*>(smem + kOffQ + eo);
             const uint32_t kraw = *reinterpret_cast<const uint32_t*>(smem + kOffK + eo);
-            qo = pack_bf16x2(bf16lo(qraw) * exp2f(G0 - GL0), bf16hi(qraw) * exp2f(G1 - GL1));
-            const float k0 = bf16lo(kraw) * exp2f(GL0 - G0), k1 = bf16hi(kraw) * exp2f(GL1 - G1);
+            qo = pack_bf16x2(bf16lo(qraw) * ex2_(G0 - GL0), bf16hi(qraw) * ex2_(G1 - GL1));
+            const float k0 = bf16lo(kraw) * ex2_(GL0 - G0), k1 = bf16hi(kraw) * ex2_(GL1 - G1);
             kh = pack_bf16x2(k0, k1);
             kl = pack_bf16x2(k0 - bf16lo(kh), k1 - bf16hi(kh));
           }
